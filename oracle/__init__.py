@@ -1,0 +1,240 @@
+"""fp64 CPU oracle for the batched Gated-DeltaNet decode step.
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference leg import this package. The CUDA product
+path never imports, links or calls it, and this package never touches the CUDA
+library.
+
+Contents:
+  * ``gdn_oracle.c`` -- the recurrence in plain C, fp64, OpenMP over
+    (request, head): short conv + SiLU, L2 normalisation, the dense gated
+    delta-rule step and the DeltaLog base+log emulation. Built with gcc by
+    :func:`build`, loaded with ctypes.
+  * ``chunked.py``   -- numpy fp64 chunkwise forms (gated linear attention
+    with a decay mask; the WY/UT form of the gated delta rule) used only to
+    pin the recurrence against an independent algorithm.
+
+Parity: every function here is pinned by a ``-m "not gpu"`` test in
+``tests/test_oracle_pins.py`` (worked example printed on the pages, closed
+forms, invariants, an independent chunked algorithm, brute force on tiny
+inputs).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gdn_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libgdn_oracle.so")
+
+# Flags understood by orc_step_batch (oracle-local values).
+CONV = 1
+L2NORM = 2
+PLAIN = 4
+GATE_RAW = 8
+KLOG_PRENORM = 16
+
+ERRORS = {0: "ok", 1: "bad argument", 2: "slot out of range", 3: "log length out of range"}
+
+
+class OrcCfg(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int32),
+        ("num_heads", ctypes.c_int32),
+        ("dk", ctypes.c_int32),
+        ("dv", ctypes.c_int32),
+        ("num_slots", ctypes.c_int32),
+        ("dlam", ctypes.c_int32),
+        ("log_capacity", ctypes.c_int32),
+        ("flags", ctypes.c_uint32),
+        ("q_scale", ctypes.c_double),
+        ("l2_eps", ctypes.c_double),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False, src: str | None = None, out_path: str | None = None) -> str:
+    """Compile gdn_oracle.c with gcc (-O2 -fopenmp, no fast-math); returns the library path.
+
+    ``src``/``out_path`` let a test compile a copy of the source with a planted
+    mistake, to show that the pins catch it.
+    """
+    src = src or _SRC
+    path = out_path or _LIB_PATH
+    if not force and os.path.exists(path) and os.path.getmtime(path) >= os.path.getmtime(src):
+        return path
+    os.makedirs(os.path.dirname(path), exist_ok=True)
+    tmp = path + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-shared", "-fPIC", "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, path)
+    return path
+
+
+def _declare(lib):
+    dp = ctypes.POINTER(ctypes.c_double)
+    ip = ctypes.POINTER(ctypes.c_int32)
+    lib.orc_num_threads.restype = ctypes.c_int
+    lib.orc_conv1d_silu.argtypes = [ctypes.c_int, dp, dp, dp, dp, dp]
+    lib.orc_conv1d_silu.restype = None
+    lib.orc_l2norm.argtypes = [ctypes.c_int, dp, ctypes.c_double, ctypes.c_double, dp]
+    lib.orc_l2norm.restype = ctypes.c_double
+    lib.orc_gdn_step.argtypes = [ctypes.c_int, ctypes.c_int, dp, dp, dp, dp, dp, ctypes.c_int,
+                                 ctypes.c_double, ctypes.c_int, dp]
+    lib.orc_gdn_step.restype = None
+    lib.orc_deltalog_step.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      dp, dp, dp, dp, dp, ip, dp, dp, dp, dp, ctypes.c_double,
+                                      ctypes.c_int, dp, ctypes.c_double, dp]
+    lib.orc_deltalog_step.restype = ctypes.c_int
+    lib.orc_step_batch.argtypes = [ctypes.POINTER(OrcCfg), ctypes.c_int, ip] + [dp] * 3 + \
+        [dp] * 4 + [dp, dp] + [dp] * 5 + [ip, dp]
+    lib.orc_step_batch.restype = ctypes.c_int
+    return lib
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) the oracle library."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            _lib = _declare(ctypes.CDLL(build()))
+        return _lib
+
+
+def _f64(a):
+    if a is None:
+        return None
+    assert isinstance(a, np.ndarray) and a.dtype == np.float64 and a.flags.c_contiguous, \
+        "oracle arrays must be C-contiguous float64"
+    return a
+
+
+def _ptr(a, ctype=ctypes.c_double):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def num_threads(lib=None) -> int:
+    return (lib or load()).orc_num_threads()
+
+
+def conv1d_silu(x, conv_state, w, bias=None, lib=None):
+    """One token of the width-4 causal conv + SiLU; ``conv_state`` [nch,3] is updated."""
+    lib = lib or load()
+    x, conv_state, w, bias = map(_f64, (x, conv_state, w, bias))
+    y = np.empty_like(x)
+    lib.orc_conv1d_silu(x.size, _ptr(x), _ptr(conv_state), _ptr(w), _ptr(bias), _ptr(y))
+    return y
+
+
+def l2norm(x, eps, scale=1.0, lib=None):
+    lib = lib or load()
+    x = _f64(np.ascontiguousarray(x, dtype=np.float64))
+    y = np.empty_like(x)
+    inv = lib.orc_l2norm(x.size, _ptr(x), float(eps), float(scale), _ptr(y))
+    return y, inv
+
+
+def gdn_step(S, q, k, v, lam, beta, plain=False, lib=None):
+    """One dense step on a single head; ``S`` [dk,dv] float64 is updated, returns o [dv]."""
+    lib = lib or load()
+    S, q, k, v, lam = map(_f64, (S, q, k, v, np.ascontiguousarray(lam, dtype=np.float64)))
+    dk, dv = S.shape
+    o = np.empty(dv)
+    lib.orc_gdn_step(dk, dv, _ptr(S), _ptr(q), _ptr(k), _ptr(v), _ptr(lam), lam.size,
+                     float(beta), int(plain), _ptr(o))
+    return o
+
+
+class HeadLog:
+    """DeltaLog physical state of one head (fp64): base, ell, K/U/Lambda logs, length."""
+
+    def __init__(self, dk, dv, C, dlam, base=None):
+        self.base = np.zeros((dk, dv)) if base is None else np.array(base, dtype=np.float64)
+        self.ell = np.zeros(dlam)
+        self.klog = np.zeros((max(C, 1), dk))
+        self.ulog = np.zeros((max(C, 1), dv))
+        self.lam = np.zeros((max(C, 1), dlam))
+        self.length = np.zeros(1, dtype=np.int32)
+        self.C, self.dlam = C, dlam
+
+    def logical_state(self):
+        """Eq. (7) of the DeltaLog notes, written out."""
+        e = self.ell if self.dlam > 1 else np.full(self.base.shape[0], self.ell[0])
+        S = np.exp(e)[:, None] * self.base
+        for i in range(int(self.length[0])):
+            li = self.lam[i] if self.dlam > 1 else np.full(self.base.shape[0], self.lam[i, 0])
+            S = S + (np.exp(e - li) * self.klog[i])[:, None] * self.ulog[i][None, :]
+        return S
+
+
+def deltalog_step(st: HeadLog, q, k, v, lam, beta, plain=False, a=None, bscale=1.0, lib=None):
+    """One DeltaLog step (append if L < C on entry, else merge) on a single head."""
+    lib = lib or load()
+    q, k, v = map(_f64, (q, k, v))
+    lam = _f64(np.ascontiguousarray(lam, dtype=np.float64))
+    a = k if a is None else _f64(a)
+    dk, dv = st.base.shape
+    o = np.empty(dv)
+    rc = lib.orc_deltalog_step(dk, dv, st.dlam, st.C, _ptr(st.base), _ptr(st.ell), _ptr(st.klog),
+                               _ptr(st.ulog), _ptr(st.lam), _ptr(st.length, ctypes.c_int32),
+                               _ptr(q), _ptr(k), _ptr(v), _ptr(lam), float(beta), int(plain),
+                               _ptr(a), float(bscale), _ptr(o))
+    if rc != 0:
+        raise ValueError(f"oracle deltalog_step: {ERRORS.get(rc, rc)}")
+    return o
+
+
+class BatchState:
+    """Slot-indexed pools (fp64) mirroring the GPU layout, for whole-batch steps."""
+
+    def __init__(self, num_slots, H, dk, dv, dlam=1, C=0, nch=None):
+        self.S = np.zeros((num_slots, H, dk, dv))
+        self.ell = np.zeros((num_slots, H, dlam))
+        c = max(C, 1)
+        self.klog = np.zeros((num_slots, H, c, dk))
+        self.ulog = np.zeros((num_slots, H, c, dv))
+        self.lamlog = np.zeros((num_slots, H, c, dlam))
+        self.len = np.zeros((num_slots, H), dtype=np.int32)
+        nch = nch if nch is not None else 2 * H * dk + H * dv
+        self.conv = np.zeros((num_slots, nch, 3))
+
+
+def step_batch(cfg: dict, mode: str, st: BatchState, slot, *, q=None, k=None, v=None,
+               mixed=None, conv_w=None, conv_b=None, lam=None, beta=None, o=None, lib=None):
+    """One decode step for a whole batch. ``mode`` is 'dense' or 'deltalog'.
+
+    ``cfg`` keys: batch, num_heads, dk, dv, num_slots, dlam, log_capacity, flags,
+    q_scale, l2_eps. Inputs are float64 arrays in the layouts documented in
+    gdn_oracle.c; returns o [B,H,dv] (rows of padding requests stay as given).
+    """
+    lib = lib or load()
+    c = OrcCfg(cfg["batch"], cfg["num_heads"], cfg["dk"], cfg["dv"], cfg["num_slots"],
+               cfg.get("dlam", 1), cfg.get("log_capacity", 0), cfg.get("flags", 0),
+               cfg.get("q_scale", 1.0), cfg.get("l2_eps", 1e-6))
+    slot = np.ascontiguousarray(slot, dtype=np.int32)
+    if o is None:
+        o = np.zeros((c.batch, c.num_heads, c.dv))
+    q, k, v, mixed, conv_w, conv_b, lam, beta = map(
+        lambda a: None if a is None else _f64(np.ascontiguousarray(a, dtype=np.float64)),
+        (q, k, v, mixed, conv_w, conv_b, lam, beta))
+    rc = lib.orc_step_batch(ctypes.byref(c), {"dense": 0, "deltalog": 1}[mode],
+                            _ptr(slot, ctypes.c_int32), _ptr(q), _ptr(k), _ptr(v), _ptr(mixed),
+                            _ptr(conv_w), _ptr(conv_b), _ptr(st.conv), _ptr(lam), _ptr(beta),
+                            _ptr(st.S), _ptr(st.ell), _ptr(st.klog), _ptr(st.ulog),
+                            _ptr(st.lamlog), _ptr(st.len, ctypes.c_int32), _ptr(o))
+    if rc != 0:
+        raise ValueError(f"oracle step_batch: {ERRORS.get(rc, rc)}")
+    return o
