@@ -1,0 +1,547 @@
+#!/usr/bin/env python3
+"""Benchmark: batched GDN decode on one GB300 (dense and DeltaLog append-merge).
+
+Default workload (``headline``): B=128 requests, H=32 heads, dk=dv=128, fp32
+state (256 MiB), bf16 q/k/v, per-head log-decay log(sigmoid(randn+3)), beta =
+sigmoid(randn); DeltaLog merge interval M=8.
+
+One benchmark *step* is one full append-merge cycle: M decode steps (M-1
+appends and one merge) over M batches of synthetic input, so every path of
+the decode step runs in every timed step and the figure is cycle-amortised.
+``value`` is head-steps/s = B * H * M * K / t over K timed steps, inputs
+already resident in HBM (a 16-step ring of pre-generated inputs). The state
+(256 MiB) is larger than L2, so no flush is needed between steps.
+
+Also reported: the dense mode on the same inputs, per-kernel CUDA-event
+durations with the algorithmic bytes each launch moves (roofline against the
+measured HBM copy bandwidth), an end-to-end figure through the public API with
+pinned host buffers, the SM clocks sampled during the timed region, and the
+fp64 CPU oracle timed on the host cores (a baseline, not the target).
+
+``--impl reference`` times the fp64 CPU oracle alone on the same metric.
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GDN decode head-steps/s and achieved HBM GB/s (% of GB300 peak), dense vs M"
+UNIT = "head-steps/s"
+RING = 16
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ("gdn_decode.cu", "gdn_device.cuh", "gdn_internal.h")
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_timing(elapsed_s: float, units: float, device=None):
+    """Max of the elapsed time and sum of the work over all ranks (identity when not
+    distributed). Uses the default process group (NCCL on GPUs, gloo on CPU)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return elapsed_s, units
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "linear_attention_decode_gdn_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = kernel_source_hash()
+    for line in open(path):
+        if line.startswith("#") or not line.strip():
+            continue
+        f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+        if f.get("kernel") == kernel and f.get("workload") == workload and f.get("src") == src:
+            return float(f["dram_bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 100):
+        self.gpu, self.ms, self.proc, self.lines = gpu_index, interval_ms, None, []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", f"-lms={self.ms}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        if not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- traffic model
+
+def head_bytes(mode: str, n: int, w, klb=2, conv=False) -> int:
+    """Algorithmic DRAM bytes one decode launch moves per (request, head), following the
+    traffic model of the DeltaLog notes (Sec. 2.5, Eqs. (8)-(11)): common inputs and
+    outputs, the state read (and write for dense / merge), the log entries replayed
+    and written, and the decay metadata."""
+    D = w.dk
+    e = 2 if w.qkv_bf16 else 4
+    dlam = w.dlam
+    common = 3 * D * e + 4 * dlam + 4 + 4 * D          # q,k,v + lambda + beta + o
+    if conv:
+        common += 3 * D * 3 * e * 2 + 3 * D * 16       # conv cache read + write, weights
+    state = 4 * D * D
+    entry = D * klb + 4 * D + 4 * dlam                  # one log position
+    if mode == "dense":
+        return common + 2 * state
+    meta = 4 * dlam + 4                                 # ell and L read
+    if mode == "append":
+        return common + state + n * entry + meta + entry + 4 * dlam + 4
+    return common + 2 * state + n * entry + meta + 4 * dlam + 4  # merge: base r+w, log read
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args, rank, local_rank, world):
+    import torch
+    import linear_attention_decode_gdn_gb300 as gdn
+    from linear_attention_decode_gdn_gb300 import build as gbuild
+    from linear_attention_decode_gdn_gb300 import workloads as wl
+
+    gbuild.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = wl.WORKLOADS[args.workload]
+    M = args.merge_interval
+    B, H, D = w.batch, w.num_heads, w.dk
+    flags = (gdn.QKV_BF16 if w.qkv_bf16 else 0) | (gdn.FUSE_CONV if w.conv else 0)
+    if args.klog_prenorm:
+        flags |= gdn.KLOG_PRENORM
+    lib = gdn._abi.load()
+    stream = torch.cuda.current_stream(dev)
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+
+    # ---- inputs: a ring of RING pre-generated decode steps, resident in HBM
+    ring = []
+    host_ring = []
+    for t in range(RING):
+        x = wl.step_inputs(w, t + 1000 * rank)
+        d = {}
+        if w.conv:
+            d["mixed_qkv"] = torch.from_numpy(x["mixed_bits"].view(np.int16)).view(torch.bfloat16)
+        else:
+            for n_ in ("q", "k", "v"):
+                d[n_] = (torch.from_numpy(x[n_ + "_bits"].view(np.int16)).view(torch.bfloat16)
+                         if w.qkv_bf16 else torch.from_numpy(x[n_]))
+        d["log_decay"] = torch.from_numpy(x["lam"])
+        d["beta"] = torch.from_numpy(x["beta"])
+        host_ring.append({k: v.pin_memory() for k, v in d.items()})
+        ring.append({k: v.to(dev) for k, v in d.items()})
+    slot = torch.arange(B, dtype=torch.int32, device=dev)
+    conv_w = None
+    if w.conv:
+        conv_w = torch.from_numpy(wl.conv_weights(w)).to(dev)
+
+    dims_dense = gdn.make_dims(B, H, D, num_slots=B, decay_per_key=w.decay_per_key, flags=flags)
+    dims_log = gdn.make_dims(B, H, D, num_slots=B, decay_per_key=w.decay_per_key,
+                             log_capacity=M - 1, flags=flags)
+    pools_d = gdn.Pools.allocate(dims_dense, device=dev, conv=w.conv)
+    pools_l = gdn.Pools.allocate(dims_log, device=dev, conv=w.conv, deltalog=M > 1)
+    if M == 1:
+        pools_l = gdn.Pools.allocate(dims_log, device=dev, conv=w.conv, deltalog=True)
+    o = torch.zeros((B, H, D), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def inputs_for(r, pools):
+        d = dict(ring[r])
+        if w.conv:
+            d.update(conv_w=conv_w, conv_pool=pools.conv)
+        return gdn.make_inputs(slot=slot, **d)
+
+    in_dense = [inputs_for(r, pools_d) for r in range(RING)]
+    in_log = [inputs_for(r, pools_l) for r in range(RING)]
+    log_l = pools_l.log()
+    P = ctypes.byref
+    fn = {"dense": lib.gdn_decode_dense, "append": lib.gdn_decode_append,
+          "merge": lib.gdn_decode_merge}
+
+    def launch(kind, r):
+        if kind == "dense":
+            rc = fn["dense"](P(dims_dense), P(in_dense[r]), pools_d.state.data_ptr(), o.data_ptr(),
+                             status.data_ptr(), sptr)
+        else:
+            rc = fn[kind](P(dims_log), P(in_log[r]), pools_l.state.data_ptr(), P(log_l),
+                          o.data_ptr(), status.data_ptr(), sptr)
+        if rc:
+            gdn._abi.check(rc, kind)
+
+    def cycle_kinds(mode):
+        if mode == "dense":
+            return ["dense"] * M
+        return ["append"] * (M - 1) + ["merge"]
+
+    def timed(mode, steps, warmup, per_kernel):
+        kinds = cycle_kinds(mode)
+        r = 0
+        for _ in range(warmup):
+            for k in kinds:
+                launch(k, r % RING)
+                r += 1
+        torch.cuda.synchronize(dev)
+        barrier()
+        torch.cuda.synchronize(dev)
+        evs = []
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(steps):
+            for k in kinds:
+                if per_kernel:
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    launch(k, r % RING)
+                    b.record(stream)
+                    evs.append((k, a, b))
+                else:
+                    launch(k, r % RING)
+                r += 1
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        elapsed = t0.elapsed_time(t1) / 1e3
+        per = {}
+        for k, a, b in evs:
+            per.setdefault(k, []).append(a.elapsed_time(b) / 1e3)
+        return elapsed, per
+
+    # ---- warm both modes, then the timed regions (clocks sampled meanwhile)
+    res = {}
+    with ClockSampler(local_rank) as clocks:
+        res["deltalog"] = timed("deltalog", args.steps, args.warmup, per_kernel=True)
+        res["dense"] = timed("dense", args.steps, args.warmup, per_kernel=True)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} during the benchmark")
+
+    peak, peak_kind = measured_peaks()
+    heads = B * H
+    klb = 4 if flags & gdn.KLOG_FP32 else 2
+    avg_n = (M - 2) / 2 if M > 1 else 0.0    # appends enter with L = 0 .. M-2
+    bytes_per_launch = {
+        "dense": heads * head_bytes("dense", 0, w, klb, w.conv),
+        "append": heads * head_bytes("append", avg_n, w, klb, w.conv),
+        "merge": heads * head_bytes("merge", M - 1, w, klb, w.conv),
+    }
+    kernels = {}
+    for mode in ("deltalog", "dense"):
+        for k, durs in res[mode][1].items():
+            tot = float(np.sum(durs))
+            avg = tot / len(durs)
+            achieved = bytes_per_launch[k] / avg / 1e9
+            kernels[k] = {"launches": len(durs), "avg_us": avg * 1e6, "total_ms": tot * 1e3,
+                          "algorithmic_bytes_per_launch": bytes_per_launch[k],
+                          "achieved_gbs": achieved, "frac_of_peak": achieved / peak}
+    lt, lu = reduce_timing(res["deltalog"][0], heads * M * args.steps, device=dev)
+    dt, du = reduce_timing(res["dense"][0], heads * M * args.steps, device=dev)
+    value = lu / lt
+    cycle_bytes = (M - 1) * bytes_per_launch["append"] + bytes_per_launch["merge"] if M > 1 \
+        else bytes_per_launch["merge"]
+    dense_bytes = M * bytes_per_launch["dense"]
+    modes = {
+        f"deltalog_M{M}": {"head_steps_per_s": value, "us_per_decode_step": lt / (args.steps * M) * 1e6,
+                            "algorithmic_gbs": cycle_bytes * args.steps / (lt / world) / 1e9 / world
+                            if world else None,
+                            "algorithmic_bytes_per_decode_step": cycle_bytes / M},
+        "dense": {"head_steps_per_s": du / dt, "us_per_decode_step": dt / (args.steps * M) * 1e6,
+                  "algorithmic_gbs": dense_bytes * args.steps / dt / 1e9,
+                  "algorithmic_bytes_per_decode_step": dense_bytes / M},
+    }
+    modes[f"deltalog_M{M}"]["algorithmic_gbs"] = cycle_bytes * args.steps / lt / 1e9
+    for m in modes.values():
+        m["frac_of_peak"] = m["algorithmic_gbs"] / peak
+    modes["speedup_deltalog_vs_dense"] = (value / (du / dt))
+
+    # dominant kernel of the timed DeltaLog cycle: largest share of device time
+    dom = max(res["deltalog"][1], key=lambda k: kernels[k]["total_ms"])
+    kd = kernels[dom]
+    traffic = profiled_traffic(dom, args.workload)
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": kd["achieved_gbs"], "peak": peak,
+                "peak_kind": f"{peak_kind} (hbm_gbs of MEASURED_PEAKS.json)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s", "unit": "GB/s", "frac": kd["achieved_gbs"] / peak,
+                "traffic": traffic,
+                "algorithmic_bytes_per_launch": kd["algorithmic_bytes_per_launch"]}
+
+    # ---- end to end through the public API: pinned host inputs in, o back to pinned host
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, M, dims_log, pools_l, host_ring, slot, conv_w, dev, stream, gdn)
+
+    launches = args.steps * M * 2 + (e2e["launches"] if e2e else 0)
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": lt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.description}", "batch": B, "num_heads": H, "dk": D,
+                   "dv": w.dv, "merge_interval": M, "decode_steps_per_step": M,
+                   "inputs": ("bf16" if w.qkv_bf16 else "fp32") + " q/k/v"
+                   + (" through the fused width-4 conv" if w.conv else "")
+                   + ", fp32 log-decay and beta; fp32 state and log values, "
+                   + ("bf16 pre-normalisation" if args.klog_prenorm else "bf16") + " key log",
+                   "l2": f"state {w.state_bytes / 2**20:.0f} MiB > L2 (inputs larger than L2, no flush)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "modes": modes,
+        "kernels": kernels,
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": {k: v for k, v in clocks.summary().items()},
+    }
+    return out
+
+
+def run_e2e(args, w, M, dims, pools, host_ring, slot, conv_w, dev, stream, gdn):
+    """Same metric through the public Python API with host buffers: every decode step
+    copies its inputs from pinned host memory, runs, and copies o back to pinned host."""
+    import torch
+    names = list(host_ring[0].keys())
+    stage = {k: torch.empty_like(host_ring[0][k], device=dev) for k in names}
+    o = torch.zeros((w.batch, w.num_heads, w.dv), dtype=torch.float32, device=dev)
+    o_host = [torch.empty_like(o, device="cpu").pin_memory() for _ in range(2)]
+    log = pools.log()
+    extra = dict(conv_w=conv_w, conv_pool=pools.conv) if w.conv else {}
+    inputs = gdn.make_inputs(slot=slot, **stage, **extra)
+    h2d = sum(t.numel() * t.element_size() for t in host_ring[0].values())
+    d2h = o.numel() * o.element_size()
+    gdn.slot_reset(dims, slot, w.batch, log, pools.conv, None)
+    steps, r, launches = args.e2e_steps or args.steps, 0, 0
+
+    def one_cycle():
+        nonlocal r, launches
+        for j in range(M):
+            src = host_ring[r % RING]
+            for k in names:
+                stage[k].copy_(src[k], non_blocking=True)
+            if j < M - 1:
+                gdn.decode_append(dims, inputs, pools.state, log, o)
+            else:
+                gdn.decode_merge(dims, inputs, pools.state, log, o)
+            o_host[r % 2].copy_(o, non_blocking=True)
+            r += 1
+            launches += 1
+
+    for _ in range(args.warmup):
+        one_cycle()
+    torch.cuda.synchronize(dev)
+    barrier()
+    launches = 0
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        one_cycle()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    el, units = reduce_timing(t0.elapsed_time(t1) / 1e3, w.batch * w.num_heads * M * steps, device=dev)
+    return {"value": units / el, "unit": UNIT, "h2d_bytes_per_step": h2d * M,
+            "d2h_bytes_per_step": d2h * M, "steps": steps, "launches": launches,
+            "api": "linear_attention_decode_gdn_gb300.decode_append / decode_merge (C ABI)"}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample(w, steps_budget_s: float, max_steps: int, batch: int, warm=1):
+    """Times the fp64 oracle (dense recurrence, OpenMP over (request, head)) on a bounded
+    sample: `batch` requests of the workload, consecutive decode steps."""
+    import oracle
+    from linear_attention_decode_gdn_gb300 import workloads as wl
+    lib = oracle.load()
+    H, D = w.num_heads, w.dk
+    flags = oracle.L2NORM | (oracle.CONV if w.conv else 0)
+    cfg = dict(batch=batch, num_heads=H, dk=D, dv=w.dv, num_slots=batch, dlam=w.dlam,
+               log_capacity=0, flags=flags, q_scale=1.0, l2_eps=1e-6)
+    st = oracle.BatchState(batch, H, D, w.dv, w.dlam, 0, nch=w.channels)
+    slot = np.arange(batch, dtype=np.int32)
+    cw = wl.conv_weights(w).astype(np.float64) if w.conv else None
+    inputs = []
+    for t in range(min(max_steps, RING)):
+        x = wl.step_inputs(w, t, batch=batch)
+        kw = dict(lam=x["lam"].astype(np.float64), beta=x["beta"].astype(np.float64))
+        if w.conv:
+            kw.update(mixed=x["mixed"].astype(np.float64), conv_w=cw)
+        else:
+            kw.update(q=x["q"].astype(np.float64), k=x["k"].astype(np.float64),
+                      v=x["v"].astype(np.float64))
+        inputs.append(kw)
+    for t in range(warm):
+        oracle.step_batch(cfg, "dense", st, slot, lib=lib, **inputs[t % len(inputs)])
+    n, t0 = 0, time.perf_counter()
+    while n < max_steps:
+        oracle.step_batch(cfg, "dense", st, slot, lib=lib, **inputs[n % len(inputs)])
+        n += 1
+        if time.perf_counter() - t0 >= steps_budget_s:
+            break
+    el = time.perf_counter() - t0
+    return batch * H * n / el, n, el, oracle.num_threads(lib)
+
+
+def cpu_baseline(w, budget_s=12.0):
+    batch = min(w.batch, 32)
+    v, n, el, cores = oracle_sample(w, budget_s, 10_000, batch)
+    return {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} decode steps of {batch} requests x {w.num_heads} heads of the {w.name} "
+                      f"workload (dk=dv={w.dk}), fp64 dense recurrence, {el:.1f} s"}
+
+
+def run_reference(args, rank):
+    """The CPU oracle as it stands, on this arm's metric: each step is one cycle of M decode
+    steps over a bounded sample (8 requests x H heads) of the workload."""
+    if rank != 0:
+        return None
+    from linear_attention_decode_gdn_gb300 import workloads as wl
+    import oracle
+    w = wl.WORKLOADS[args.workload]
+    M = args.merge_interval
+    batch = min(8, w.batch)
+    oracle_sample(w, 0.0, max(1, args.warmup) * M, batch)  # warm-up
+    v, n, el, cores = oracle_sample(w, 1e30, args.steps * M, batch, warm=0)
+    sample = (f"{args.steps} steps x {M} decode steps of {batch} requests x {w.num_heads} heads "
+              f"(dk=dv={w.dk}) of the {w.name} workload, fp64 dense recurrence")
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": f"{w.name}: {w.description}", "merge_interval": M,
+                       "decode_steps_per_step": M, "sample_batch": batch},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+# ----------------------------------------------------------------------------- main
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400, help="timed steps (append-merge cycles)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
+    ap.add_argument("--workload", default="headline")
+    ap.add_argument("--merge-interval", type=int, default=8)
+    ap.add_argument("--klog-prenorm", action="store_true",
+                    help="key log keeps the pre-normalisation bf16 key (exact factor)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+
+    world, rank, local = dist_info()
+    if args.impl == "reference":
+        line = run_reference(args, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    out = run_gpu(args, rank, local, world)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            from linear_attention_decode_gdn_gb300 import workloads as wl
+            out["cpu_baseline"] = cpu_baseline(wl.WORKLOADS[args.workload])
+        else:
+            out["cpu_baseline"] = None
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

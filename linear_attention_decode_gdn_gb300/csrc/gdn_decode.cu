@@ -1,0 +1,465 @@
+// gdn_decode.cu -- the decode-step kernels (dense, DeltaLog append, merge, auto step).
+//
+// One CTA owns one (request, head): it is the single writer of that head's
+// state / base tile, its output row and its log entries (DeltaLog notes,
+// Sec. 2.6 / Fig. 5 split the tile along dv across CTAs and need a separate
+// finalize pass for the shared metadata; on GB300 a whole 128x128 fp32 tile
+// (64 KiB) fits in shared memory three times per SM, so the head is not split
+// and the metadata commit needs no second pass).
+//
+// Per CTA:
+//   prologue  TMA bulk copies of the tile (4 row chunks for dk = 128) and of the
+//             first L log entries start at once; meanwhile the threads load q/k/v
+//             (or run the width-4 conv + SiLU), L2-normalise q and k, form the
+//             decays exp(ell') and, for every log entry i < L, the two projection
+//             coefficients  c^k_i = k^T D(ell' - Lambda_i) K_i,  c^q_i = q^T D(...) K_i
+//             (DeltaLog notes Sec. 2.4, one warp-shuffle reduction per entry).
+//   phase 1   one pass over the tile as chunks land:  r_k = S^T (e^{ell'} * k),
+//             r_q = S^T (e^{ell'} * q)  (warp-local sums, then across warps).
+//   phase 2   per value column j:  vhat = r_k + sum_i c^k_i U_i,  b = beta (v - vhat),
+//             o = r_q + sum_i c^q_i U_i + (q.k) b.   Append commits the new entry.
+//   phase 3   dense / merge only: S' = D(ell') S + sum_i D(ell' - Lambda_i) K_i U_i^T + k b^T,
+//             written back with 16-byte coalesced stores.
+#include <atomic>
+
+#include "gdn_device.cuh"
+
+namespace gdn {
+
+// Shared-memory layout of one decode CTA (bytes). Identical on host and device.
+struct Layout {
+  uint32_t tile, bars, scal, vec, uni, us, kd, coef, total;
+  int cp;  // row stride (entries) of the merge coefficient table, multiple of 8
+};
+
+__host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1u) / a * a; }
+
+__host__ __device__ inline Layout decode_layout(int mode, int D, int C, int klog_bytes) {
+  Layout L{};
+  const bool has_log = mode != MODE_DENSE;
+  const bool can_merge = mode == MODE_MERGE || mode == MODE_STEP;
+  const bool writes_state = mode != MODE_APPEND;
+  L.cp = can_merge ? static_cast<int>(align_up(static_cast<uint32_t>(C + 1), 8u)) : 0;
+  uint32_t off = 0;
+  L.tile = off;
+  off += static_cast<uint32_t>(D * D * 4);
+  L.bars = off;
+  off += 64;
+  L.scal = off;
+  off += 128;
+  L.vec = off;  // q (later b), k, q*dec, k*dec, ell', [dec]
+  off += static_cast<uint32_t>(D * 4 * (writes_state ? 6 : 5));
+  // K_log entries while the coefficients are formed, then the cross-warp partial sums.
+  const uint32_t kbytes = has_log ? static_cast<uint32_t>(C * D * klog_bytes) : 0u;
+  const uint32_t redbytes = static_cast<uint32_t>(8 * D * 4);
+  L.uni = off;
+  off += align_up(kbytes > redbytes ? kbytes : redbytes, 16u);
+  L.us = off;
+  off += has_log ? static_cast<uint32_t>((can_merge ? L.cp : C) * D * 4) : 0u;
+  L.kd = off;
+  off += can_merge ? static_cast<uint32_t>(D * L.cp * 4) : 0u;
+  L.coef = off;
+  off += has_log ? align_up(static_cast<uint32_t>(2 * C * 4), 16u) : 0u;
+  L.total = off;
+  return L;
+}
+
+template <int D, int MODE>
+__global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+
+  constexpr int NCHUNK = (D >= 128) ? 4 : 1;       // TMA row chunks of the tile
+  constexpr int CHUNK_ROWS = D / NCHUNK;
+  constexpr uint32_t CHUNK_BYTES = CHUNK_ROWS * D * 4;
+  constexpr int VPR = D / 4;                        // float4 per tile row
+  constexpr int RPW = 32 / VPR;                     // rows a warp covers per pass
+  constexpr int RPI = NW * RPW;                     // rows the CTA covers per pass
+  constexpr int NIT = (D + RPI - 1) / RPI;
+  constexpr int ITC = NIT / NCHUNK;                 // passes per chunk
+  static_assert(NCHUNK == 1 || (NIT % NCHUNK == 0 && CHUNK_ROWS % RPI == 0), "chunking");
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x / p.H;
+  const int h = blockIdx.x - b * p.H;
+  const int slot = __ldg(p.slot + b);
+  if (slot < 0) return;  // padding request
+  if (slot >= p.num_slots) {
+    if (tid == 0) atomic_status(p.status, GDN_STATUS_BAD_SLOT);
+    return;
+  }
+
+  const int C = p.C, dlam = p.dlam;
+  const uint32_t fl = p.flags;
+  const int klb = (fl & GDN_KLOG_FP32) ? 4 : 2;
+  const Layout L = decode_layout(MODE, D, C, klb);
+  float* tile = reinterpret_cast<float*>(smem + L.tile);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  int* scal_i = reinterpret_cast<int*>(smem + L.scal);             // [0] L on entry, [1] status bits
+  float* scal_f = reinterpret_cast<float*>(smem + L.scal + 16);    // [0..7] norm partials, [8] q.k
+  float* q_s = reinterpret_cast<float*>(smem + L.vec);
+  float* b_s = q_s;  // b takes q's place once the prologue is done
+  float* k_s = q_s + D;
+  float* qdec_s = q_s + 2 * D;
+  float* kdec_s = q_s + 3 * D;
+  float* ellp_s = q_s + 4 * D;
+  float* dec_s = q_s + 5 * D;  // only when the state is written
+  unsigned char* uni = smem + L.uni;
+  float* red = reinterpret_cast<float*>(uni);
+  float* u_s = reinterpret_cast<float*>(smem + L.us);
+  float* kd_s = reinterpret_cast<float*>(smem + L.kd);
+  float* ck_s = reinterpret_cast<float*>(smem + L.coef);
+  float* cq_s = ck_s + C;
+  const int cp = L.cp;
+
+  const size_t sh = static_cast<size_t>(slot) * p.H + h;
+  const float* tile_g = p.state + sh * static_cast<size_t>(D * D);
+
+  // ---- prologue: start every asynchronous copy first -------------------------
+  if (tid == 0) {
+    for (int c = 0; c <= NCHUNK; ++c) mbar_init(&bars[c], 1u);
+    fence_mbar_init();
+    const uint64_t pol = l2_policy_evict_first();
+    const uint32_t starve = (fl & GDN_TEST_STARVE_WAIT) ? 16u : 0u;
+#pragma unroll
+    for (int c = 0; c < NCHUNK; ++c) {
+      mbar_arrive_expect_tx(&bars[c], CHUNK_BYTES + (c == 0 ? starve : 0u));
+      bulk_load_hint(tile + c * CHUNK_ROWS * D, tile_g + c * CHUNK_ROWS * D, CHUNK_BYTES, &bars[c],
+                     pol);
+    }
+    int n = 0;
+    uint32_t bad = 0u;
+    if (MODE != MODE_DENSE) {
+      n = p.len[sh];
+      if (n < 0 || n > C)
+        bad = GDN_STATUS_BAD_LEN;
+      else if (MODE == MODE_APPEND && n == C)
+        bad = GDN_STATUS_LOG_FULL;
+      if (bad) n = 0;
+      const uint32_t kbytes = static_cast<uint32_t>(n * D * klb);
+      const uint32_t ubytes = static_cast<uint32_t>(n * D * 4);
+      mbar_arrive_expect_tx(&bars[NCHUNK], kbytes + ubytes);
+      if (n > 0) {
+        bulk_load(uni, static_cast<const unsigned char*>(p.k_log) + sh * C * D * klb, kbytes,
+                  &bars[NCHUNK]);
+        bulk_load(u_s, p.u_log + sh * C * D, ubytes, &bars[NCHUNK]);
+      }
+    }
+    scal_i[0] = n;
+    scal_i[1] = static_cast<int>(bad);
+  }
+
+  // ---- inputs, norms, gates ----------------------------------------------------
+  const bool is_q = tid < D;                     // owns q[tid], v[tid], row tid, column tid
+  const bool is_k = tid >= 128 && tid < 128 + D;  // owns k[tid - 128]
+  const int ii = is_q ? tid : tid - 128;
+  float x, vj;
+  load_token(p, b, h, slot, tid, &x, &vj);
+  {
+    const float ss = warp_sum(x * x);
+    if (lane == 0) scal_f[warp] = ss;
+  }
+  float lam_t = 0.0f, ell_t = 0.0f;
+  if (tid < dlam) {
+    lam_t = __ldg(p.lam + (static_cast<size_t>(b) * p.H + h) * dlam + tid);
+    if (fl & GDN_GATE_RAW) lam_t = log_sigmoidf_(lam_t);
+    if (MODE != MODE_DENSE) ell_t = p.ell[sh * dlam + tid];
+  }
+  float beta = __ldg(p.beta + static_cast<size_t>(b) * p.H + h);
+  if (fl & GDN_GATE_RAW) beta = sigmoidf_(beta);
+  __syncthreads();  // (A) n, status bits, norm partials
+
+  const int n = scal_i[0];
+  const uint32_t bad = static_cast<uint32_t>(scal_i[1]);
+  if (bad) {  // skip the slot-head: wait for this CTA's own copies, then leave
+#pragma unroll
+    for (int c = 0; c < NCHUNK; ++c) (void)mbar_wait(&bars[c], 0u);
+    if (tid == 0) atomic_status(p.status, bad);
+    return;
+  }
+  if (fl & GDN_FUSE_CONV) conv_commit(p, b, h, slot, tid);
+
+  const float qss = scal_f[0] + scal_f[1] + scal_f[2] + scal_f[3];
+  const float kss = scal_f[4] + scal_f[5] + scal_f[6] + scal_f[7];
+  const bool l2 = (fl & GDN_NO_QK_L2NORM) == 0u;
+  const float qinv = l2 ? 1.0f / sqrtf(qss + p.l2_eps) : 1.0f;
+  const float kinv = l2 ? 1.0f / sqrtf(kss + p.l2_eps) : 1.0f;
+  float kn = 0.0f;
+  if (is_q) q_s[ii] = x * qinv * p.q_scale;
+  if (is_k) {
+    kn = x * kinv;
+    k_s[ii] = kn;
+  }
+  if (tid < dlam) ellp_s[tid] = ell_t + lam_t;  // ell' = ell + lambda (closure of the decays)
+  __syncthreads();  // (B)
+
+  const bool is_merge = (MODE == MODE_MERGE) || (MODE == MODE_STEP && n == C);
+  const bool is_append = (MODE == MODE_APPEND) || (MODE == MODE_STEP && n < C);
+  bool timeout = false;
+
+  if (is_q) {  // decays of key row tid
+    const float dcy = expf(ellp_s[dlam == 1 ? 0 : tid]);
+    qdec_s[tid] = q_s[tid] * dcy;
+    kdec_s[tid] = k_s[tid] * dcy;
+    if (MODE != MODE_APPEND) dec_s[tid] = dcy;
+  }
+  if (MODE != MODE_DENSE && n > 0) {
+    if (!mbar_wait(&bars[NCHUNK], 0u)) timeout = true;
+    // one warp per log entry: w_i = D(ell' - Lambda_i) K_i, c^k_i = k.w_i, c^q_i = q.w_i
+    for (int e = warp; e < n; e += NW) {
+      const float* lam_e = p.lam_log + (sh * C + e) * dlam;
+      const float fscal = (dlam == 1) ? expf(ellp_s[0] - __ldg(lam_e)) : 0.0f;
+      float ak = 0.0f, aq = 0.0f;
+      for (int d = lane; d < D; d += 32) {
+        const float kv = (klb == 2)
+                             ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(uni)[e * D + d])
+                             : reinterpret_cast<const float*>(uni)[e * D + d];
+        const float wgt = (dlam == 1) ? fscal : expf(ellp_s[d] - __ldg(lam_e + d));
+        const float wd = wgt * kv;
+        ak = fmaf(k_s[d], wd, ak);
+        aq = fmaf(q_s[d], wd, aq);
+        if (is_merge) kd_s[d * cp + e] = wd;
+      }
+      ak = warp_sum(ak);
+      aq = warp_sum(aq);
+      if (lane == 0) {
+        ck_s[e] = ak;
+        cq_s[e] = aq;
+      }
+    }
+  }
+  if (is_merge) {
+    // the current update enters the merge at weight D(0) = I; pad the tables with zeros
+    for (int idx = tid; idx < D * cp; idx += NT) {
+      const int d = idx / cp, e = idx - d * cp;
+      if (e == n)
+        kd_s[idx] = k_s[d];
+      else if (e > n)
+        kd_s[idx] = 0.0f;
+    }
+    for (int idx = tid; idx < (cp - n - 1) * D; idx += NT) u_s[(n + 1) * D + idx] = 0.0f;
+  }
+  if (warp == 0) {
+    float t = 0.0f;
+    for (int d = lane; d < D; d += 32) t = fmaf(q_s[d], k_s[d], t);
+    t = warp_sum(t);
+    if (lane == 0) scal_f[8] = t;
+  }
+  __syncthreads();  // (C)
+
+  // ---- phase 1: r_k = S^T (e^{ell'} k), r_q = S^T (e^{ell'} q), one pass --------
+  const int c4 = lane % VPR, rsub = lane / VPR;
+  const float4* tile4 = reinterpret_cast<const float4*>(tile);
+  float ak[4] = {0.f, 0.f, 0.f, 0.f}, aq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int c = 0; c < NCHUNK; ++c) {
+    if (!mbar_wait(&bars[c], 0u)) timeout = true;
+#pragma unroll
+    for (int it = c * ITC; it < (c + 1) * ITC; ++it) {
+      const int r = it * RPI + warp * RPW + rsub;
+      if (r < D) {
+        const float4 s = tile4[r * VPR + c4];
+        const float kd = kdec_s[r], qd = qdec_s[r];
+        ak[0] = fmaf(s.x, kd, ak[0]);
+        ak[1] = fmaf(s.y, kd, ak[1]);
+        ak[2] = fmaf(s.z, kd, ak[2]);
+        ak[3] = fmaf(s.w, kd, ak[3]);
+        aq[0] = fmaf(s.x, qd, aq[0]);
+        aq[1] = fmaf(s.y, qd, aq[1]);
+        aq[2] = fmaf(s.z, qd, aq[2]);
+        aq[3] = fmaf(s.w, qd, aq[3]);
+      }
+    }
+  }
+#pragma unroll
+  for (int off = VPR; off < 32; off <<= 1) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      ak[m] += __shfl_xor_sync(0xffffffffu, ak[m], off);
+      aq[m] += __shfl_xor_sync(0xffffffffu, aq[m], off);
+    }
+  }
+  // across warps, fixed order: red[w] = part[w + 4] + part[w], then sum over w
+  if (warp >= 4 && rsub == 0) {
+    float* r0 = red + (warp - 4) * 2 * D + c4 * 4;
+    *reinterpret_cast<float4*>(r0) = make_float4(ak[0], ak[1], ak[2], ak[3]);
+    *reinterpret_cast<float4*>(r0 + D) = make_float4(aq[0], aq[1], aq[2], aq[3]);
+  }
+  __syncthreads();  // (D)
+  if (warp < 4 && rsub == 0) {
+    float* r0 = red + warp * 2 * D + c4 * 4;
+    float4 pk = *reinterpret_cast<float4*>(r0), pq = *reinterpret_cast<float4*>(r0 + D);
+    pk.x += ak[0];
+    pk.y += ak[1];
+    pk.z += ak[2];
+    pk.w += ak[3];
+    pq.x += aq[0];
+    pq.y += aq[1];
+    pq.z += aq[2];
+    pq.w += aq[3];
+    *reinterpret_cast<float4*>(r0) = pk;
+    *reinterpret_cast<float4*>(r0 + D) = pq;
+  }
+  if (__syncthreads_or(timeout)) {  // (E)
+    if (tid == 0) atomic_status(p.status, GDN_STATUS_TIMEOUT);
+    return;
+  }
+
+  // ---- phase 2: residual, write strength, readout, log commit ----------------------
+  if (is_q) {
+    const int j = tid;
+    float rk = red[j];
+    rk += red[2 * D + j];
+    rk += red[4 * D + j];
+    rk += red[6 * D + j];
+    float rq = red[D + j];
+    rq += red[3 * D + j];
+    rq += red[5 * D + j];
+    rq += red[7 * D + j];
+    for (int e = 0; e < n; ++e) {
+      const float u = u_s[e * D + j];
+      rk = fmaf(ck_s[e], u, rk);
+      rq = fmaf(cq_s[e], u, rq);
+    }
+    const float bj = (fl & GDN_PLAIN_UPDATE) ? beta * vj : beta * (vj - rk);
+    const float oj = fmaf(scal_f[8], bj, rq);
+    p.o[(static_cast<size_t>(b) * p.H + h) * D + j] = oj;
+    b_s[j] = bj;
+    if (is_append)
+      p.u_log[(sh * C + n) * D + j] = (fl & GDN_KLOG_PRENORM) ? bj * kinv : bj;
+    if (is_merge) u_s[n * D + j] = bj;
+  }
+  if (is_append) {
+    if (is_k) {
+      const float kval = (fl & GDN_KLOG_PRENORM) ? x : kn;
+      const size_t at = (sh * C + n) * D + ii;
+      if (klb == 2)
+        reinterpret_cast<__nv_bfloat16*>(p.k_log)[at] = __float2bfloat16_rn(kval);
+      else
+        reinterpret_cast<float*>(p.k_log)[at] = kval;
+    }
+    if (tid < dlam) {
+      p.lam_log[(sh * C + n) * dlam + tid] = ellp_s[tid];
+      p.ell[sh * dlam + tid] = ellp_s[tid];
+    }
+    if (tid == 0) p.len[sh] = n + 1;
+  } else if (is_merge) {
+    if (tid < dlam) p.ell[sh * dlam + tid] = 0.0f;
+    if (tid == 0) p.len[sh] = 0;
+  }
+
+  // ---- phase 3: write the state (dense) or fold the log into the base (merge) ------
+  if (MODE == MODE_DENSE || is_merge) {
+    __syncthreads();  // (F) b and the current entry are in shared memory
+    float* out = p.state + sh * static_cast<size_t>(D * D);
+    float4* tilew = reinterpret_cast<float4*>(tile);
+    if (MODE == MODE_DENSE) {
+      const float4 bb = reinterpret_cast<const float4*>(b_s)[c4];
+#pragma unroll
+      for (int it = 0; it < NIT; ++it) {
+        const int r = it * RPI + warp * RPW + rsub;
+        if (r < D) {
+          const float4 s = tile4[r * VPR + c4];
+          const float dc = dec_s[r], kk = k_s[r];
+          float4 o4;
+          o4.x = fmaf(kk, bb.x, dc * s.x);
+          o4.y = fmaf(kk, bb.y, dc * s.y);
+          o4.z = fmaf(kk, bb.z, dc * s.z);
+          o4.w = fmaf(kk, bb.w, dc * s.w);
+          *reinterpret_cast<float4*>(out + r * D + c4 * 4) = o4;
+        }
+      }
+    } else {
+      const int ng = (n + 1 + 7) / 8;  // groups of 8 rank-1 terms (log entries + current)
+      for (int g = 0; g < ng; ++g) {
+        float4 u[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) u[e] = reinterpret_cast<const float4*>(u_s + (g * 8 + e) * D)[c4];
+#pragma unroll
+        for (int it = 0; it < NIT; ++it) {
+          const int r = it * RPI + warp * RPW + rsub;
+          if (r < D) {
+            float4 acc = tile4[r * VPR + c4];
+            if (g == 0) {
+              const float dc = dec_s[r];
+              acc.x *= dc;
+              acc.y *= dc;
+              acc.z *= dc;
+              acc.w *= dc;
+            }
+            const float4 w0 = *reinterpret_cast<const float4*>(kd_s + r * cp + g * 8);
+            const float4 w1 = *reinterpret_cast<const float4*>(kd_s + r * cp + g * 8 + 4);
+            const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              acc.x = fmaf(wv[e], u[e].x, acc.x);
+              acc.y = fmaf(wv[e], u[e].y, acc.y);
+              acc.z = fmaf(wv[e], u[e].z, acc.z);
+              acc.w = fmaf(wv[e], u[e].w, acc.w);
+            }
+            if (g == ng - 1)
+              *reinterpret_cast<float4*>(out + r * D + c4 * 4) = acc;
+            else
+              tilew[r * VPR + c4] = acc;
+          }
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------
+// launchers
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+template <int D, int MODE>
+cudaError_t launch_one(const DecodeParams& p, cudaStream_t stream) {
+  static std::atomic<uint32_t> configured[kMaxDevices];
+  const int klb = (p.flags & GDN_KLOG_FP32) ? 4 : 2;
+  const Layout L = decode_layout(MODE, D, p.C, klb);
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (configured[dev].load(std::memory_order_relaxed) < L.total) {
+    err = cudaFuncSetAttribute(gdn_decode_kernel<D, MODE>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(L.total));
+    if (err != cudaSuccess) return err;
+    configured[dev].store(L.total, std::memory_order_relaxed);
+  }
+  gdn_decode_kernel<D, MODE><<<dim3(static_cast<unsigned>(p.B * p.H)), dim3(NT), L.total, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(int mode, const DecodeParams& p, cudaStream_t stream) {
+  switch (mode) {
+    case MODE_DENSE: return launch_one<D, MODE_DENSE>(p, stream);
+    case MODE_APPEND: return launch_one<D, MODE_APPEND>(p, stream);
+    case MODE_MERGE: return launch_one<D, MODE_MERGE>(p, stream);
+    case MODE_STEP: return launch_one<D, MODE_STEP>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+size_t decode_smem_bytes(int mode, int D, int C, int klog_bytes) {
+  if (D != 16 && D != 32 && D != 64 && D != 128) return 0;
+  return decode_layout(mode, D, C, klog_bytes).total;
+}
+
+cudaError_t launch_decode(int mode, const DecodeParams& p, cudaStream_t stream) {
+  switch (p.D) {
+    case 16: return launch_d<16>(mode, p, stream);
+    case 32: return launch_d<32>(mode, p, stream);
+    case 64: return launch_d<64>(mode, p, stream);
+    case 128: return launch_d<128>(mode, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace gdn

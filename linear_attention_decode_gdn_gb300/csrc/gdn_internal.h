@@ -1,0 +1,67 @@
+// gdn_internal.h -- launch parameters shared by the C-ABI layer and the kernels.
+// Not part of the public interface (include/gdn.h is).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime_api.h>
+
+namespace gdn {
+
+// Which path of Algorithm 1 (DeltaLog notes, Sec. 2.3) a launch takes.
+enum Mode : int {
+  MODE_DENSE = 0,   // full state read + write every token
+  MODE_APPEND = 1,  // base read only, one log entry written
+  MODE_MERGE = 2,   // base read, log + current token folded into the base (Eq. (6))
+  MODE_STEP = 3,    // per slot-head: append if L < C on entry, else merge
+};
+
+struct DecodeParams {
+  int32_t B, H, D, num_slots, C, dlam, channels;
+  uint32_t flags;
+  float q_scale, l2_eps;
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* mixed;
+  const float* conv_w;
+  const float* conv_b;
+  void* conv_pool;
+  const float* lam;
+  const float* beta;
+  const int32_t* slot;
+  float* state;  // dense: state pool; DeltaLog: base pool
+  void* k_log;
+  float* u_log;
+  float* lam_log;
+  float* ell;
+  int32_t* len;
+  float* o;
+  int32_t* status;
+  // conv_l2norm outputs
+  float* q_out;
+  float* k_out;
+  float* v_out;
+};
+
+struct ResetParams {
+  int32_t H, D, num_slots, dlam, channels, n;
+  uint32_t flags;
+  const int32_t* slots;
+  float* ell;
+  int32_t* len;
+  void* conv_pool;
+  float* state;
+  int32_t* status;
+};
+
+// Kernel launchers (defined in the .cu files). Return cudaSuccess or the launch error.
+cudaError_t launch_decode(int mode, const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_conv_l2norm(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_slot_reset(const ResetParams& p, cudaStream_t stream);
+
+// Dynamic shared memory a decode launch needs (bytes); 0 if the shape is not built.
+size_t decode_smem_bytes(int mode, int D, int C, int klog_bytes);
+
+}  // namespace gdn

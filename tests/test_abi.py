@@ -1,0 +1,145 @@
+"""Host-side checks of the C-ABI library (no GPU needed, no compute launched).
+
+* the library loads and exports every function include/gdn.h declares;
+* gdn_log_bytes reproduces the DeltaLog notes' capacity table (Sec. 2.5);
+* argument validation rejects bad calls before anything is launched.
+Only invalid arguments are passed: every call here returns from validation.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+MiB = 1 << 20
+
+
+@pytest.fixture(scope="module")
+def gdn():
+    from linear_attention_decode_gdn_gb300 import build
+    build.build()
+    import linear_attention_decode_gdn_gb300 as g
+    return g
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(gdn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("gdn_conv_l2norm", "gdn_decode_dense", "gdn_decode_append", "gdn_decode_merge"):
+        assert required in names
+    from linear_attention_decode_gdn_gb300 import _abi
+    assert sorted(_abi.EXPORTS) == names
+
+
+def test_library_exports_every_declared_symbol(gdn):
+    lib = gdn._abi.load()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", gdn._abi.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (gdn_\w+)", out))
+    assert set(declared_functions()) <= exported
+    assert lib.gdn_version() == 1
+
+
+def test_strerror(gdn):
+    lib = gdn._abi.load()
+    for code in range(4):
+        assert lib.gdn_strerror(code)
+    assert lib.gdn_strerror(99) == b"unknown error code"
+
+
+@pytest.mark.parametrize("per_key,M,C_entry_bytes,expected_mib", [
+    (False, 8, 2 * 128 + 4 * 128 + 4, 21.125),   # GDN row of the capacity table
+    (True, 4, 2 * 128 + 4 * 128 + 4 * 128, 17.0),  # KDA row
+])
+def test_log_bytes_matches_capacity_table(gdn, per_key, M, C_entry_bytes, expected_mib):
+    d = gdn.make_dims(128, 32, 128, num_slots=128, decay_per_key=per_key, log_capacity=M - 1)
+    s = gdn.log_bytes(d)
+    assert s["residency"] == expected_mib * MiB
+    B, H = 128, 32
+    dlam = 128 if per_key else 1
+    assert s["residency"] == (M - 1) * B * H * C_entry_bytes + 4 * B * H * dlam
+    assert s["total"] == s["residency"] + 4 * B * H
+    assert s["residency"] / (4 * B * H * 128 * 128) == pytest.approx(
+        0.0825 if not per_key else 0.0664, abs=5e-4)
+
+
+def test_log_bytes_fp32_keys(gdn):
+    d = gdn.make_dims(2, 3, 64, num_slots=5, log_capacity=4, flags=gdn.KLOG_FP32)
+    s = gdn.log_bytes(d)
+    assert s["k_log"] == 5 * 3 * 4 * 64 * 4 and s["u_log"] == 5 * 3 * 4 * 64 * 4
+    assert s["lam_log"] == 5 * 3 * 4 * 4 and s["ell"] == 5 * 3 * 4 and s["len"] == 5 * 3 * 4
+
+
+def _expect(gdn, fn, code):
+    with pytest.raises(gdn.GDNError) as ei:
+        fn()
+    assert ei.value.code == code, str(ei.value)
+
+
+def test_validation_rejects_before_launch(gdn):
+    from linear_attention_decode_gdn_gb300 import _abi
+    lib = _abi.load()
+    # NULL dims
+    assert lib.gdn_decode_dense(None, None, None, None, None, None) == _abi.GDN_ERR_INVALID_ARG
+    assert b"dims" in lib.gdn_last_error()
+    fake = 1 << 20  # never dereferenced: every call below fails validation first
+    ok_in = gdn.make_inputs(q=fake, k=fake, v=fake, log_decay=fake, beta=fake, slot=fake)
+    # unsupported head sizes
+    for dk, dv in ((48, 48), (128, 64), (256, 256)):
+        d = gdn.make_dims(1, 1, dk, dv)
+        _expect(gdn, lambda: gdn.decode_dense(d, ok_in, fake, fake, stream=0), _abi.GDN_ERR_UNSUPPORTED)
+    d = gdn.make_dims(1, 1, 128)
+    # missing inputs
+    _expect(gdn, lambda: gdn.decode_dense(d, gdn.make_inputs(q=fake, k=fake, log_decay=fake, beta=fake,
+                                                              slot=fake), fake, fake, stream=0),
+            _abi.GDN_ERR_INVALID_ARG)
+    # misaligned pointers
+    bad_in = gdn.make_inputs(q=fake + 8, k=fake, v=fake, log_decay=fake, beta=fake, slot=fake)
+    _expect(gdn, lambda: gdn.decode_dense(d, bad_in, fake, fake, stream=0), _abi.GDN_ERR_UNSUPPORTED)
+    _expect(gdn, lambda: gdn.decode_dense(d, ok_in, fake + 4, fake, stream=0), _abi.GDN_ERR_UNSUPPORTED)
+    # unknown flags, bad decay mode, negative sizes
+    for dd in (gdn.make_dims(1, 1, 128, flags=1 << 20), gdn.make_dims(-1, 1, 128),
+               gdn.make_dims(1, 0, 128)):
+        _expect(gdn, lambda: gdn.decode_dense(dd, ok_in, fake, fake, stream=0), _abi.GDN_ERR_INVALID_ARG)
+    d2 = gdn.make_dims(1, 1, 128)
+    d2.decay_per_key = 2
+    _expect(gdn, lambda: gdn.decode_dense(d2, ok_in, fake, fake, stream=0), _abi.GDN_ERR_INVALID_ARG)
+    # DeltaLog calls: log required; append needs C >= 1; C <= 63; log pointers when C > 0
+    dl = gdn.make_dims(1, 1, 128, log_capacity=7)
+    log_ok = gdn.make_log(fake, fake, fake, fake, fake)
+    _expect(gdn, lambda: lib_call(lib, "gdn_decode_append", dl, ok_in, fake, None, fake),
+            _abi.GDN_ERR_INVALID_ARG)
+    _expect(gdn, lambda: gdn.decode_append(gdn.make_dims(1, 1, 128, log_capacity=0), ok_in, fake,
+                                           log_ok, fake, stream=0), _abi.GDN_ERR_INVALID_ARG)
+    _expect(gdn, lambda: gdn.decode_merge(gdn.make_dims(1, 1, 128, log_capacity=64), ok_in, fake,
+                                          log_ok, fake, stream=0), _abi.GDN_ERR_UNSUPPORTED)
+    _expect(gdn, lambda: gdn.decode_merge(dl, ok_in, fake, gdn.make_log(None, fake, fake, fake, fake),
+                                          fake, stream=0), _abi.GDN_ERR_INVALID_ARG)
+    # flag combinations
+    _expect(gdn, lambda: gdn.decode_merge(
+        gdn.make_dims(1, 1, 128, log_capacity=7, flags=gdn.KLOG_PRENORM | gdn.FUSE_CONV), ok_in,
+        fake, log_ok, fake, stream=0), _abi.GDN_ERR_UNSUPPORTED)
+    _expect(gdn, lambda: gdn.conv_l2norm(gdn.make_dims(1, 1, 128), ok_in, fake, fake, fake, stream=0),
+            _abi.GDN_ERR_INVALID_ARG)
+    _expect(gdn, lambda: gdn.slot_reset(gdn.make_dims(1, 1, 128), None, -1, stream=0),
+            _abi.GDN_ERR_INVALID_ARG)
+    # batch == 0 is a no-op that launches nothing
+    gdn.decode_dense(gdn.make_dims(0, 1, 128, num_slots=1), ok_in, fake, fake, stream=0)
+
+
+def lib_call(lib, name, dims, inputs, pool, log, o):
+    from linear_attention_decode_gdn_gb300 import _abi
+    rc = getattr(lib, name)(ctypes.byref(dims), ctypes.byref(inputs), pool,
+                            None if log is None else ctypes.byref(log), o, None, None)
+    _abi.check(rc, name)

@@ -1,0 +1,436 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the fp64 oracle.
+
+Bars (from the problem statement): max|err|/max|ref| <= 1e-4 for the dense
+path and <= 5e-3 for the DeltaLog append-merge path, over the whole output
+tensor of a rollout, on the five workloads of the benchmark suite, plus edge
+cases: every head size, ragged batches, padding and permuted slots, M = 1,
+log contents, status bits, the timeout path, the standalone input stage.
+"""
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+from oracle import chunked  # noqa: E402
+import linear_attention_decode_gdn_gb300 as gdn  # noqa: E402
+from linear_attention_decode_gdn_gb300 import workloads as wl  # noqa: E402
+
+from gpu_harness import Lockstep, Variant, dev_bf16, dev_f32, dev_i32  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+DENSE_TOL = 1e-4
+LOG_TOL = 5e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from linear_attention_decode_gdn_gb300 import build
+    build.build()
+    torch.manual_seed(0)
+
+
+def _check(ls: Lockstep, tol_dense=DENSE_TOL, tol_log=LOG_TOL):
+    ls.compare_states()
+    report = []
+    for v in ls.variants:
+        tol = tol_dense if v.mode == "dense" else tol_log
+        report.append(f"{v.name}: out {v.rel_err:.3e} state {v.state_rel_err:.3e}")
+        assert ls.status(v) == 0, f"{v.name}: status {ls.status(v)}"
+        assert v.rel_err <= tol, report
+        if not math.isnan(v.state_err):
+            assert v.state_rel_err <= tol, report
+    print("; ".join(report))
+    return report
+
+
+# ---------------------------------------------------------------- the five workloads
+
+def test_tiny_fp32():
+    w = wl.WORKLOADS["tiny"]
+    ls = Lockstep(w, [Variant("dense"), Variant("deltalog", 4), Variant("deltalog", 4, "step"),
+                      Variant("deltalog", 4, extra_flags=gdn.KLOG_FP32, name="M=4/fp32K")]).run()
+    rep = _check(ls)
+    assert ls.variants[3].rel_err <= 1e-4, rep
+
+
+def test_small_conv():
+    w = wl.WORKLOADS["small_conv"]
+    _check(Lockstep(w, [Variant("dense"), Variant("deltalog", 8)]).run())
+
+
+def test_headline():
+    w = wl.WORKLOADS["headline"]
+    ls = Lockstep(w, [Variant("dense"), Variant("deltalog", 1, name="M=1/merge"),
+                      Variant("deltalog", 8), Variant("deltalog", 8, "step"),
+                      Variant("deltalog", 8, extra_flags=gdn.KLOG_PRENORM, name="M=8/prenorm")]).run()
+    rep = _check(ls)
+    assert ls.variants[4].rel_err <= 1e-4, rep  # exact key factors: fp32 rounding only
+
+
+@pytest.mark.slow
+def test_high_concurrency_merge_sweep():
+    w = wl.WORKLOADS["high_concurrency"]
+    _check(Lockstep(w, [Variant("dense")] + [Variant("deltalog", M) for M in (2, 4, 8, 16)]).run())
+
+
+def test_kda():
+    w = wl.WORKLOADS["kda"]
+    _check(Lockstep(w, [Variant("dense"), Variant("deltalog", 8),
+                        Variant("deltalog", 8, extra_flags=gdn.KLOG_PRENORM, name="M=8/prenorm")]).run())
+
+
+# ---------------------------------------------------------------- shapes and slots
+
+def _custom(name, B, H, D, steps, bf16=True, conv=False, per_key=False, qk_mult=1.0, seed=77):
+    return wl.Workload(name, B, H, D, D, steps, (1,), bf16, conv, per_key, seed, qk_mult=qk_mult)
+
+
+@pytest.mark.parametrize("D", [16, 32, 64, 128])
+@pytest.mark.parametrize("per_key", [False, True])
+def test_head_sizes_ragged_batch_and_slots(D, per_key):
+    w = _custom(f"d{D}", 5, 3, D, 24, per_key=per_key, seed=100 + D)
+    slot = np.array([6, -1, 0, 3, 5], dtype=np.int32)   # permuted, padded, gaps in the pool
+    ls = Lockstep(w, [Variant("dense"), Variant("deltalog", 3), Variant("deltalog", 5, "step"),
+                      Variant("deltalog", 4, extra_flags=gdn.KLOG_PRENORM, name="M=4/prenorm")],
+                  slot=slot, num_slots=8, q_scale=D ** -0.5).run()
+    _check(ls)
+    for v in ls.variants:  # padding row untouched; unused slots untouched
+        assert torch.all(v.o[1] == 0)
+        for s in (1, 2, 4, 7):
+            assert torch.all(v.pools.state[s] == 0)
+
+
+@pytest.mark.parametrize("D", [16, 128])
+def test_conv_fp32_inputs_and_raw_gates(D):
+    w = _custom(f"conv{D}", 3, 2, D, 20, bf16=False, conv=True, seed=300 + D)
+    ls = Lockstep(w, [Variant("dense"), Variant("deltalog", 4)], gate_raw=True).run()
+    _check(ls)
+
+
+def test_m1_merge_is_bitwise_dense():
+    w = _custom("m1", 16, 8, 128, 12, seed=5)
+    ls = Lockstep(w, [Variant("dense"), Variant("deltalog", 1, name="M=1")], keep_outputs=True).run()
+    a, b = ls.variants
+    for oa, ob in zip(a.outputs, b.outputs):
+        assert np.array_equal(oa, ob)
+    assert torch.equal(a.pools.state, b.pools.state)
+
+
+def test_determinism():
+    w = _custom("det", 32, 8, 128, 9, seed=6)
+    runs = [Lockstep(w, [Variant("deltalog", 4), Variant("dense")], keep_outputs=True).run()
+            for _ in range(2)]
+    for va, vb in zip(runs[0].variants, runs[1].variants):
+        for oa, ob in zip(va.outputs, vb.outputs):
+            assert np.array_equal(oa, ob)
+        assert torch.equal(va.pools.state, vb.pools.state)
+        if va.mode == "deltalog":
+            for name in ("k_log", "u_log", "lam_log", "ell", "length"):
+                assert torch.equal(getattr(va.pools, name), getattr(vb.pools, name)), name
+
+
+# ---------------------------------------------------------------- log contents
+
+@pytest.mark.parametrize("flags", [0, gdn.KLOG_FP32, gdn.KLOG_PRENORM])
+@pytest.mark.parametrize("per_key", [False, True])
+def test_log_contents_match_oracle_emulation(flags, per_key):
+    """After every step, GPU base / log / metadata == the oracle's literal DeltaLog emulation."""
+    D, B, H, M = 32, 3, 2, 4
+    C = M - 1
+    w = _custom("logc", B, H, D, 11, per_key=per_key, seed=8)
+    v = Variant("deltalog", M, extra_flags=flags)
+    ls = Lockstep(w, [v])
+    dlam = w.dlam
+    ocfg = dict(ls.cfg, log_capacity=C)
+    if flags & gdn.KLOG_PRENORM:
+        ocfg["flags"] |= oracle.KLOG_PRENORM
+    emu = oracle.BatchState(ls.num_slots, H, D, D, dlam, C)
+    # bf16 key factors (the pages' log precision) perturb every later replay by about one
+    # bf16 rounding (2^-9 relative) against the fp64-key emulation; exact keys: fp32 only
+    exact_keys = bool(flags & (gdn.KLOG_FP32 | gdn.KLOG_PRENORM))
+    u_tol = 1e-4 if exact_keys else 4e-3
+    o_tol = 1e-4 if exact_keys else LOG_TOL
+    for t in range(w.steps):
+        x = ls.step()
+        o_emu = oracle.step_batch(ocfg, "deltalog", emu, ls.slot, q=x["q"].astype(np.float64),
+                                  k=x["k"].astype(np.float64), v=x["v"].astype(np.float64),
+                                  lam=x["lam"].astype(np.float64), beta=x["beta"].astype(np.float64))
+        length = v.pools.length.cpu().numpy()
+        assert np.array_equal(length, emu.len), (t, length, emu.len)
+        assert np.allclose(v.pools.ell.cpu().numpy(), emu.ell, atol=2e-6, rtol=0)
+        base = v.pools.state.cpu().numpy()
+        assert np.max(np.abs(base - emu.S)) <= o_tol * max(1.0, np.max(np.abs(emu.S)))
+        klog = v.pools.k_log.float().cpu().numpy()
+        ulog = v.pools.u_log.cpu().numpy()
+        lamlog = v.pools.lam_log.cpu().numpy()
+        for s in range(B):
+            for h in range(H):
+                n = int(emu.len[s, h])
+                if n == 0:
+                    continue
+                assert np.allclose(lamlog[s, h, :n], emu.lamlog[s, h, :n], atol=2e-6, rtol=0)
+                uref = emu.ulog[s, h, :n]
+                assert np.max(np.abs(ulog[s, h, :n] - uref)) <= u_tol * max(1e-3, np.max(np.abs(uref)))
+                kref = emu.klog[s, h, :n]
+                if flags & gdn.KLOG_PRENORM:
+                    assert np.array_equal(klog[s, h, :n], kref)  # the raw bf16 key, bit for bit
+                elif flags & gdn.KLOG_FP32:
+                    assert np.allclose(klog[s, h, :n], kref, atol=1e-6, rtol=0)
+                else:  # one bf16 rounding of the normalised key
+                    assert np.all(np.abs(klog[s, h, :n] - kref) <= 2.0 ** -8 * np.abs(kref) + 1e-7)
+        o_gpu = v.o.cpu().numpy()
+        assert np.max(np.abs(o_gpu - o_emu)) <= o_tol * max(1.0, np.max(np.abs(o_emu)))
+
+
+# ---------------------------------------------------------------- pages' worked examples
+
+def test_teaching_example_on_gpu():
+    """DeltaLog notes Sec. 2.3: S0 = 10, decay 1/2, increments 2, 3, 4, M = 3 -> 7, 6.5, 7.25;
+    base 10, 10, 7.25. Embedded as entry [0,0] of a 16x16 state, plain update, beta = 1."""
+    D = 16
+    dims_d = gdn.make_dims(1, 1, D, num_slots=1, flags=gdn.PLAIN_UPDATE | gdn.NO_QK_L2NORM)
+    dims_l = gdn.make_dims(1, 1, D, num_slots=1, log_capacity=2,
+                           flags=gdn.PLAIN_UPDATE | gdn.NO_QK_L2NORM)
+    pd = gdn.Pools.allocate(dims_d)
+    pl = gdn.Pools.allocate(dims_l, deltalog=True)
+    pd.state[0, 0, 0, 0] = 10.0
+    pl.state[0, 0, 0, 0] = 10.0
+    e0 = torch.zeros((1, 1, D), device="cuda")
+    e0[0, 0, 0] = 1.0
+    lam = torch.full((1, 1), math.log(0.5), device="cuda")
+    beta = torch.ones((1, 1), device="cuda")
+    slot = torch.zeros(1, dtype=torch.int32, device="cuda")
+    od = torch.zeros((1, 1, D), device="cuda")
+    ol = torch.zeros((1, 1, D), device="cuda")
+    expected = [(2.0, 7.0, 10.0), (3.0, 6.5, 10.0), (4.0, 7.25, 7.25)]
+    for step, (inc, logical, base) in enumerate(expected):
+        v = e0 * inc
+        inp = gdn.make_inputs(q=e0, k=e0, v=v, log_decay=lam, beta=beta, slot=slot)
+        gdn.decode_dense(dims_d, inp, pd.state, od)
+        if step < 2:
+            gdn.decode_append(dims_l, inp, pl.state, pl.log(), ol)
+        else:
+            gdn.decode_merge(dims_l, inp, pl.state, pl.log(), ol)
+        torch.cuda.synchronize()
+        assert abs(od[0, 0, 0].item() - logical) < 1e-5
+        assert abs(ol[0, 0, 0].item() - logical) < 1e-5
+        assert abs(pl.state[0, 0, 0, 0].item() - base) < 1e-5
+    assert pl.length.item() == 0 and pl.ell.item() == 0.0
+
+
+def test_gla_recurrent_matches_chunked_on_gpu():
+    """Inference handbook, "同一个计算的两种写法": T=64, DK=DV=16, C=16, q,k = randn/4, v = randn,
+    alpha = sigmoid(randn + 3); the recurrent GPU path (plain update, beta = 1) equals the
+    chunked form within atol 1e-5, outputs and final state."""
+    T, D = 64, 16
+    r = np.random.default_rng(0)
+    q = (r.standard_normal((T, D)) / 4).astype(np.float32)
+    k = (r.standard_normal((T, D)) / 4).astype(np.float32)
+    v = r.standard_normal((T, D)).astype(np.float32)
+    alpha = (1 / (1 + np.exp(-(r.standard_normal(T) + 3)))).astype(np.float32)
+    lam = np.log(alpha.astype(np.float64)).astype(np.float32)
+    o_ch, S_ch = chunked.gla_chunked(q, k, v, lam.astype(np.float64), 16)
+    for mode, M in (("dense", 1), ("deltalog", 4)):
+        dims = gdn.make_dims(1, 1, D, num_slots=1, log_capacity=M - 1,
+                             flags=gdn.PLAIN_UPDATE | gdn.NO_QK_L2NORM | gdn.KLOG_FP32)
+        pools = gdn.Pools.allocate(dims, deltalog=mode == "deltalog")
+        o = torch.zeros((1, 1, D), device="cuda")
+        outs = []
+        slot = torch.zeros(1, dtype=torch.int32, device="cuda")
+        beta = torch.ones((1, 1), device="cuda")
+        for t in range(T):
+            inp = gdn.make_inputs(q=dev_f32(q[t][None, None]), k=dev_f32(k[t][None, None]),
+                                  v=dev_f32(v[t][None, None]), log_decay=dev_f32(lam[t:t + 1][None]),
+                                  beta=beta, slot=slot)
+            if mode == "dense":
+                gdn.decode_dense(dims, inp, pools.state, o)
+            elif (t + 1) % M:
+                gdn.decode_append(dims, inp, pools.state, pools.log(), o)
+            else:
+                gdn.decode_merge(dims, inp, pools.state, pools.log(), o)
+            outs.append(o[0, 0].cpu().numpy().copy())
+        assert np.allclose(np.stack(outs), o_ch, atol=1e-5, rtol=0)
+        assert np.allclose(pools.state[0, 0].cpu().numpy(), S_ch, atol=1e-5, rtol=0)
+
+
+def test_non_expansion_on_gpu():
+    """v = 0, unit keys, 0 <= beta <= 1, alpha <= 1: the Frobenius norm of every state never grows."""
+    B, H, D = 4, 4, 128
+    dims = gdn.make_dims(B, H, D)
+    pools = gdn.Pools.allocate(dims)
+    pools.state.normal_()
+    o = torch.zeros((B, H, D), device="cuda")
+    slot = torch.arange(B, dtype=torch.int32, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(3)
+    for _ in range(20):
+        before = pools.state.flatten(2).norm(dim=2)
+        k = torch.randn((B, H, D), device="cuda", generator=g)
+        lam = -torch.rand((B, H), device="cuda", generator=g) * 0.1
+        beta = torch.rand((B, H), device="cuda", generator=g)
+        inp = gdn.make_inputs(q=k, k=k, v=torch.zeros_like(k), log_decay=lam, beta=beta, slot=slot)
+        gdn.decode_dense(dims, inp, pools.state, o)
+        after = pools.state.flatten(2).norm(dim=2)
+        assert torch.all(after <= before * (1 + 1e-5))
+
+
+# ---------------------------------------------------------------- status bits and failure paths
+
+def _simple_setup(B=2, H=2, D=32, C=3, num_slots=4):
+    dims = gdn.make_dims(B, H, D, num_slots=num_slots, log_capacity=C)
+    pools = gdn.Pools.allocate(dims, deltalog=True)
+    q = torch.randn((B, H, D), device="cuda")
+    inp = dict(q=q, k=torch.randn_like(q), v=torch.randn_like(q),
+               log_decay=-torch.rand((B, H), device="cuda") * 0.1,
+               beta=torch.rand((B, H), device="cuda"))
+    return dims, pools, inp
+
+
+def test_bad_slot_and_padding_status():
+    dims, pools, inp = _simple_setup()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o = torch.full((2, 2, 32), 9.0, device="cuda")
+    gdn.decode_dense(dims, gdn.make_inputs(**inp, slot=dev_i32([-1, 4])), pools.state, o, status)
+    torch.cuda.synchronize()
+    assert status.item() == gdn.STATUS_BAD_SLOT
+    assert torch.all(o == 9.0) and torch.all(pools.state == 0)
+
+
+def test_log_full_and_bad_len_status():
+    dims, pools, inp = _simple_setup()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o = torch.full((2, 2, 32), 9.0, device="cuda")
+    pools.length[0, 0] = 3      # full: append must refuse
+    pools.length[1, 1] = 7      # corrupt: > C
+    slot = dev_i32([0, 1])
+    gdn.decode_append(dims, gdn.make_inputs(**inp, slot=slot), pools.state, pools.log(), o, status)
+    torch.cuda.synchronize()
+    assert status.item() == gdn.STATUS_LOG_FULL | gdn.STATUS_BAD_LEN
+    assert torch.all(o[0, 0] == 9.0) and torch.all(o[1, 1] == 9.0)
+    assert torch.all(o[0, 1] != 9.0) and torch.all(o[1, 0] != 9.0)
+    assert pools.length[0, 0].item() == 3 and pools.length[1, 1].item() == 7
+    assert pools.length[0, 1].item() == 1 and pools.length[1, 0].item() == 1
+    # merge accepts the full log and flushes it
+    status.zero_()
+    pools.length[1, 1] = 0
+    gdn.decode_merge(dims, gdn.make_inputs(**inp, slot=slot), pools.state, pools.log(), o, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0 and torch.all(pools.length == 0)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """The test-only flag starves one barrier: the bounded wait gives up (about a second),
+    the call reports GDN_STATUS_TIMEOUT and writes nothing; the next call works."""
+    dims, pools, inp = _simple_setup(B=1, H=1, D=128)
+    dims_starve = gdn.make_dims(1, 1, 128, num_slots=4, flags=gdn.TEST_STARVE_WAIT)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o = torch.full((1, 1, 128), 9.0, device="cuda")
+    pools.state.normal_()
+    before = pools.state.clone()
+    slot = dev_i32([2])
+    gdn.decode_dense(dims_starve, gdn.make_inputs(**inp, slot=slot), pools.state, o, status)
+    torch.cuda.synchronize()
+    assert status.item() == gdn.STATUS_TIMEOUT
+    assert torch.all(o == 9.0) and torch.equal(pools.state, before)
+    status.zero_()
+    gdn.decode_dense(gdn.make_dims(1, 1, 128, num_slots=4), gdn.make_inputs(**inp, slot=slot),
+                     pools.state, o, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0 and not torch.all(o == 9.0)
+
+
+# ---------------------------------------------------------------- input stage
+
+@pytest.mark.parametrize("bf16", [True, False])
+def test_conv_l2norm_standalone_and_fused_equivalence(bf16):
+    w = _custom("convsa", 4, 3, 64, 6, bf16=bf16, conv=True, seed=11)
+    flags = gdn.FUSE_CONV | (gdn.QKV_BF16 if bf16 else 0)
+    B, H, D = w.batch, w.num_heads, w.dk
+    dims = gdn.make_dims(B, H, D, num_slots=5, flags=flags, q_scale=0.125)
+    dims_dec = gdn.make_dims(B, H, D, num_slots=5, flags=flags, q_scale=0.125)
+    dims_unf = gdn.make_dims(B, H, D, num_slots=5, flags=gdn.NO_QK_L2NORM)
+    slot = np.array([4, 0, 2, -1], dtype=np.int32)
+    cw = wl.conv_weights(w)
+    cw_dev = dev_f32(cw)
+    conv_a = gdn.Pools.allocate(dims, conv=True).conv
+    conv_b = conv_a.clone()
+    state_f = torch.zeros((5, H, D, D), device="cuda")
+    state_u = torch.zeros_like(state_f)
+    o_f = torch.zeros((B, H, D), device="cuda")
+    o_u = torch.zeros_like(o_f)
+    q_o, k_o, v_o = (torch.zeros((B, H, D), device="cuda") for _ in range(3))
+    oconv = np.zeros((5, w.channels, 3))
+    for t in range(w.steps):
+        x = wl.step_inputs(w, t)
+        mixed = dev_bf16(x["mixed_bits"]) if bf16 else dev_f32(x["mixed"])
+        gates = dict(log_decay=dev_f32(x["lam"]), beta=dev_f32(x["beta"]), slot=dev_i32(slot))
+        gdn.conv_l2norm(dims, gdn.make_inputs(mixed_qkv=mixed, conv_w=cw_dev, conv_pool=conv_a,
+                                              **gates), q_o, k_o, v_o)
+        gdn.decode_dense(dims_unf, gdn.make_inputs(q=q_o, k=k_o, v=v_o, **gates), state_u, o_u)
+        gdn.decode_dense(dims_dec, gdn.make_inputs(mixed_qkv=mixed, conv_w=cw_dev, conv_pool=conv_b,
+                                                   **gates), state_f, o_f)
+        torch.cuda.synchronize()
+        # oracle: conv + SiLU + L2 per request
+        for b in range(B):
+            s = slot[b]
+            if s < 0:
+                continue
+            y = oracle.conv1d_silu(x["mixed"][b].astype(np.float64), oconv[s], cw.astype(np.float64))
+            for h in range(H):
+                qr = y[h * D:(h + 1) * D]
+                kr = y[H * D + h * D:H * D + (h + 1) * D]
+                vr = y[2 * H * D + h * D:2 * H * D + (h + 1) * D]
+                qn, _ = oracle.l2norm(qr, 1e-6, 0.125)
+                kn, _ = oracle.l2norm(kr, 1e-6)
+                assert np.allclose(q_o[b, h].cpu().numpy(), qn, atol=2e-6, rtol=0)
+                assert np.allclose(k_o[b, h].cpu().numpy(), kn, atol=2e-6, rtol=0)
+                assert np.allclose(v_o[b, h].cpu().numpy(), vr, atol=1e-5, rtol=1e-5)
+        assert torch.equal(o_f[slot >= 0], o_u[slot >= 0])   # fused == unfused, bit for bit
+        assert torch.equal(state_f, state_u) and torch.equal(conv_a, conv_b)
+    # the conv cache holds the last three pre-conv inputs exactly
+    conv_np = conv_a.float().cpu().numpy()
+    assert np.array_equal(conv_np[slot[slot >= 0]], oconv[slot[slot >= 0]].astype(np.float32))
+    assert torch.all(conv_a[1] == 0) and torch.all(conv_a[3] == 0)
+
+
+def test_slot_reset():
+    dims = gdn.make_dims(3, 2, 64, num_slots=4, log_capacity=3, decay_per_key=True,
+                         flags=gdn.FUSE_CONV | gdn.QKV_BF16)
+    pools = gdn.Pools.allocate(dims, conv=True, deltalog=True)
+    for t in (pools.state, pools.ell, pools.u_log):
+        t.normal_()
+    pools.length.fill_(2)
+    pools.conv.fill_(1.5)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gdn.slot_reset(dims, dev_i32([2, -1, 0, 9]), 4, pools.log(), pools.conv, pools.state, status)
+    torch.cuda.synchronize()
+    assert status.item() == gdn.STATUS_BAD_SLOT
+    for s in (0, 2):
+        assert torch.all(pools.length[s] == 0) and torch.all(pools.ell[s] == 0)
+        assert torch.all(pools.conv[s] == 0) and torch.all(pools.state[s] == 0)
+    for s in (1, 3):
+        assert torch.all(pools.length[s] == 2) and torch.all(pools.conv[s] == 1.5)
+        assert not torch.all(pools.state[s] == 0)
+
+
+def test_step_entry_with_requests_at_different_phases():
+    """gdn_decode_step: slots reset at different times sit at different log lengths in one
+    launch; every output still equals the dense recurrence."""
+    w = _custom("phases", 8, 4, 64, 30, seed=12)
+    v = Variant("deltalog", 5, "step")
+    ls = Lockstep(w, [v])
+    for t in range(w.steps):
+        if t in (3, 7, 11):
+            resets = np.array({3: [1, 4], 7: [2], 11: [0, 5, 6]}[t], dtype=np.int32)
+            gdn.slot_reset(v.dims, dev_i32(resets), len(resets), v.pools.log(), None, v.pools.state)
+            ls.ost.S[resets] = 0.0
+        ls.step()
+    lens = v.pools.length.cpu().numpy()
+    assert len(set(lens[:, 0].tolist())) > 1  # phases really differ
+    assert ls.status(v) == 0
+    assert v.rel_err <= LOG_TOL, v.rel_err
