@@ -115,7 +115,7 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, interval_ms: int = 100):
+    def __init__(self, gpu_index: int, interval_ms: int = 50):
         self.gpu, self.ms, self.proc, self.lines = gpu_index, interval_ms, None, []
 
     def __enter__(self):
@@ -325,22 +325,18 @@ def run_gpu(args, rank, local_rank, world):
     lt, lu = reduce_timing(res["deltalog"][0], heads * M * args.steps, device=dev)
     dt, du = reduce_timing(res["dense"][0], heads * M * args.steps, device=dev)
     value = lu / lt
-    cycle_bytes = (M - 1) * bytes_per_launch["append"] + bytes_per_launch["merge"] if M > 1 \
+    cycle_bytes = ((M - 1) * bytes_per_launch["append"] + bytes_per_launch["merge"]) if M > 1 \
         else bytes_per_launch["merge"]
     dense_bytes = M * bytes_per_launch["dense"]
-    modes = {
-        f"deltalog_M{M}": {"head_steps_per_s": value, "us_per_decode_step": lt / (args.steps * M) * 1e6,
-                            "algorithmic_gbs": cycle_bytes * args.steps / (lt / world) / 1e9 / world
-                            if world else None,
-                            "algorithmic_bytes_per_decode_step": cycle_bytes / M},
-        "dense": {"head_steps_per_s": du / dt, "us_per_decode_step": dt / (args.steps * M) * 1e6,
-                  "algorithmic_gbs": dense_bytes * args.steps / dt / 1e9,
-                  "algorithmic_bytes_per_decode_step": dense_bytes / M},
-    }
-    modes[f"deltalog_M{M}"]["algorithmic_gbs"] = cycle_bytes * args.steps / lt / 1e9
-    for m in modes.values():
-        m["frac_of_peak"] = m["algorithmic_gbs"] / peak
-    modes["speedup_deltalog_vs_dense"] = (value / (du / dt))
+    modes = {}
+    for name, (el, units), nbytes in ((f"deltalog_M{M}", (lt, lu), cycle_bytes),
+                                      ("dense", (dt, du), dense_bytes)):
+        gbs = nbytes * args.steps * world / el / 1e9
+        modes[name] = {"head_steps_per_s": units / el,
+                       "us_per_decode_step": el / (args.steps * M) * 1e6,
+                       "algorithmic_bytes_per_decode_step": nbytes / M,
+                       "algorithmic_gbs": gbs, "frac_of_peak": gbs / peak}
+    modes["speedup_deltalog_vs_dense"] = value / (du / dt)
 
     # dominant kernel of the timed DeltaLog cycle: largest share of device time
     dom = max(res["deltalog"][1], key=lambda k: kernels[k]["total_ms"])
@@ -505,7 +501,7 @@ def run_reference(args, rank):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400, help="timed steps (append-merge cycles)")
+    ap.add_argument("--steps", type=int, default=2000, help="timed steps (append-merge cycles)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
     ap.add_argument("--workload", default="headline")

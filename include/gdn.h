@@ -102,7 +102,8 @@ typedef struct gdn_dims {
   int32_t dk, dv;        /* key / value head size; dk == dv in {16, 32, 64, 128} */
   int32_t num_slots;     /* rows of the state, conv and log pools */
   int32_t decay_per_key; /* 0: per-head scalar log-decay (GDN); 1: per-key-channel (KDA) */
-  int32_t log_capacity;  /* C = M - 1 log entries per slot-head, 0..63 (DeltaLog calls only) */
+  int32_t log_capacity;  /* C = M - 1 log entries per slot-head, 0..63 (DeltaLog calls only);
+                            larger values are rejected with GDN_ERR_UNSUPPORTED */
   uint32_t flags;        /* GDN_* flags above */
   float q_scale;         /* multiplies q after normalisation (1.0: o = S^T q exactly) */
   float l2_eps;          /* x / sqrt(sum x^2 + l2_eps) */

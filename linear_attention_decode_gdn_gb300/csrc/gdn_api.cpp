@@ -127,6 +127,12 @@ int decode_common(int mode, const gdn_dims* dims, const gdn_inputs* in, float* p
   if (log_call && (rc = check_log(dims, log)) != GDN_OK) return rc;
   if (mode == gdn::MODE_APPEND && dims->log_capacity < 1)
     return fail(GDN_ERR_INVALID_ARG, "append needs log_capacity >= 1");
+  if (gdn::decode_smem_bytes(mode, dims->dk, log_call ? dims->log_capacity : 0,
+                             dims->decay_per_key ? dims->dk : 1,
+                             (dims->flags & GDN_KLOG_FP32) ? 4 : 2,
+                             (dims->flags & GDN_QKV_BF16) ? 2 : 4) == 0)
+    return fail(GDN_ERR_UNSUPPORTED, "log_capacity %d does not fit in shared memory for this shape",
+                dims->log_capacity);
   gdn::DecodeParams p = make_params(dims, in);
   p.state = pool;
   p.o = o;

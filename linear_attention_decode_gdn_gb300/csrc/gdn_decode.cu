@@ -58,8 +58,8 @@ __host__ __device__ inline Layout decode_layout(int mode, int D, int C, int klog
   off += has_log ? static_cast<uint32_t>((can_merge ? L.cp : C) * D * 4) : 0u;
   L.kd = off;
   off += can_merge ? static_cast<uint32_t>(D * L.cp * 4) : 0u;
-  L.coef = off;
-  off += has_log ? align_up(static_cast<uint32_t>(2 * C * 4), 16u) : 0u;
+  L.coef = off;  // c^k | c^q | per-head decay snapshots Lambda_i
+  off += has_log ? align_up(static_cast<uint32_t>(3 * C * 4), 16u) : 0u;
   L.total = off;
   return L;
 }
@@ -109,14 +109,19 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
   float* kd_s = reinterpret_cast<float*>(smem + L.kd);
   float* ck_s = reinterpret_cast<float*>(smem + L.coef);
   float* cq_s = ck_s + C;
+  float* lam_s = ck_s + 2 * C;
   const int cp = L.cp;
 
   const size_t sh = static_cast<size_t>(slot) * p.H + h;
   const float* tile_g = p.state + sh * static_cast<size_t>(D * D);
 
   // ---- prologue: start every asynchronous copy first -------------------------
+  // the log length is loaded now and first used after barrier (A), so the load's
+  // latency overlaps the input loads instead of holding the CTA at the barrier
+  const int n_raw = (MODE != MODE_DENSE && tid == 0) ? p.len[sh] : 0;
   if (tid == 0) {
-    for (int c = 0; c <= NCHUNK; ++c) mbar_init(&bars[c], 1u);
+    for (int c = 0; c < NCHUNK; ++c) mbar_init(&bars[c], 1u);
+    mbar_init(&bars[NCHUNK], 2u);  // log entries: TMA bytes + the cp.async snapshots
     fence_mbar_init();
     const uint64_t pol = l2_policy_evict_first();
     const uint32_t starve = (fl & GDN_TEST_STARVE_WAIT) ? 16u : 0u;
@@ -126,26 +131,6 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
       bulk_load_hint(tile + c * CHUNK_ROWS * D, tile_g + c * CHUNK_ROWS * D, CHUNK_BYTES, &bars[c],
                      pol);
     }
-    int n = 0;
-    uint32_t bad = 0u;
-    if (MODE != MODE_DENSE) {
-      n = p.len[sh];
-      if (n < 0 || n > C)
-        bad = GDN_STATUS_BAD_LEN;
-      else if (MODE == MODE_APPEND && n == C)
-        bad = GDN_STATUS_LOG_FULL;
-      if (bad) n = 0;
-      const uint32_t kbytes = static_cast<uint32_t>(n * D * klb);
-      const uint32_t ubytes = static_cast<uint32_t>(n * D * 4);
-      mbar_arrive_expect_tx(&bars[NCHUNK], kbytes + ubytes);
-      if (n > 0) {
-        bulk_load(uni, static_cast<const unsigned char*>(p.k_log) + sh * C * D * klb, kbytes,
-                  &bars[NCHUNK]);
-        bulk_load(u_s, p.u_log + sh * C * D, ubytes, &bars[NCHUNK]);
-      }
-    }
-    scal_i[0] = n;
-    scal_i[1] = static_cast<int>(bad);
   }
 
   // ---- inputs, norms, gates ----------------------------------------------------
@@ -166,17 +151,33 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
   }
   float beta = __ldg(p.beta + static_cast<size_t>(b) * p.H + h);
   if (fl & GDN_GATE_RAW) beta = sigmoidf_(beta);
-  __syncthreads();  // (A) n, status bits, norm partials
+  __syncthreads();  // (A) norm partials
 
-  const int n = scal_i[0];
-  const uint32_t bad = static_cast<uint32_t>(scal_i[1]);
-  if (bad) {  // skip the slot-head: wait for this CTA's own copies, then leave
-#pragma unroll
-    for (int c = 0; c < NCHUNK; ++c) (void)mbar_wait(&bars[c], 0u);
-    if (tid == 0) atomic_status(p.status, bad);
-    return;
+  if (tid == 0) {
+    int n0 = 0;
+    uint32_t bad0 = 0u;
+    if (MODE != MODE_DENSE) {
+      n0 = n_raw;
+      if (n0 < 0 || n0 > C)
+        bad0 = GDN_STATUS_BAD_LEN;
+      else if (MODE == MODE_APPEND && n0 == C)
+        bad0 = GDN_STATUS_LOG_FULL;
+      if (bad0) n0 = 0;
+      const uint32_t kbytes = static_cast<uint32_t>(n0 * D * klb);
+      const uint32_t ubytes = static_cast<uint32_t>(n0 * D * 4);
+      mbar_arrive_expect_tx(&bars[NCHUNK], kbytes + ubytes);
+      if (n0 > 0) {
+        bulk_load(uni, static_cast<const unsigned char*>(p.k_log) + sh * C * D * klb, kbytes,
+                  &bars[NCHUNK]);
+        bulk_load(u_s, p.u_log + sh * C * D, ubytes, &bars[NCHUNK]);
+        if (dlam == 1)
+          for (int e = 0; e < n0; ++e) cp_async4(lam_s + e, p.lam_log + sh * C + e);
+      }
+      cp_async_arrive(&bars[NCHUNK]);
+    }
+    scal_i[0] = n0;
+    scal_i[1] = static_cast<int>(bad0);
   }
-  if (fl & GDN_FUSE_CONV) conv_commit(p, b, h, slot, tid);
 
   const float qss = scal_f[0] + scal_f[1] + scal_f[2] + scal_f[3];
   const float kss = scal_f[4] + scal_f[5] + scal_f[6] + scal_f[7];
@@ -190,7 +191,17 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
     k_s[ii] = kn;
   }
   if (tid < dlam) ellp_s[tid] = ell_t + lam_t;  // ell' = ell + lambda (closure of the decays)
-  __syncthreads();  // (B)
+  __syncthreads();  // (B) n, status bits, q, k, ell'
+
+  const int n = scal_i[0];
+  const uint32_t bad = static_cast<uint32_t>(scal_i[1]);
+  if (bad) {  // skip the slot-head: wait for this CTA's own copies, then leave
+#pragma unroll
+    for (int c = 0; c < NCHUNK; ++c) (void)mbar_wait(&bars[c], 0u);
+    if (tid == 0) atomic_status(p.status, bad);
+    return;
+  }
+  if (fl & GDN_FUSE_CONV) conv_commit(p, b, h, slot, tid);
 
   const bool is_merge = (MODE == MODE_MERGE) || (MODE == MODE_STEP && n == C);
   const bool is_append = (MODE == MODE_APPEND) || (MODE == MODE_STEP && n < C);
@@ -201,31 +212,6 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
     qdec_s[tid] = q_s[tid] * dcy;
     kdec_s[tid] = k_s[tid] * dcy;
     if (MODE != MODE_APPEND) dec_s[tid] = dcy;
-  }
-  if (MODE != MODE_DENSE && n > 0) {
-    if (!mbar_wait(&bars[NCHUNK], 0u)) timeout = true;
-    // one warp per log entry: w_i = D(ell' - Lambda_i) K_i, c^k_i = k.w_i, c^q_i = q.w_i
-    for (int e = warp; e < n; e += NW) {
-      const float* lam_e = p.lam_log + (sh * C + e) * dlam;
-      const float fscal = (dlam == 1) ? expf(ellp_s[0] - __ldg(lam_e)) : 0.0f;
-      float ak = 0.0f, aq = 0.0f;
-      for (int d = lane; d < D; d += 32) {
-        const float kv = (klb == 2)
-                             ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(uni)[e * D + d])
-                             : reinterpret_cast<const float*>(uni)[e * D + d];
-        const float wgt = (dlam == 1) ? fscal : expf(ellp_s[d] - __ldg(lam_e + d));
-        const float wd = wgt * kv;
-        ak = fmaf(k_s[d], wd, ak);
-        aq = fmaf(q_s[d], wd, aq);
-        if (is_merge) kd_s[d * cp + e] = wd;
-      }
-      ak = warp_sum(ak);
-      aq = warp_sum(aq);
-      if (lane == 0) {
-        ck_s[e] = ak;
-        cq_s[e] = aq;
-      }
-    }
   }
   if (is_merge) {
     // the current update enters the merge at weight D(0) = I; pad the tables with zeros
@@ -270,6 +256,33 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
       }
     }
   }
+  // log replay coefficients, off the critical path of the tile pass:
+  if (MODE != MODE_DENSE && n > 0) {
+    if (!mbar_wait(&bars[NCHUNK], 0u)) timeout = true;
+    // one warp per log entry: w_i = D(ell' - Lambda_i) K_i, c^k_i = k.w_i, c^q_i = q.w_i
+    for (int e = warp; e < n; e += NW) {
+      const float* lam_e = p.lam_log + (sh * C + e) * dlam;
+      const float fscal = (dlam == 1) ? expf(ellp_s[0] - lam_s[e]) : 0.0f;
+      float ak = 0.0f, aq = 0.0f;
+      for (int d = lane; d < D; d += 32) {
+        const float kv = (klb == 2)
+                             ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(uni)[e * D + d])
+                             : reinterpret_cast<const float*>(uni)[e * D + d];
+        const float wgt = (dlam == 1) ? fscal : expf(ellp_s[d] - __ldg(lam_e + d));
+        const float wd = wgt * kv;
+        ak = fmaf(k_s[d], wd, ak);
+        aq = fmaf(q_s[d], wd, aq);
+        if (is_merge) kd_s[d * cp + e] = wd;
+      }
+      ak = warp_sum(ak);
+      aq = warp_sum(aq);
+      if (lane == 0) {
+        ck_s[e] = ak;
+        cq_s[e] = aq;
+      }
+    }
+  }
+  if (MODE != MODE_DENSE) __syncthreads();  // the K entries share space with the partial sums
 #pragma unroll
   for (int off = VPR; off < 32; off <<= 1) {
 #pragma unroll
@@ -414,6 +427,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+
 template <int D, int MODE>
 cudaError_t launch_one(const DecodeParams& p, cudaStream_t stream) {
   static std::atomic<uint32_t> configured[kMaxDevices];
@@ -447,7 +461,9 @@ cudaError_t launch_d(int mode, const DecodeParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-size_t decode_smem_bytes(int mode, int D, int C, int klog_bytes) {
+size_t decode_smem_bytes(int mode, int D, int C, int dlam, int klog_bytes, int in_elem) {
+  (void)dlam;
+  (void)in_elem;
   if (D != 16 && D != 32 && D != 64 && D != 128) return 0;
   return decode_layout(mode, D, C, klog_bytes).total;
 }

@@ -62,6 +62,6 @@ cudaError_t launch_conv_l2norm(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_slot_reset(const ResetParams& p, cudaStream_t stream);
 
 // Dynamic shared memory a decode launch needs (bytes); 0 if the shape is not built.
-size_t decode_smem_bytes(int mode, int D, int C, int klog_bytes);
+size_t decode_smem_bytes(int mode, int D, int C, int dlam, int klog_bytes, int in_elem);
 
 }  // namespace gdn

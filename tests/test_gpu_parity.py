@@ -390,8 +390,12 @@ def test_conv_l2norm_standalone_and_fused_equivalence(bf16):
                 assert np.allclose(q_o[b, h].cpu().numpy(), qn, atol=2e-6, rtol=0)
                 assert np.allclose(k_o[b, h].cpu().numpy(), kn, atol=2e-6, rtol=0)
                 assert np.allclose(v_o[b, h].cpu().numpy(), vr, atol=1e-5, rtol=1e-5)
-        assert torch.equal(o_f[slot >= 0], o_u[slot >= 0])   # fused == unfused, bit for bit
-        assert torch.equal(state_f, state_u) and torch.equal(conv_a, conv_b)
+        # fused == unfused up to the order of the norm reductions (warp vs block sums)
+        live = torch.from_numpy(slot >= 0).cuda()
+        scale = max(1e-30, float(o_u[live].abs().max()))
+        assert float((o_f[live] - o_u[live]).abs().max()) <= 1e-5 * scale
+        assert float((state_f - state_u).abs().max()) <= 1e-5 * max(1e-30, float(state_u.abs().max()))
+        assert torch.equal(conv_a, conv_b)
     # the conv cache holds the last three pre-conv inputs exactly
     conv_np = conv_a.float().cpu().numpy()
     assert np.array_equal(conv_np[slot[slot >= 0]], oconv[slot[slot >= 0]].astype(np.float32))
