@@ -376,33 +376,75 @@ def run_gpu(args, rank, local_rank, world):
     return out
 
 
+def _packed(arrays: dict, align: int = 256):
+    """Byte offsets of `arrays` packed into one buffer (each start 256-byte aligned)."""
+    offs, off = {}, 0
+    for k, t in arrays.items():
+        offs[k] = off
+        off += (t.numel() * t.element_size() + align - 1) // align * align
+    return offs, off
+
+
+def _views(buf, offs, like: dict):
+    return {k: buf[offs[k]:offs[k] + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+            for k, t in like.items()}
+
+
 def run_e2e(args, w, M, dims, pools, host_ring, slot, conv_w, dev, stream, gdn):
-    """Same metric through the public Python API with host buffers: every decode step
-    copies its inputs from pinned host memory, runs, and copies o back to pinned host."""
+    """Same metric through the public Python API with host buffers. Every decode step
+    copies its inputs (one packed pinned buffer: q/k/v or the conv input, log-decay,
+    beta) host -> device, runs the decode call, and copies o back to pinned host memory.
+    The copies run on their own streams, double-buffered against the decode kernels
+    (event-ordered), the way a serving loop overlaps the next token's upload and the
+    last token's readback with the current step."""
     import torch
     names = list(host_ring[0].keys())
-    stage = {k: torch.empty_like(host_ring[0][k], device=dev) for k in names}
-    o = torch.zeros((w.batch, w.num_heads, w.dv), dtype=torch.float32, device=dev)
-    o_host = [torch.empty_like(o, device="cpu").pin_memory() for _ in range(2)]
+    offs, nbytes = _packed(host_ring[0])
+    host_packed = []
+    for src in host_ring:
+        hb = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+        for k, v in _views(hb, offs, src).items():
+            v.copy_(src[k])
+        host_packed.append(hb)
+    stage = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    o = [torch.zeros((w.batch, w.num_heads, w.dv), dtype=torch.float32, device=dev)
+         for _ in range(2)]
+    o_host = [torch.empty_like(o[0], device="cpu").pin_memory() for _ in range(2)]
     log = pools.log()
     extra = dict(conv_w=conv_w, conv_pool=pools.conv) if w.conv else {}
-    inputs = gdn.make_inputs(slot=slot, **stage, **extra)
-    h2d = sum(t.numel() * t.element_size() for t in host_ring[0].values())
-    d2h = o.numel() * o.element_size()
-    gdn.slot_reset(dims, slot, w.batch, log, pools.conv, None)
+    inputs = [gdn.make_inputs(slot=slot, **_views(stage[b], offs, host_ring[0]), **extra)
+              for b in range(2)]
+    h2d = nbytes
+    d2h = o[0].numel() * o[0].element_size()
+    gdn.slot_reset(dims, slot, w.batch, log, pools.conv, None, stream=stream)
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_k = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
     steps, r, launches = args.e2e_steps or args.steps, 0, 0
+    del names
 
     def one_cycle():
         nonlocal r, launches
         for j in range(M):
-            src = host_ring[r % RING]
-            for k in names:
-                stage[k].copy_(src[k], non_blocking=True)
-            if j < M - 1:
-                gdn.decode_append(dims, inputs, pools.state, log, o)
-            else:
-                gdn.decode_merge(dims, inputs, pools.state, log, o)
-            o_host[r % 2].copy_(o, non_blocking=True)
+            b = r & 1
+            # upload step r into stage[b] once kernel r-2 has consumed it
+            if r >= 2:
+                s_in.wait_event(ev_k[b])
+            with torch.cuda.stream(s_in):
+                stage[b].copy_(host_packed[r % RING], non_blocking=True)
+            ev_in[b].record(s_in)
+            stream.wait_event(ev_in[b])
+            if r >= 2:
+                stream.wait_event(ev_out[b])      # o[b] of step r-2 has been read back
+            call = gdn.decode_append if j < M - 1 else gdn.decode_merge
+            call(dims, inputs[b], pools.state, log, o[b], stream=stream)
+            ev_k[b].record(stream)
+            s_out.wait_event(ev_k[b])
+            with torch.cuda.stream(s_out):
+                o_host[b].copy_(o[b], non_blocking=True)
+            ev_out[b].record(s_out)
             r += 1
             launches += 1
 
@@ -414,14 +456,24 @@ def run_e2e(args, w, M, dims, pools, host_ring, slot, conv_w, dev, stream, gdn):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
+    s_in.wait_event(t0)
+    s_out.wait_event(t0)
+    wall0 = time.perf_counter()
     for _ in range(steps):
         one_cycle()
+    for e in ev_out:
+        stream.wait_event(e)
     t1.record(stream)
     torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
     barrier()
+    if not bool(torch.isfinite(o_host[(r - 1) & 1]).all()):
+        raise RuntimeError("non-finite output read back in the end-to-end run")
     el, units = reduce_timing(t0.elapsed_time(t1) / 1e3, w.batch * w.num_heads * M * steps, device=dev)
     return {"value": units / el, "unit": UNIT, "h2d_bytes_per_step": h2d * M,
             "d2h_bytes_per_step": d2h * M, "steps": steps, "launches": launches,
+            "host_wall_s": wall, "device_s": el,
+            "pipeline": "H2D / decode / D2H on three streams, double-buffered",
             "api": "linear_attention_decode_gdn_gb300.decode_append / decode_merge (C ABI)"}
 
 

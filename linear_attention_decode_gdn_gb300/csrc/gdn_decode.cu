@@ -131,6 +131,27 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
       bulk_load_hint(tile + c * CHUNK_ROWS * D, tile_g + c * CHUNK_ROWS * D, CHUNK_BYTES, &bars[c],
                      pol);
     }
+    // the CTA that runs about one resident wave later finds its token inputs in L2
+    // (they depend only on (request, head); the state tile depends on the slot)
+    const int gp = static_cast<int>(blockIdx.x) + p.prefetch_ahead;
+    if (p.prefetch_ahead > 0 && gp < p.B * p.H) {
+      const int bp = gp / p.H, hp = gp - bp * p.H;
+      const uint32_t ie = (fl & GDN_QKV_BF16) ? 2u : 4u;
+      const uint32_t rowb = static_cast<uint32_t>(D) * ie;
+      if (fl & GDN_FUSE_CONV) {
+        const unsigned char* row = static_cast<const unsigned char*>(p.mixed) +
+                                   static_cast<size_t>(bp) * p.channels * ie;
+        const size_t HD = static_cast<size_t>(p.H) * D;
+        bulk_prefetch_l2(row + static_cast<size_t>(hp) * D * ie, rowb);
+        bulk_prefetch_l2(row + (HD + static_cast<size_t>(hp) * D) * ie, rowb);
+        bulk_prefetch_l2(row + (2 * HD + static_cast<size_t>(hp) * D) * ie, rowb);
+      } else {
+        const size_t off = static_cast<size_t>(gp) * D * ie;
+        bulk_prefetch_l2(static_cast<const unsigned char*>(p.q) + off, rowb);
+        bulk_prefetch_l2(static_cast<const unsigned char*>(p.k) + off, rowb);
+        bulk_prefetch_l2(static_cast<const unsigned char*>(p.v) + off, rowb);
+      }
+    }
   }
 
   // ---- inputs, norms, gates ----------------------------------------------------
@@ -232,6 +253,34 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
   }
   __syncthreads();  // (C)
 
+  // log replay coefficients: one warp per entry, w_i = D(ell' - Lambda_i) K_i,
+  // c^k_i = k.w_i, c^q_i = q.w_i (warp-shuffle sums); needs only q, k and the log
+  auto replay_coefficients = [&]() {
+    if (MODE == MODE_DENSE || n == 0) return;
+    if (!mbar_wait(&bars[NCHUNK], 0u)) timeout = true;
+    for (int e = warp; e < n; e += NW) {
+      const float* lam_e = p.lam_log + (sh * C + e) * dlam;
+      const float fscal = (dlam == 1) ? expf(ellp_s[0] - lam_s[e]) : 0.0f;
+      float ck = 0.0f, cq = 0.0f;
+      for (int d = lane; d < D; d += 32) {
+        const float kv = (klb == 2)
+                             ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(uni)[e * D + d])
+                             : reinterpret_cast<const float*>(uni)[e * D + d];
+        const float wgt = (dlam == 1) ? fscal : expf(ellp_s[d] - __ldg(lam_e + d));
+        const float wd = wgt * kv;
+        ck = fmaf(k_s[d], wd, ck);
+        cq = fmaf(q_s[d], wd, cq);
+        if (is_merge) kd_s[d * cp + e] = wd;
+      }
+      ck = warp_sum(ck);
+      cq = warp_sum(cq);
+      if (lane == 0) {
+        ck_s[e] = ck;
+        cq_s[e] = cq;
+      }
+    }
+  };
+
   // ---- phase 1: r_k = S^T (e^{ell'} k), r_q = S^T (e^{ell'} q), one pass --------
   const int c4 = lane % VPR, rsub = lane / VPR;
   const float4* tile4 = reinterpret_cast<const float4*>(tile);
@@ -255,33 +304,10 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
         aq[3] = fmaf(s.w, qd, aq[3]);
       }
     }
+    // the replay coefficients fill the wait for the last chunk
+    if (NCHUNK > 1 && c == NCHUNK - 2) replay_coefficients();
   }
-  // log replay coefficients, off the critical path of the tile pass:
-  if (MODE != MODE_DENSE && n > 0) {
-    if (!mbar_wait(&bars[NCHUNK], 0u)) timeout = true;
-    // one warp per log entry: w_i = D(ell' - Lambda_i) K_i, c^k_i = k.w_i, c^q_i = q.w_i
-    for (int e = warp; e < n; e += NW) {
-      const float* lam_e = p.lam_log + (sh * C + e) * dlam;
-      const float fscal = (dlam == 1) ? expf(ellp_s[0] - lam_s[e]) : 0.0f;
-      float ak = 0.0f, aq = 0.0f;
-      for (int d = lane; d < D; d += 32) {
-        const float kv = (klb == 2)
-                             ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(uni)[e * D + d])
-                             : reinterpret_cast<const float*>(uni)[e * D + d];
-        const float wgt = (dlam == 1) ? fscal : expf(ellp_s[d] - __ldg(lam_e + d));
-        const float wd = wgt * kv;
-        ak = fmaf(k_s[d], wd, ak);
-        aq = fmaf(q_s[d], wd, aq);
-        if (is_merge) kd_s[d * cp + e] = wd;
-      }
-      ak = warp_sum(ak);
-      aq = warp_sum(aq);
-      if (lane == 0) {
-        ck_s[e] = ak;
-        cq_s[e] = aq;
-      }
-    }
-  }
+  if (NCHUNK == 1) replay_coefficients();
   if (MODE != MODE_DENSE) __syncthreads();  // the K entries share space with the partial sums
 #pragma unroll
   for (int off = VPR; off < 32; off <<= 1) {
@@ -427,6 +453,16 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+int sm_count(int dev) {
+  static std::atomic<int> cache[kMaxDevices];
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
+    cache[dev].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+
 
 template <int D, int MODE>
 cudaError_t launch_one(const DecodeParams& p, cudaStream_t stream) {
@@ -442,9 +478,26 @@ cudaError_t launch_one(const DecodeParams& p, cudaStream_t stream) {
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(L.total));
     if (err != cudaSuccess) return err;
+    // several 64 KiB-tile CTAs per SM only fit with the whole L1/shared array as shared memory
+    err = cudaFuncSetAttribute(gdn_decode_kernel<D, MODE>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               static_cast<int>(cudaSharedmemCarveoutMaxShared));
+    if (err != cudaSuccess) return err;
     configured[dev].store(L.total, std::memory_order_relaxed);
   }
-  gdn_decode_kernel<D, MODE><<<dim3(static_cast<unsigned>(p.B * p.H)), dim3(NT), L.total, stream>>>(p);
+  // prefetch distance for the token inputs: the number of CTAs resident at once
+  // (cached per device as (shared bytes << 32 | CTAs per SM))
+  static std::atomic<uint64_t> resident[kMaxDevices];
+  uint64_t rc = resident[dev].load(std::memory_order_relaxed);
+  if ((rc >> 32) != L.total) {
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gdn_decode_kernel<D, MODE>, NT, L.total);
+    if (err != cudaSuccess) return err;
+    rc = (static_cast<uint64_t>(L.total) << 32) | static_cast<uint32_t>(per_sm > 0 ? per_sm : 1);
+    resident[dev].store(rc, std::memory_order_relaxed);
+  }
+  DecodeParams q = p;
+  q.prefetch_ahead = static_cast<int>(rc & 0xffffffffu) * sm_count(dev);
+  gdn_decode_kernel<D, MODE><<<dim3(static_cast<unsigned>(p.B * p.H)), dim3(NT), L.total, stream>>>(q);
   return cudaGetLastError();
 }
 
