@@ -8,16 +8,20 @@
 // and the metadata commit needs no second pass).
 //
 // Per CTA:
-//   prologue  TMA bulk copies of the tile (4 row chunks for dk = 128) and of the
-//             first L log entries start at once; meanwhile the threads load q/k/v
-//             (or run the width-4 conv + SiLU), L2-normalise q and k, form the
-//             decays exp(ell') and, for every log entry i < L, the two projection
-//             coefficients  c^k_i = k^T D(ell' - Lambda_i) K_i,  c^q_i = q^T D(...) K_i
+//   prologue  TMA bulk copies of the tile (4 row chunks for dk = 128) start first, then
+//             the copy of the first L log entries as soon as L has been read; meanwhile
+//             the threads load q/k/v (or run the width-4 conv + SiLU) and form the
+//             decays exp(ell').  One barrier, then phase 1 starts.
+//   phase 1   one pass over the tile as chunks land, on the raw vectors:
+//             r_k = S^T (e^{ell'} * k),  r_q = S^T (e^{ell'} * q)  (warp-local sums,
+//             then across warps).  Between the last two chunks the warps form, for
+//             every log entry i < L, the projection coefficients
+//             c^k_i = k^T D(ell' - Lambda_i) K_i,  c^q_i = q^T D(...) K_i
 //             (DeltaLog notes Sec. 2.4, one warp-shuffle reduction per entry).
-//   phase 1   one pass over the tile as chunks land:  r_k = S^T (e^{ell'} * k),
-//             r_q = S^T (e^{ell'} * q)  (warp-local sums, then across warps).
-//   phase 2   per value column j:  vhat = r_k + sum_i c^k_i U_i,  b = beta (v - vhat),
-//             o = r_q + sum_i c^q_i U_i + (q.k) b.   Append commits the new entry.
+//   phase 2   the L2 norms of q and k (and q_scale) are scalars of the head and scale
+//             the reduced sums; per value column j:  vhat = r_k + sum_i c^k_i U_i,
+//             b = beta (v - vhat),  o = r_q + sum_i c^q_i U_i + (q.k) b.
+//             Append commits the new entry.
 //   phase 3   dense / merge only: S' = D(ell') S + sum_i D(ell' - Lambda_i) K_i U_i^T + k b^T,
 //             written back with 16-byte coalesced stores.
 #include <atomic>
@@ -154,109 +158,114 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
     }
   }
 
-  // ---- inputs, norms, gates ----------------------------------------------------
+  // ---- inputs and decays ------------------------------------------------------
+  // Phase 1 runs on the raw q and k times the decays: the L2 norms and q_scale are
+  // scalars of the head, applied to the reduced sums, so the only barrier between
+  // the token loads and the first tile chunk is (A).
   const bool is_q = tid < D;                     // owns q[tid], v[tid], row tid, column tid
   const bool is_k = tid >= 128 && tid < 128 + D;  // owns k[tid - 128]
   const int ii = is_q ? tid : tid - 128;
   float x, vj;
   load_token(p, b, h, slot, tid, &x, &vj);
+  if (MODE != MODE_DENSE && tid == 0) {
+    // the log copy starts as soon as L is known, alongside the token loads
+    int n0 = n_raw;
+    uint32_t bad0 = 0u;
+    if (n0 < 0 || n0 > C)
+      bad0 = GDN_STATUS_BAD_LEN;
+    else if (MODE == MODE_APPEND && n0 == C)
+      bad0 = GDN_STATUS_LOG_FULL;
+    if (bad0) n0 = 0;
+    const uint32_t kbytes = static_cast<uint32_t>(n0 * D * klb);
+    const uint32_t ubytes = static_cast<uint32_t>(n0 * D * 4);
+    mbar_arrive_expect_tx(&bars[NCHUNK], kbytes + ubytes);
+    if (n0 > 0) {
+      bulk_load(uni, static_cast<const unsigned char*>(p.k_log) + sh * C * D * klb, kbytes,
+                &bars[NCHUNK]);
+      bulk_load(u_s, p.u_log + sh * C * D, ubytes, &bars[NCHUNK]);
+      if (dlam == 1)
+        for (int e = 0; e < n0; ++e) cp_async4(lam_s + e, p.lam_log + sh * C + e);
+    }
+    cp_async_arrive(&bars[NCHUNK]);
+    scal_i[0] = n0;
+    scal_i[1] = static_cast<int>(bad0);
+  }
+  // both owners of key row ii form its decay exp(ell'), ell' = ell + lambda (closure
+  // of the decays; a per-head decay reads entry 0)
+  float lam_t = 0.0f, ell_t = 0.0f;
+  if (is_q || is_k) {
+    const int di = dlam == 1 ? 0 : ii;
+    lam_t = __ldg(p.lam + (static_cast<size_t>(b) * p.H + h) * dlam + di);
+    if (fl & GDN_GATE_RAW) lam_t = log_sigmoidf_(lam_t);
+    if (MODE != MODE_DENSE) ell_t = p.ell[sh * dlam + di];
+  }
+  float beta = __ldg(p.beta + static_cast<size_t>(b) * p.H + h);
+  if (fl & GDN_GATE_RAW) beta = sigmoidf_(beta);
   {
     const float ss = warp_sum(x * x);
     if (lane == 0) scal_f[warp] = ss;
   }
-  float lam_t = 0.0f, ell_t = 0.0f;
-  if (tid < dlam) {
-    lam_t = __ldg(p.lam + (static_cast<size_t>(b) * p.H + h) * dlam + tid);
-    if (fl & GDN_GATE_RAW) lam_t = log_sigmoidf_(lam_t);
-    if (MODE != MODE_DENSE) ell_t = p.ell[sh * dlam + tid];
+  const float ellp = ell_t + lam_t;
+  if (is_q) {
+    const float dcy = expf(ellp);
+    q_s[ii] = x;
+    qdec_s[ii] = x * dcy;
+    if (MODE != MODE_APPEND) dec_s[ii] = dcy;
+    if (ii < dlam) ellp_s[ii] = ellp;
+  } else if (is_k) {
+    k_s[ii] = x;
+    kdec_s[ii] = x * expf(ellp);
   }
-  float beta = __ldg(p.beta + static_cast<size_t>(b) * p.H + h);
-  if (fl & GDN_GATE_RAW) beta = sigmoidf_(beta);
-  __syncthreads();  // (A) norm partials
+  __syncthreads();  // (A) raw and decayed q, k, decays, norm partials, L and status bits
 
-  if (tid == 0) {
-    int n0 = 0;
-    uint32_t bad0 = 0u;
-    if (MODE != MODE_DENSE) {
-      n0 = n_raw;
-      if (n0 < 0 || n0 > C)
-        bad0 = GDN_STATUS_BAD_LEN;
-      else if (MODE == MODE_APPEND && n0 == C)
-        bad0 = GDN_STATUS_LOG_FULL;
-      if (bad0) n0 = 0;
-      const uint32_t kbytes = static_cast<uint32_t>(n0 * D * klb);
-      const uint32_t ubytes = static_cast<uint32_t>(n0 * D * 4);
-      mbar_arrive_expect_tx(&bars[NCHUNK], kbytes + ubytes);
-      if (n0 > 0) {
-        bulk_load(uni, static_cast<const unsigned char*>(p.k_log) + sh * C * D * klb, kbytes,
-                  &bars[NCHUNK]);
-        bulk_load(u_s, p.u_log + sh * C * D, ubytes, &bars[NCHUNK]);
-        if (dlam == 1)
-          for (int e = 0; e < n0; ++e) cp_async4(lam_s + e, p.lam_log + sh * C + e);
-      }
-      cp_async_arrive(&bars[NCHUNK]);
-    }
-    scal_i[0] = n0;
-    scal_i[1] = static_cast<int>(bad0);
-  }
-
-  const float qss = scal_f[0] + scal_f[1] + scal_f[2] + scal_f[3];
-  const float kss = scal_f[4] + scal_f[5] + scal_f[6] + scal_f[7];
-  const bool l2 = (fl & GDN_NO_QK_L2NORM) == 0u;
-  const float qinv = l2 ? 1.0f / sqrtf(qss + p.l2_eps) : 1.0f;
-  const float kinv = l2 ? 1.0f / sqrtf(kss + p.l2_eps) : 1.0f;
-  float kn = 0.0f;
-  if (is_q) q_s[ii] = x * qinv * p.q_scale;
-  if (is_k) {
-    kn = x * kinv;
-    k_s[ii] = kn;
-  }
-  if (tid < dlam) ellp_s[tid] = ell_t + lam_t;  // ell' = ell + lambda (closure of the decays)
-  __syncthreads();  // (B) n, status bits, q, k, ell'
-
-  const int n = scal_i[0];
-  const uint32_t bad = static_cast<uint32_t>(scal_i[1]);
+  const int n = (MODE == MODE_DENSE) ? 0 : scal_i[0];
+  const uint32_t bad = (MODE == MODE_DENSE) ? 0u : static_cast<uint32_t>(scal_i[1]);
   if (bad) {  // skip the slot-head: wait for this CTA's own copies, then leave
 #pragma unroll
     for (int c = 0; c < NCHUNK; ++c) (void)mbar_wait(&bars[c], 0u);
+    (void)mbar_wait(&bars[NCHUNK], 0u);
     if (tid == 0) atomic_status(p.status, bad);
     return;
   }
+  const float qss = scal_f[0] + scal_f[1] + scal_f[2] + scal_f[3];
+  const float kss = scal_f[4] + scal_f[5] + scal_f[6] + scal_f[7];
+  const bool l2 = (fl & GDN_NO_QK_L2NORM) == 0u;
+  const float kinv = l2 ? 1.0f / sqrtf(kss + p.l2_eps) : 1.0f;
+  const float qsc = (l2 ? 1.0f / sqrtf(qss + p.l2_eps) : 1.0f) * p.q_scale;
+
   if (fl & GDN_FUSE_CONV) conv_commit(p, b, h, slot, tid);
 
   const bool is_merge = (MODE == MODE_MERGE) || (MODE == MODE_STEP && n == C);
   const bool is_append = (MODE == MODE_APPEND) || (MODE == MODE_STEP && n < C);
   bool timeout = false;
 
-  if (is_q) {  // decays of key row tid
-    const float dcy = expf(ellp_s[dlam == 1 ? 0 : tid]);
-    qdec_s[tid] = q_s[tid] * dcy;
-    kdec_s[tid] = k_s[tid] * dcy;
-    if (MODE != MODE_APPEND) dec_s[tid] = dcy;
-  }
-  if (is_merge) {
-    // the current update enters the merge at weight D(0) = I; pad the tables with zeros
-    for (int idx = tid; idx < D * cp; idx += NT) {
-      const int d = idx / cp, e = idx - d * cp;
-      if (e == n)
-        kd_s[idx] = k_s[d];
-      else if (e > n)
-        kd_s[idx] = 0.0f;
-    }
-    for (int idx = tid; idx < (cp - n - 1) * D; idx += NT) u_s[(n + 1) * D + idx] = 0.0f;
-  }
-  if (warp == 0) {
+  // q.k of the raw vectors (the last warp has the fewest log entries to replay)
+  auto qk_dot = [&]() {
+    if (warp != NW - 1) return;
     float t = 0.0f;
+#pragma unroll
     for (int d = lane; d < D; d += 32) t = fmaf(q_s[d], k_s[d], t);
     t = warp_sum(t);
     if (lane == 0) scal_f[8] = t;
-  }
-  __syncthreads();  // (C)
+  };
 
   // log replay coefficients: one warp per entry, w_i = D(ell' - Lambda_i) K_i,
   // c^k_i = k.w_i, c^q_i = q.w_i (warp-shuffle sums); needs only q, k and the log
   auto replay_coefficients = [&]() {
-    if (MODE == MODE_DENSE || n == 0) return;
+    if (MODE == MODE_DENSE) return;
+    if (is_merge) {
+      // the current update enters the merge at weight D(0) = I with the normalised
+      // key; pad the tables with zeros
+      for (int idx = tid; idx < D * cp; idx += NT) {
+        const int d = idx / cp, e = idx - d * cp;
+        if (e == n)
+          kd_s[idx] = k_s[d] * kinv;
+        else if (e > n)
+          kd_s[idx] = 0.0f;
+      }
+      for (int idx = tid; idx < (cp - n - 1) * D; idx += NT) u_s[(n + 1) * D + idx] = 0.0f;
+    }
+    if (n == 0) return;
     if (!mbar_wait(&bars[NCHUNK], 0u)) timeout = true;
     for (int e = warp; e < n; e += NW) {
       const float* lam_e = p.lam_log + (sh * C + e) * dlam;
@@ -275,8 +284,8 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
       ck = warp_sum(ck);
       cq = warp_sum(cq);
       if (lane == 0) {
-        ck_s[e] = ck;
-        cq_s[e] = cq;
+        ck_s[e] = ck * kinv;
+        cq_s[e] = cq * qsc;
       }
     }
   };
@@ -305,9 +314,15 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
       }
     }
     // the replay coefficients fill the wait for the last chunk
-    if (NCHUNK > 1 && c == NCHUNK - 2) replay_coefficients();
+    if (NCHUNK > 1 && c == NCHUNK - 2) {
+      replay_coefficients();
+      qk_dot();
+    }
   }
-  if (NCHUNK == 1) replay_coefficients();
+  if (NCHUNK == 1) {
+    replay_coefficients();
+    qk_dot();
+  }
   if (MODE != MODE_DENSE) __syncthreads();  // the K entries share space with the partial sums
 #pragma unroll
   for (int off = VPR; off < 32; off <<= 1) {
@@ -354,13 +369,17 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
     rq += red[3 * D + j];
     rq += red[5 * D + j];
     rq += red[7 * D + j];
+    // the sums ran on the raw vectors; an explicit rounded product keeps every mode
+    // (with or without log terms after it) on the same arithmetic
+    rk = __fmul_rn(rk, kinv);
+    rq = __fmul_rn(rq, qsc);
     for (int e = 0; e < n; ++e) {
       const float u = u_s[e * D + j];
       rk = fmaf(ck_s[e], u, rk);
       rq = fmaf(cq_s[e], u, rq);
     }
     const float bj = (fl & GDN_PLAIN_UPDATE) ? beta * vj : beta * (vj - rk);
-    const float oj = fmaf(scal_f[8], bj, rq);
+    const float oj = fmaf(scal_f[8] * qsc * kinv, bj, rq);
     p.o[(static_cast<size_t>(b) * p.H + h) * D + j] = oj;
     b_s[j] = bj;
     if (is_append)
@@ -369,7 +388,7 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
   }
   if (is_append) {
     if (is_k) {
-      const float kval = (fl & GDN_KLOG_PRENORM) ? x : kn;
+      const float kval = (fl & GDN_KLOG_PRENORM) ? x : x * kinv;
       const size_t at = (sh * C + n) * D + ii;
       if (klb == 2)
         reinterpret_cast<__nv_bfloat16*>(p.k_log)[at] = __float2bfloat16_rn(kval);
@@ -398,7 +417,7 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
         const int r = it * RPI + warp * RPW + rsub;
         if (r < D) {
           const float4 s = tile4[r * VPR + c4];
-          const float dc = dec_s[r], kk = k_s[r];
+          const float dc = dec_s[r], kk = k_s[r] * kinv;
           float4 o4;
           o4.x = fmaf(kk, bb.x, dc * s.x);
           o4.y = fmaf(kk, bb.y, dc * s.y);
