@@ -68,8 +68,10 @@ __host__ __device__ inline Layout decode_layout(int mode, int D, int C, int klog
   return L;
 }
 
+// The auto step carries both paths; its register cap keeps two CTAs per SM (its shared
+// memory allows two).  The other modes take no minimum (0: none).
 template <int D, int MODE>
-__global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
 
   constexpr int NCHUNK = (D >= 128) ? 4 : 1;       // TMA row chunks of the tile
@@ -83,6 +85,7 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
   static_assert(NCHUNK == 1 || (NIT % NCHUNK == 0 && CHUNK_ROWS % RPI == 0), "chunking");
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool ctrl = warp == NW;  // the copy-issuing warp; warps 0..NW-1 compute
   const int b = blockIdx.x / p.H;
   const int h = blockIdx.x - b * p.H;
   const int slot = __ldg(p.slot + b);
@@ -119,89 +122,95 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
   const size_t sh = static_cast<size_t>(slot) * p.H + h;
   const float* tile_g = p.state + sh * static_cast<size_t>(D * D);
 
-  // ---- prologue: start every asynchronous copy first -------------------------
-  // the log length is loaded now and first used after barrier (A), so the load's
-  // latency overlaps the input loads instead of holding the CTA at the barrier
-  const int n_raw = (MODE != MODE_DENSE && tid == 0) ? p.len[sh] : 0;
-  if (tid == 0) {
-    for (int c = 0; c < NCHUNK; ++c) mbar_init(&bars[c], 1u);
-    mbar_init(&bars[NCHUNK], 2u);  // log entries: TMA bytes + the cp.async snapshots
-    fence_mbar_init();
-    const uint64_t pol = l2_policy_evict_first();
-    const uint32_t starve = (fl & GDN_TEST_STARVE_WAIT) ? 16u : 0u;
-#pragma unroll
-    for (int c = 0; c < NCHUNK; ++c) {
-      mbar_arrive_expect_tx(&bars[c], CHUNK_BYTES + (c == 0 ? starve : 0u));
-      bulk_load_hint(tile + c * CHUNK_ROWS * D, tile_g + c * CHUNK_ROWS * D, CHUNK_BYTES, &bars[c],
-                     pol);
-    }
-    // the CTA that runs about one resident wave later finds its token inputs in L2
-    // (they depend only on (request, head); the state tile depends on the slot)
-    const int gp = static_cast<int>(blockIdx.x) + p.prefetch_ahead;
-    if (p.prefetch_ahead > 0 && gp < p.B * p.H) {
-      const int bp = gp / p.H, hp = gp - bp * p.H;
-      const uint32_t ie = (fl & GDN_QKV_BF16) ? 2u : 4u;
-      const uint32_t rowb = static_cast<uint32_t>(D) * ie;
-      if (fl & GDN_FUSE_CONV) {
-        const unsigned char* row = static_cast<const unsigned char*>(p.mixed) +
-                                   static_cast<size_t>(bp) * p.channels * ie;
-        const size_t HD = static_cast<size_t>(p.H) * D;
-        bulk_prefetch_l2(row + static_cast<size_t>(hp) * D * ie, rowb);
-        bulk_prefetch_l2(row + (HD + static_cast<size_t>(hp) * D) * ie, rowb);
-        bulk_prefetch_l2(row + (2 * HD + static_cast<size_t>(hp) * D) * ie, rowb);
-      } else {
-        const size_t off = static_cast<size_t>(gp) * D * ie;
-        bulk_prefetch_l2(static_cast<const unsigned char*>(p.q) + off, rowb);
-        bulk_prefetch_l2(static_cast<const unsigned char*>(p.k) + off, rowb);
-        bulk_prefetch_l2(static_cast<const unsigned char*>(p.v) + off, rowb);
-      }
-    }
-  }
-
-  // ---- inputs and decays ------------------------------------------------------
-  // Phase 1 runs on the raw q and k times the decays: the L2 norms and q_scale are
-  // scalars of the head, applied to the reduced sums, so the only barrier between
-  // the token loads and the first tile chunk is (A).
+  // ---- prologue -------------------------------------------------------------------
+  // One lane of the copy-issuing warp starts the tile copy (4 row chunks), the L2
+  // prefetch of a later CTA's inputs and, once L has been read, the copy of the first
+  // L log entries; the compute warps meanwhile load q/k/v (or run the width-4 conv +
+  // SiLU) and form the decays.
   const bool is_q = tid < D;                     // owns q[tid], v[tid], row tid, column tid
   const bool is_k = tid >= 128 && tid < 128 + D;  // owns k[tid - 128]
   const int ii = is_q ? tid : tid - 128;
-  float x, vj;
-  load_token(p, b, h, slot, tid, &x, &vj);
-  if (MODE != MODE_DENSE && tid == 0) {
-    // the log copy starts as soon as L is known, alongside the token loads
-    int n0 = n_raw;
-    uint32_t bad0 = 0u;
-    if (n0 < 0 || n0 > C)
-      bad0 = GDN_STATUS_BAD_LEN;
-    else if (MODE == MODE_APPEND && n0 == C)
-      bad0 = GDN_STATUS_LOG_FULL;
-    if (bad0) n0 = 0;
-    const uint32_t kbytes = static_cast<uint32_t>(n0 * D * klb);
-    const uint32_t ubytes = static_cast<uint32_t>(n0 * D * 4);
-    mbar_arrive_expect_tx(&bars[NCHUNK], kbytes + ubytes);
-    if (n0 > 0) {
-      bulk_load(uni, static_cast<const unsigned char*>(p.k_log) + sh * C * D * klb, kbytes,
-                &bars[NCHUNK]);
-      bulk_load(u_s, p.u_log + sh * C * D, ubytes, &bars[NCHUNK]);
-      if (dlam == 1)
-        for (int e = 0; e < n0; ++e) cp_async4(lam_s + e, p.lam_log + sh * C + e);
+  float x = 0.0f, vj = 0.0f;
+  if (ctrl) {
+    const int n_raw = (MODE != MODE_DENSE && lane == 0) ? p.len[sh] : 0;
+    if (lane == 0) {
+      for (int c = 0; c < NCHUNK; ++c) mbar_init(&bars[c], 1u);
+      mbar_init(&bars[NCHUNK], 32u);  // log entries: one cp.async arrival per lane
+      fence_mbar_init();
+      const uint64_t pol = l2_policy_evict_first();
+      const uint32_t starve = (fl & GDN_TEST_STARVE_WAIT) ? 16u : 0u;
+#pragma unroll
+      for (int c = 0; c < NCHUNK; ++c) {
+        mbar_arrive_expect_tx(&bars[c], CHUNK_BYTES + (c == 0 ? starve : 0u));
+        bulk_load_hint(tile + c * CHUNK_ROWS * D, tile_g + c * CHUNK_ROWS * D, CHUNK_BYTES, &bars[c],
+                       pol);
+      }
     }
-    cp_async_arrive(&bars[NCHUNK]);
-    scal_i[0] = n0;
-    scal_i[1] = static_cast<int>(bad0);
+    __syncwarp();  // the log barrier is initialised
+    if (MODE != MODE_DENSE) {
+      // all C log entries, whatever L is: the copy does not wait for L, and entries
+      // past L are never read (the log of a slot-head is C entries long)
+      const uint4* ksrc = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(p.k_log) +
+                                                         sh * C * D * klb);
+      const uint4* usrc = reinterpret_cast<const uint4*>(p.u_log + sh * C * D);
+      const int kvec = C * D * klb / 16, uvec = C * D * 4 / 16;
+      for (int i = lane; i < kvec; i += 32) cp_async16(reinterpret_cast<uint4*>(uni) + i, ksrc + i);
+      for (int i = lane; i < uvec; i += 32) cp_async16(reinterpret_cast<uint4*>(u_s) + i, usrc + i);
+      if (dlam == 1)
+        for (int e = lane; e < C; e += 32) cp_async4(lam_s + e, p.lam_log + sh * C + e);
+      cp_async_arrive(&bars[NCHUNK]);
+    }
+    if (lane == 0) {
+      // the CTA that runs about one resident wave later finds its token inputs in L2
+      // (they depend only on (request, head); the state tile depends on the slot)
+      const int gp = static_cast<int>(blockIdx.x) + p.prefetch_ahead;
+      if (p.prefetch_ahead > 0 && gp < p.B * p.H) {
+        const int bp = gp / p.H, hp = gp - bp * p.H;
+        const uint32_t ie = (fl & GDN_QKV_BF16) ? 2u : 4u;
+        const uint32_t rowb = static_cast<uint32_t>(D) * ie;
+        if (fl & GDN_FUSE_CONV) {
+          const unsigned char* row = static_cast<const unsigned char*>(p.mixed) +
+                                     static_cast<size_t>(bp) * p.channels * ie;
+          const size_t HD = static_cast<size_t>(p.H) * D;
+          bulk_prefetch_l2(row + static_cast<size_t>(hp) * D * ie, rowb);
+          bulk_prefetch_l2(row + (HD + static_cast<size_t>(hp) * D) * ie, rowb);
+          bulk_prefetch_l2(row + (2 * HD + static_cast<size_t>(hp) * D) * ie, rowb);
+        } else {
+          const size_t off = static_cast<size_t>(gp) * D * ie;
+          bulk_prefetch_l2(static_cast<const unsigned char*>(p.q) + off, rowb);
+          bulk_prefetch_l2(static_cast<const unsigned char*>(p.k) + off, rowb);
+          bulk_prefetch_l2(static_cast<const unsigned char*>(p.v) + off, rowb);
+        }
+      }
+      if (MODE != MODE_DENSE) {
+        int n0 = n_raw;
+        uint32_t bad0 = 0u;
+        if (n0 < 0 || n0 > C)
+          bad0 = GDN_STATUS_BAD_LEN;
+        else if (MODE == MODE_APPEND && n0 == C)
+          bad0 = GDN_STATUS_LOG_FULL;
+        if (bad0) n0 = 0;
+        scal_i[0] = n0;
+        scal_i[1] = static_cast<int>(bad0);
+      }
+    }
   }
   // both owners of key row ii form its decay exp(ell'), ell' = ell + lambda (closure
-  // of the decays; a per-head decay reads entry 0)
-  float lam_t = 0.0f, ell_t = 0.0f;
+  // of the decays; a per-head decay reads entry 0).  The gate loads are issued before
+  // the token loads so that the two latencies overlap.
+  float lam_t = 0.0f, ell_t = 0.0f, beta = 0.0f;
   if (is_q || is_k) {
     const int di = dlam == 1 ? 0 : ii;
     lam_t = __ldg(p.lam + (static_cast<size_t>(b) * p.H + h) * dlam + di);
-    if (fl & GDN_GATE_RAW) lam_t = log_sigmoidf_(lam_t);
     if (MODE != MODE_DENSE) ell_t = p.ell[sh * dlam + di];
   }
-  float beta = __ldg(p.beta + static_cast<size_t>(b) * p.H + h);
-  if (fl & GDN_GATE_RAW) beta = sigmoidf_(beta);
-  {
+  if (!ctrl) {
+    beta = __ldg(p.beta + static_cast<size_t>(b) * p.H + h);
+    load_token(p, b, h, slot, tid, &x, &vj);
+    if (fl & GDN_GATE_RAW) {
+      lam_t = log_sigmoidf_(lam_t);
+      beta = sigmoidf_(beta);
+    }
     const float ss = warp_sum(x * x);
     if (lane == 0) scal_f[warp] = ss;
   }
@@ -217,6 +226,7 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
     kdec_s[ii] = x * expf(ellp);
   }
   __syncthreads();  // (A) raw and decayed q, k, decays, norm partials, L and status bits
+  if (ctrl) return;  // from here on only the compute warps (named barrier 1)
 
   const int n = (MODE == MODE_DENSE) ? 0 : scal_i[0];
   const uint32_t bad = (MODE == MODE_DENSE) ? 0u : static_cast<uint32_t>(scal_i[1]);
@@ -227,11 +237,14 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
     if (tid == 0) atomic_status(p.status, bad);
     return;
   }
-  const float qss = scal_f[0] + scal_f[1] + scal_f[2] + scal_f[3];
-  const float kss = scal_f[4] + scal_f[5] + scal_f[6] + scal_f[7];
-  const bool l2 = (fl & GDN_NO_QK_L2NORM) == 0u;
-  const float kinv = l2 ? 1.0f / sqrtf(kss + p.l2_eps) : 1.0f;
-  const float qsc = (l2 ? 1.0f / sqrtf(qss + p.l2_eps) : 1.0f) * p.q_scale;
+  float kinv = 1.0f, qsc = 1.0f;
+  auto norms = [&]() {
+    const float qss = scal_f[0] + scal_f[1] + scal_f[2] + scal_f[3];
+    const float kss = scal_f[4] + scal_f[5] + scal_f[6] + scal_f[7];
+    const bool l2 = (fl & GDN_NO_QK_L2NORM) == 0u;
+    kinv = l2 ? 1.0f / sqrtf(kss + p.l2_eps) : 1.0f;
+    qsc = (l2 ? 1.0f / sqrtf(qss + p.l2_eps) : 1.0f) * p.q_scale;
+  };
 
   if (fl & GDN_FUSE_CONV) conv_commit(p, b, h, slot, tid);
 
@@ -253,6 +266,8 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
   // c^k_i = k.w_i, c^q_i = q.w_i (warp-shuffle sums); needs only q, k and the log
   auto replay_coefficients = [&]() {
     if (MODE == MODE_DENSE) return;
+    // the copy covers all C entries: wait for it even when L = 0, and pad only after it
+    if (!mbar_wait(&bars[NCHUNK], 0u)) timeout = true;
     if (is_merge) {
       // the current update enters the merge at weight D(0) = I with the normalised
       // key; pad the tables with zeros
@@ -265,30 +280,38 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
       }
       for (int idx = tid; idx < (cp - n - 1) * D; idx += NT) u_s[(n + 1) * D + idx] = 0.0f;
     }
-    if (n == 0) return;
-    if (!mbar_wait(&bars[NCHUNK], 0u)) timeout = true;
     for (int e = warp; e < n; e += NW) {
       const float* lam_e = p.lam_log + (sh * C + e) * dlam;
-      const float fscal = (dlam == 1) ? expf(ellp_s[0] - lam_s[e]) : 0.0f;
+      // a per-head decay is one factor of the entry, applied to the two sums
+      const float fscal = (dlam == 1) ? expf(ellp_s[0] - lam_s[e]) : 1.0f;
       float ck = 0.0f, cq = 0.0f;
-      for (int d = lane; d < D; d += 32) {
-        const float kv = (klb == 2)
-                             ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(uni)[e * D + d])
-                             : reinterpret_cast<const float*>(uni)[e * D + d];
-        const float wgt = (dlam == 1) ? fscal : expf(ellp_s[d] - __ldg(lam_e + d));
-        const float wd = wgt * kv;
-        ck = fmaf(k_s[d], wd, ck);
-        cq = fmaf(q_s[d], wd, cq);
-        if (is_merge) kd_s[d * cp + e] = wd;
+#pragma unroll
+      for (int i = 0; i < (D + 31) / 32; ++i) {
+        const int d = lane + 32 * i;
+        if (d < D) {
+          const float kv = (klb == 2)
+                               ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(uni)[e * D + d])
+                               : reinterpret_cast<const float*>(uni)[e * D + d];
+          const float wd = (dlam == 1) ? kv : expf(ellp_s[d] - __ldg(lam_e + d)) * kv;
+          ck = fmaf(k_s[d], wd, ck);
+          cq = fmaf(q_s[d], wd, cq);
+          if (is_merge) kd_s[d * cp + e] = (dlam == 1) ? fscal * kv : wd;
+        }
       }
       ck = warp_sum(ck);
       cq = warp_sum(cq);
       if (lane == 0) {
-        ck_s[e] = ck * kinv;
-        cq_s[e] = cq * qsc;
+        ck_s[e] = ck * fscal * kinv;
+        cq_s[e] = cq * fscal * qsc;
       }
     }
   };
+
+  // the log was copied from the start; the norm scales, q.k and the replay
+  // coefficients are formed while the first tile chunks are still in flight
+  norms();
+  replay_coefficients();
+  qk_dot();
 
   // ---- phase 1: r_k = S^T (e^{ell'} k), r_q = S^T (e^{ell'} q), one pass --------
   const int c4 = lane % VPR, rsub = lane / VPR;
@@ -314,16 +337,8 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
       }
     }
     // the replay coefficients fill the wait for the last chunk
-    if (NCHUNK > 1 && c == NCHUNK - 2) {
-      replay_coefficients();
-      qk_dot();
-    }
   }
-  if (NCHUNK == 1) {
-    replay_coefficients();
-    qk_dot();
-  }
-  if (MODE != MODE_DENSE) __syncthreads();  // the K entries share space with the partial sums
+  if (MODE != MODE_DENSE) consumer_sync();  // the K entries share space with the partial sums
 #pragma unroll
   for (int off = VPR; off < 32; off <<= 1) {
 #pragma unroll
@@ -338,7 +353,7 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
     *reinterpret_cast<float4*>(r0) = make_float4(ak[0], ak[1], ak[2], ak[3]);
     *reinterpret_cast<float4*>(r0 + D) = make_float4(aq[0], aq[1], aq[2], aq[3]);
   }
-  __syncthreads();  // (D)
+  consumer_sync();  // (D)
   if (warp < 4 && rsub == 0) {
     float* r0 = red + warp * 2 * D + c4 * 4;
     float4 pk = *reinterpret_cast<float4*>(r0), pq = *reinterpret_cast<float4*>(r0 + D);
@@ -353,7 +368,7 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
     *reinterpret_cast<float4*>(r0) = pk;
     *reinterpret_cast<float4*>(r0 + D) = pq;
   }
-  if (__syncthreads_or(timeout)) {  // (E)
+  if (consumer_sync_or(timeout)) {  // (E)
     if (tid == 0) atomic_status(p.status, GDN_STATUS_TIMEOUT);
     return;
   }
@@ -407,7 +422,7 @@ __global__ void __launch_bounds__(NT) gdn_decode_kernel(const DecodeParams p) {
 
   // ---- phase 3: write the state (dense) or fold the log into the base (merge) ------
   if (MODE == MODE_DENSE || is_merge) {
-    __syncthreads();  // (F) b and the current entry are in shared memory
+    consumer_sync();  // (F) b and the current entry are in shared memory
     float* out = p.state + sh * static_cast<size_t>(D * D);
     float4* tilew = reinterpret_cast<float4*>(tile);
     if (MODE == MODE_DENSE) {
@@ -509,14 +524,15 @@ cudaError_t launch_one(const DecodeParams& p, cudaStream_t stream) {
   uint64_t rc = resident[dev].load(std::memory_order_relaxed);
   if ((rc >> 32) != L.total) {
     int per_sm = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gdn_decode_kernel<D, MODE>, NT, L.total);
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gdn_decode_kernel<D, MODE>, NT_DECODE,
+                                                        L.total);
     if (err != cudaSuccess) return err;
     rc = (static_cast<uint64_t>(L.total) << 32) | static_cast<uint32_t>(per_sm > 0 ? per_sm : 1);
     resident[dev].store(rc, std::memory_order_relaxed);
   }
   DecodeParams q = p;
   q.prefetch_ahead = static_cast<int>(rc & 0xffffffffu) * sm_count(dev);
-  gdn_decode_kernel<D, MODE><<<dim3(static_cast<unsigned>(p.B * p.H)), dim3(NT), L.total, stream>>>(q);
+  gdn_decode_kernel<D, MODE><<<dim3(static_cast<unsigned>(p.B * p.H)), dim3(NT_DECODE), L.total, stream>>>(q);
   return cudaGetLastError();
 }
 

@@ -12,8 +12,9 @@
 
 namespace gdn {
 
-constexpr int NT = 256;  // threads per CTA
+constexpr int NT = 256;  // threads per CTA (decode: the compute threads)
 constexpr int NW = NT / 32;
+constexpr int NT_DECODE = NT + 32;  // decode CTA: NW compute warps and one copy-issuing warp
 
 // Upper bound, in SM clock cycles, on any wait for an asynchronous copy
 // (about a second at GB300 clocks). A copy that has not landed by then is
@@ -57,10 +58,10 @@ __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Named barrier 1 over the 256 consumer threads (the producer warp never joins it).
+// Named barrier 1 over the 256 compute threads (the copy-issuing warp never joins it).
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-// consumer_sync() that also returns the OR of `pred` over the consumer threads.
+// consumer_sync() that also returns the OR of `pred` over the compute threads.
 __device__ __forceinline__ bool consumer_sync_or(bool pred) {
   uint32_t r;
   asm volatile(
@@ -107,6 +108,11 @@ __device__ __forceinline__ void bulk_load_hint(void* dst, const void* src, uint3
 // Ampere-style asynchronous 4-byte copy global -> shared (no register round trip).
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
+// 16-byte asynchronous copy global -> shared through L2 (both addresses 16-byte aligned).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
 
 // One arrival on `bar` once every cp.async this thread issued so far has landed.
