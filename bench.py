@@ -296,11 +296,16 @@ def run_gpu(args, rank, local_rank, world):
             per.setdefault(k, []).append(a.elapsed_time(b) / 1e3)
         return elapsed, per
 
-    # ---- warm both modes, then the timed regions (clocks sampled meanwhile)
-    res = {}
+    # ---- warm both modes, then the timed regions (clocks sampled meanwhile). The
+    # throughput comes from launches back to back (nothing between them, so a launch can
+    # overlap the tail of the previous one); the per-kernel durations from a second
+    # region with an event pair around every launch (which serialises the launches).
+    res, per = {}, {}
     with ClockSampler(local_rank) as clocks:
-        res["deltalog"] = timed("deltalog", args.steps, args.warmup, per_kernel=True)
-        res["dense"] = timed("dense", args.steps, args.warmup, per_kernel=True)
+        res["deltalog"] = timed("deltalog", args.steps, args.warmup, per_kernel=False)
+        res["dense"] = timed("dense", args.steps, args.warmup, per_kernel=False)
+        per["deltalog"] = timed("deltalog", args.steps, args.warmup, per_kernel=True)
+        per["dense"] = timed("dense", args.steps, args.warmup, per_kernel=True)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} during the benchmark")
 
@@ -315,7 +320,7 @@ def run_gpu(args, rank, local_rank, world):
     }
     kernels = {}
     for mode in ("deltalog", "dense"):
-        for k, durs in res[mode][1].items():
+        for k, durs in per[mode][1].items():
             tot = float(np.sum(durs))
             avg = tot / len(durs)
             achieved = bytes_per_launch[k] / avg / 1e9
@@ -339,21 +344,23 @@ def run_gpu(args, rank, local_rank, world):
     modes["speedup_deltalog_vs_dense"] = value / (du / dt)
 
     # dominant kernel of the timed DeltaLog cycle: largest share of device time
-    dom = max(res["deltalog"][1], key=lambda k: kernels[k]["total_ms"])
+    dom = max(per["deltalog"][1], key=lambda k: kernels[k]["total_ms"])
     kd = kernels[dom]
     traffic = profiled_traffic(dom, args.workload)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": kd["achieved_gbs"], "peak": peak,
                 "peak_kind": f"{peak_kind} (hbm_gbs of MEASURED_PEAKS.json)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s", "unit": "GB/s", "frac": kd["achieved_gbs"] / peak,
                 "traffic": traffic,
-                "algorithmic_bytes_per_launch": kd["algorithmic_bytes_per_launch"]}
+                "algorithmic_bytes_per_launch": kd["algorithmic_bytes_per_launch"],
+                "duration": "CUDA events around every launch of the second timed region "
+                            "(serialised launches: no overlap with the previous grid)"}
 
     # ---- end to end through the public API: pinned host inputs in, o back to pinned host
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, w, M, dims_log, pools_l, host_ring, slot, conv_w, dev, stream, gdn)
 
-    launches = args.steps * M * 2 + (e2e["launches"] if e2e else 0)
+    launches = args.steps * M * 4 + (e2e["launches"] if e2e else 0)
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": lt / args.steps * 1e3, "higher_is_better": True,
@@ -390,15 +397,44 @@ def _views(buf, offs, like: dict):
             for k, t in like.items()}
 
 
+class _Cudart:
+    """The few CUDA runtime calls the end-to-end loop issues per step, bound through
+    ctypes (the runtime the decode library itself links), so the host side of a step
+    costs a handful of microseconds."""
+    H2D, D2H = 1, 2
+
+    def __init__(self):
+        self.lib = ctypes.CDLL("libcudart.so.13")
+        for name, args in (("cudaMemcpyAsync", [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                                 ctypes.c_int, ctypes.c_void_p]),
+                           ("cudaEventRecord", [ctypes.c_void_p, ctypes.c_void_p]),
+                           ("cudaStreamWaitEvent", [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]),
+                           ("cudaEventCreateWithFlags", [ctypes.c_void_p, ctypes.c_uint]),
+                           ("cudaEventDestroy", [ctypes.c_void_p])):
+            fn = getattr(self.lib, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+
+    def event(self):
+        e = ctypes.c_void_p()
+        self._ok(self.lib.cudaEventCreateWithFlags(ctypes.byref(e), 2), "cudaEventCreateWithFlags")
+        return e
+
+    @staticmethod
+    def _ok(rc, what):
+        if rc != 0:
+            raise RuntimeError(f"{what} failed with CUDA error {rc}")
+
+
 def run_e2e(args, w, M, dims, pools, host_ring, slot, conv_w, dev, stream, gdn):
-    """Same metric through the public Python API with host buffers. Every decode step
-    copies its inputs (one packed pinned buffer: q/k/v or the conv input, log-decay,
-    beta) host -> device, runs the decode call, and copies o back to pinned host memory.
-    The copies run on their own streams, double-buffered against the decode kernels
-    (event-ordered), the way a serving loop overlaps the next token's upload and the
-    last token's readback with the current step."""
+    """Same metric through the C ABI with host buffers. Every decode step copies its
+    inputs (one packed pinned buffer: q/k/v or the conv input, log-decay, beta) host ->
+    device, runs the decode call, and copies o back to pinned host memory. The copies
+    run on their own streams, double-buffered against the decode kernels and ordered by
+    events, the way a serving loop overlaps the next token's upload and the last token's
+    readback with the current step."""
     import torch
-    names = list(host_ring[0].keys())
+    rt = _Cudart()
     offs, nbytes = _packed(host_ring[0])
     host_packed = []
     for src in host_ring:
@@ -419,32 +455,44 @@ def run_e2e(args, w, M, dims, pools, host_ring, slot, conv_w, dev, stream, gdn):
     gdn.slot_reset(dims, slot, w.batch, log, pools.conv, None, stream=stream)
     s_in = torch.cuda.Stream(dev)
     s_out = torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_k = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [torch.cuda.Event() for _ in range(2)]
+    sc, si, so = (ctypes.c_void_p(x.cuda_stream) for x in (stream, s_in, s_out))
+    ev_in = [rt.event() for _ in range(2)]
+    ev_k = [rt.event() for _ in range(2)]
+    ev_out = [rt.event() for _ in range(2)]
+    lib = gdn._abi.load()
+    P = ctypes.byref
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    # the decode calls' arguments, built once: (entry point, inputs, o) per buffer parity
+    base_ptr, st_ptr = ctypes.c_void_p(pools.state.data_ptr()), ctypes.c_void_p(status.data_ptr())
+    calls = [[(lib.gdn_decode_append if j < M - 1 else lib.gdn_decode_merge, P(inputs[b]),
+               ctypes.c_void_p(o[b].data_ptr())) for j in range(M)] for b in range(2)]
+    hp = [ctypes.c_void_p(t.data_ptr()) for t in host_packed]
+    sp = [ctypes.c_void_p(t.data_ptr()) for t in stage]
+    op = [ctypes.c_void_p(t.data_ptr()) for t in o]
+    ohp = [ctypes.c_void_p(t.data_ptr()) for t in o_host]
+    dims_p, log_p = P(dims), P(log)
     steps, r, launches = args.e2e_steps or args.steps, 0, 0
-    del names
+    memcpy, record, wait = rt.lib.cudaMemcpyAsync, rt.lib.cudaEventRecord, rt.lib.cudaStreamWaitEvent
 
     def one_cycle():
         nonlocal r, launches
         for j in range(M):
             b = r & 1
-            # upload step r into stage[b] once kernel r-2 has consumed it
             if r >= 2:
-                s_in.wait_event(ev_k[b])
-            with torch.cuda.stream(s_in):
-                stage[b].copy_(host_packed[r % RING], non_blocking=True)
-            ev_in[b].record(s_in)
-            stream.wait_event(ev_in[b])
+                wait(si, ev_k[b], 0)                  # kernel r-2 has consumed stage[b]
+            memcpy(sp[b], hp[r % RING], h2d, rt.H2D, si)
+            record(ev_in[b], si)
+            wait(sc, ev_in[b], 0)
             if r >= 2:
-                stream.wait_event(ev_out[b])      # o[b] of step r-2 has been read back
-            call = gdn.decode_append if j < M - 1 else gdn.decode_merge
-            call(dims, inputs[b], pools.state, log, o[b], stream=stream)
-            ev_k[b].record(stream)
-            s_out.wait_event(ev_k[b])
-            with torch.cuda.stream(s_out):
-                o_host[b].copy_(o[b], non_blocking=True)
-            ev_out[b].record(s_out)
+                wait(sc, ev_out[b], 0)                # o[b] of step r-2 has been read back
+            fn, inp, optr = calls[b][j]
+            rc = fn(dims_p, inp, base_ptr, log_p, optr, st_ptr, sc)
+            if rc:
+                gdn._abi.check(rc, "decode")
+            record(ev_k[b], sc)
+            wait(so, ev_k[b], 0)
+            memcpy(ohp[b], op[b], d2h, rt.D2H, so)
+            record(ev_out[b], so)
             r += 1
             launches += 1
 
@@ -462,19 +510,23 @@ def run_e2e(args, w, M, dims, pools, host_ring, slot, conv_w, dev, stream, gdn):
     for _ in range(steps):
         one_cycle()
     for e in ev_out:
-        stream.wait_event(e)
+        wait(sc, e, 0)
     t1.record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
     barrier()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the end-to-end run")
     if not bool(torch.isfinite(o_host[(r - 1) & 1]).all()):
         raise RuntimeError("non-finite output read back in the end-to-end run")
+    for e in ev_in + ev_k + ev_out:
+        rt.lib.cudaEventDestroy(e)
     el, units = reduce_timing(t0.elapsed_time(t1) / 1e3, w.batch * w.num_heads * M * steps, device=dev)
     return {"value": units / el, "unit": UNIT, "h2d_bytes_per_step": h2d * M,
             "d2h_bytes_per_step": d2h * M, "steps": steps, "launches": launches,
             "host_wall_s": wall, "device_s": el,
-            "pipeline": "H2D / decode / D2H on three streams, double-buffered",
-            "api": "linear_attention_decode_gdn_gb300.decode_append / decode_merge (C ABI)"}
+            "pipeline": "H2D / decode / D2H on three streams, double-buffered, event-ordered",
+            "api": "gdn_decode_append / gdn_decode_merge (C ABI), host copies through the CUDA runtime"}
 
 
 # ----------------------------------------------------------------------------- CPU oracle

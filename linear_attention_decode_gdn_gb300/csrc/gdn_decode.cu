@@ -88,6 +88,23 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
   const bool ctrl = warp == NW;  // the copy-issuing warp; warps 0..NW-1 compute
   const int b = blockIdx.x / p.H;
   const int h = blockIdx.x - b * p.H;
+
+  // Launched with programmatic stream serialisation: the first resident wave of CTAs may
+  // start while the previous launch in the stream is finishing.  Until griddep_wait() a
+  // CTA reads nothing that launch may write and only warms L2: the slot is read as a hint
+  // (bounds-checked, used for the prefetch address alone) and the state tile prefetched,
+  // so the tail of the previous grid overlaps this grid's first HBM reads.  Later waves
+  // start after the previous grid has ended; for them the prefetch would only duplicate
+  // their tile copy.
+  if (ctrl && lane == 0 && static_cast<int>(blockIdx.x) < p.prefetch_ahead) {
+    const int hint = *static_cast<const volatile int*>(p.slot + b);
+    if (hint >= 0 && hint < p.num_slots)
+      bulk_prefetch_l2(p.state + (static_cast<size_t>(hint) * p.H + h) * static_cast<size_t>(D * D),
+                       static_cast<uint32_t>(D * D * 4));
+  }
+  griddep_launch_dependents();
+  griddep_wait();
+
   const int slot = __ldg(p.slot + b);
   if (slot < 0) return;  // padding request
   if (slot >= p.num_slots) {
@@ -148,16 +165,22 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
     }
     __syncwarp();  // the log barrier is initialised
     if (MODE != MODE_DENSE) {
-      // all C log entries, whatever L is: the copy does not wait for L, and entries
-      // past L are never read (the log of a slot-head is C entries long)
+      // A merge replays the whole log (L = C), so it copies all C entries at once; the
+      // other modes copy the first L as soon as L has been read (entries past L are
+      // stale and never read).
+      int nc = C;
+      if (MODE != MODE_MERGE) {
+        nc = __shfl_sync(0xffffffffu, n_raw, 0);
+        nc = nc < 0 ? 0 : (nc > C ? C : nc);
+      }
       const uint4* ksrc = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(p.k_log) +
                                                          sh * C * D * klb);
       const uint4* usrc = reinterpret_cast<const uint4*>(p.u_log + sh * C * D);
-      const int kvec = C * D * klb / 16, uvec = C * D * 4 / 16;
+      const int kvec = nc * D * klb / 16, uvec = nc * D * 4 / 16;
       for (int i = lane; i < kvec; i += 32) cp_async16(reinterpret_cast<uint4*>(uni) + i, ksrc + i);
       for (int i = lane; i < uvec; i += 32) cp_async16(reinterpret_cast<uint4*>(u_s) + i, usrc + i);
       if (dlam == 1)
-        for (int e = lane; e < C; e += 32) cp_async4(lam_s + e, p.lam_log + sh * C + e);
+        for (int e = lane; e < nc; e += 32) cp_async4(lam_s + e, p.lam_log + sh * C + e);
       cp_async_arrive(&bars[NCHUNK]);
     }
     if (lane == 0) {
@@ -266,7 +289,8 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
   // c^k_i = k.w_i, c^q_i = q.w_i (warp-shuffle sums); needs only q, k and the log
   auto replay_coefficients = [&]() {
     if (MODE == MODE_DENSE) return;
-    // the copy covers all C entries: wait for it even when L = 0, and pad only after it
+    // wait for the log copy even when L = 0 (a merge copies all C entries), and pad
+    // the merge tables only after it
     if (!mbar_wait(&bars[NCHUNK], 0u)) timeout = true;
     if (is_merge) {
       // the current update enters the merge at weight D(0) = I with the normalised
@@ -532,7 +556,19 @@ cudaError_t launch_one(const DecodeParams& p, cudaStream_t stream) {
   }
   DecodeParams q = p;
   q.prefetch_ahead = static_cast<int>(rc & 0xffffffffu) * sm_count(dev);
-  gdn_decode_kernel<D, MODE><<<dim3(static_cast<unsigned>(p.B * p.H)), dim3(NT_DECODE), L.total, stream>>>(q);
+  // programmatic stream serialisation: the kernel orders its own reads (griddep_wait)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.B * p.H));
+  cfg.blockDim = dim3(NT_DECODE);
+  cfg.dynamicSmemBytes = L.total;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, gdn_decode_kernel<D, MODE>, q);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 

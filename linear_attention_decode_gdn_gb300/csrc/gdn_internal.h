@@ -19,7 +19,8 @@ enum Mode : int {
 
 struct DecodeParams {
   int32_t B, H, D, num_slots, C, dlam, channels;
-  int32_t prefetch_ahead;  // decode: CTA i prefetches the inputs of work item i + this into L2 (0: off)
+  int32_t prefetch_ahead;  // decode: CTAs resident at once (one wave); CTA i prefetches the inputs
+                           // of item i + this into L2, the first wave its own tile (0: off)
   uint32_t flags;
   float q_scale, l2_eps;
   const void* q;
