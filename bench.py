@@ -86,10 +86,14 @@ def measured_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources' code: line comments and blank space are dropped, so a
+    comment edit keeps a capture's counters valid while any code change drops them."""
+    import re
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "linear_attention_decode_gdn_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "linear_attention_decode_gdn_gb300", "csrc", name)) as f:
+            code = re.sub(r"//[^\n]*", "", f.read())
+        h.update(" ".join(code.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -7,21 +7,23 @@
 // (64 KiB) fits in shared memory three times per SM, so the head is not split
 // and the metadata commit needs no second pass).
 //
-// Per CTA:
-//   prologue  TMA bulk copies of the tile (4 row chunks for dk = 128) start first, then
-//             the copy of the first L log entries as soon as L has been read; meanwhile
-//             the threads load q/k/v (or run the width-4 conv + SiLU) and form the
-//             decays exp(ell').  One barrier, then phase 1 starts.
+// Per CTA (8 compute warps + 1 copy-issuing warp):
+//   launch    programmatic stream serialisation: the CTA lets the next launch schedule at
+//             once and waits for the previous grid before its first read (first-wave
+//             CTAs prefetch their tile into L2 before that wait).
+//   prologue  the copy warp starts the TMA bulk copies of the tile (4 row chunks for
+//             dk = 128) and the log copy (append: the first L entries once L is read;
+//             merge: all C); the compute warps load the gates and q/k/v (or run the
+//             width-4 conv + SiLU) and form the decays exp(ell').  One barrier.
+//   replay    while the tile is in flight, one warp per log entry i < L forms the
+//             projection coefficients  c^k_i = k^T D(ell' - Lambda_i) K_i,
+//             c^q_i = q^T D(...) K_i  (DeltaLog notes Sec. 2.4, warp-shuffle sums), and
+//             the L2 norms of q and k (and q_scale) give two per-head scale factors.
 //   phase 1   one pass over the tile as chunks land, on the raw vectors:
 //             r_k = S^T (e^{ell'} * k),  r_q = S^T (e^{ell'} * q)  (warp-local sums,
-//             then across warps).  Between the last two chunks the warps form, for
-//             every log entry i < L, the projection coefficients
-//             c^k_i = k^T D(ell' - Lambda_i) K_i,  c^q_i = q^T D(...) K_i
-//             (DeltaLog notes Sec. 2.4, one warp-shuffle reduction per entry).
-//   phase 2   the L2 norms of q and k (and q_scale) are scalars of the head and scale
-//             the reduced sums; per value column j:  vhat = r_k + sum_i c^k_i U_i,
-//             b = beta (v - vhat),  o = r_q + sum_i c^q_i U_i + (q.k) b.
-//             Append commits the new entry.
+//             then across warps), scaled by the norm factors afterwards.
+//   phase 2   per value column j:  vhat = r_k + sum_i c^k_i U_i,  b = beta (v - vhat),
+//             o = r_q + sum_i c^q_i U_i + (q.k) b.   Append commits the new entry.
 //   phase 3   dense / merge only: S' = D(ell') S + sum_i D(ell' - Lambda_i) K_i U_i^T + k b^T,
 //             written back with 16-byte coalesced stores.
 #include <atomic>
