@@ -164,7 +164,7 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- traffic model
 
-def head_bytes(mode: str, n: int, w, klb=2, conv=False) -> int:
+def head_bytes(mode: str, n: int, w, klb=2, conv=False, ulb=4) -> int:
     """Algorithmic DRAM bytes one decode launch moves per (request, head), following the
     traffic model of the DeltaLog notes (Sec. 2.5, Eqs. (8)-(11)): common inputs and
     outputs, the state read (and write for dense / merge), the log entries replayed
@@ -172,11 +172,11 @@ def head_bytes(mode: str, n: int, w, klb=2, conv=False) -> int:
     D = w.dk
     e = 2 if w.qkv_bf16 else 4
     dlam = w.dlam
-    common = 3 * D * e + 4 * dlam + 4 + 4 * D          # q,k,v + lambda + beta + o
+    common = 3 * D * e + 4 * dlam + (0 if w.raw_value else 4) + 4 * D  # q,k,v + lambda + beta + o
     if conv:
         common += 3 * D * 3 * e * 2 + 3 * D * 16       # conv cache read + write, weights
     state = 4 * D * D
-    entry = D * klb + 4 * D + 4 * dlam                  # one log position
+    entry = D * klb + ulb * D + 4 * dlam                # one log position
     if mode == "dense":
         return common + 2 * state
     meta = 4 * dlam + 4                                 # ell and L read
@@ -202,6 +202,8 @@ def run_gpu(args, rank, local_rank, world):
     flags = (gdn.QKV_BF16 if w.qkv_bf16 else 0) | (gdn.FUSE_CONV if w.conv else 0)
     if args.klog_prenorm:
         flags |= gdn.KLOG_PRENORM
+    if w.raw_value:  # the RWKV6 instantiation: b = v (beta NULL), raw q/k, bf16 value log
+        flags |= gdn.PLAIN_UPDATE | gdn.NO_QK_L2NORM | gdn.ULOG_BF16
     lib = gdn._abi.load()
     stream = torch.cuda.current_stream(dev)
     sptr = ctypes.c_void_p(stream.cuda_stream)
@@ -219,7 +221,8 @@ def run_gpu(args, rank, local_rank, world):
                 d[n_] = (torch.from_numpy(x[n_ + "_bits"].view(np.int16)).view(torch.bfloat16)
                          if w.qkv_bf16 else torch.from_numpy(x[n_]))
         d["log_decay"] = torch.from_numpy(x["lam"])
-        d["beta"] = torch.from_numpy(x["beta"])
+        if not w.raw_value:
+            d["beta"] = torch.from_numpy(x["beta"])
         host_ring.append({k: v.pin_memory() for k, v in d.items()})
         ring.append({k: v.to(dev) for k, v in d.items()})
     slot = torch.arange(B, dtype=torch.int32, device=dev)
@@ -316,11 +319,12 @@ def run_gpu(args, rank, local_rank, world):
     peak, peak_kind = measured_peaks()
     heads = B * H
     klb = 4 if flags & gdn.KLOG_FP32 else 2
+    ulb = 2 if flags & gdn.ULOG_BF16 else 4
     avg_n = (M - 2) / 2 if M > 1 else 0.0    # appends enter with L = 0 .. M-2
     bytes_per_launch = {
-        "dense": heads * head_bytes("dense", 0, w, klb, w.conv),
-        "append": heads * head_bytes("append", avg_n, w, klb, w.conv),
-        "merge": heads * head_bytes("merge", M - 1, w, klb, w.conv),
+        "dense": heads * head_bytes("dense", 0, w, klb, w.conv, ulb),
+        "append": heads * head_bytes("append", avg_n, w, klb, w.conv, ulb),
+        "merge": heads * head_bytes("merge", M - 1, w, klb, w.conv, ulb),
     }
     kernels = {}
     for mode in ("deltalog", "dense"):
@@ -373,8 +377,10 @@ def run_gpu(args, rank, local_rank, world):
                    "dv": w.dv, "merge_interval": M, "decode_steps_per_step": M,
                    "inputs": ("bf16" if w.qkv_bf16 else "fp32") + " q/k/v"
                    + (" through the fused width-4 conv" if w.conv else "")
-                   + ", fp32 log-decay and beta; fp32 state and log values, "
-                   + ("bf16 pre-normalisation" if args.klog_prenorm else "bf16") + " key log",
+                   + (", fp32 log-decay, raw-value update (beta = 1); fp32 state, bf16 key and value logs"
+                      if w.raw_value else
+                      ", fp32 log-decay and beta; fp32 state and log values, "
+                      + ("bf16 pre-normalisation" if args.klog_prenorm else "bf16") + " key log"),
                    "l2": f"state {w.state_bytes / 2**20:.0f} MiB > L2 (inputs larger than L2, no flush)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "modes": modes,
@@ -542,7 +548,7 @@ def oracle_sample(w, steps_budget_s: float, max_steps: int, batch: int, warm=1):
     from linear_attention_decode_gdn_gb300 import workloads as wl
     lib = oracle.load()
     H, D = w.num_heads, w.dk
-    flags = oracle.L2NORM | (oracle.CONV if w.conv else 0)
+    flags = (oracle.PLAIN if w.raw_value else oracle.L2NORM) | (oracle.CONV if w.conv else 0)
     cfg = dict(batch=batch, num_heads=H, dk=D, dv=w.dv, num_slots=batch, dlam=w.dlam,
                log_capacity=0, flags=flags, q_scale=1.0, l2_eps=1e-6)
     st = oracle.BatchState(batch, H, D, w.dv, w.dlam, 0, nch=w.channels)

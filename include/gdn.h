@@ -23,7 +23,9 @@
  *     layout; Sec. 2.2 Eq. (7) -- invariant; Sec. 2.3 Algorithm 1, Eq. (6) --
  *     append / merge; Sec. 2.4 -- readout from base + log, a_t = k_t,
  *     b_t = beta_t (v_t - vhat_t); Sec. 2.6 Fig. 5 -- one writer per state slice;
- *     Sec. 2.7 -- K log bf16, U log fp32, decay metadata fp32.
+ *     Sec. 2.7 -- the three instantiations: GDN (per-head decay), KDA (per-key
+ *     decay), both with K log bf16 and U log fp32; RWKV6 (per-key decay, raw
+ *     value update, no correction, K and U logs bf16); decay metadata fp32.
  *   "线性注意力与混合架构的推理" (inference handbook): fp32 state, bf16 conv cache,
  *     slot-indexed state pools read by a batched kernel.
  *
@@ -89,6 +91,10 @@ extern "C" {
                                       value factor times the key's inverse norm (same product
                                       k b^T, no rounding of the normalised key); requires L2
                                       normalisation and no fused conv */
+#define GDN_ULOG_BF16 (1u << 7)    /* U_log entries are bf16 instead of fp32 (the RWKV6 instantiation
+                                      of the DeltaLog notes, Sec. 2.7: a raw-value update has no
+                                      correction to protect, so both logs are bf16). Exact when
+                                      b = v of bf16 inputs (GDN_PLAIN_UPDATE, beta == NULL) */
 #define GDN_TEST_STARVE_WAIT (1u << 31) /* test only: the decode kernels expect 16 bytes more than
                                            the first tile copy delivers, so that bounded wait runs
                                            out (about a second) and the call reports
@@ -120,14 +126,16 @@ typedef struct gdn_inputs {
   void *conv_pool;        /* GDN_FUSE_CONV: [num_slots][channels][3] pre-conv inputs, column 0 oldest;
                              same dtype as mixed_qkv; updated in place */
   const float *log_decay; /* lambda: [B][H][dlam] (<= 0), or raw gate logits with GDN_GATE_RAW */
-  const float *beta;      /* [B][H] write strength in [0, 1], or raw logits with GDN_GATE_RAW */
+  const float *beta;      /* [B][H] write strength in [0, 1], or raw logits with GDN_GATE_RAW;
+                             NULL: beta = 1 for every head (the RWKV6 update k v^T with
+                             GDN_PLAIN_UPDATE) */
   const int32_t *slot;    /* [B] pool row of each request; < 0 = padding */
 } gdn_inputs;
 
 /* DeltaLog log pools (all [num_slots][H][...], updated in place). */
 typedef struct gdn_log {
   void *k_log;      /* [num_slots][H][C][dk] bf16 (or fp32 with GDN_KLOG_FP32): key factors a_i */
-  float *u_log;     /* [num_slots][H][C][dv] value factors b_i */
+  void *u_log;      /* [num_slots][H][C][dv] fp32 (or bf16 with GDN_ULOG_BF16): value factors b_i */
   float *lam_log;   /* [num_slots][H][C][dlam] cumulative log-decay at insertion, Lambda_i */
   float *ell;       /* [num_slots][H][dlam] cumulative log-decay since the last merge */
   int32_t *len;     /* [num_slots][H] log length L, 0 <= L <= C */
@@ -204,10 +212,11 @@ int gdn_decode_step(const gdn_dims *dims, const gdn_inputs *in, float *base_pool
 
 /*
  * gdn_log_bytes -- byte sizes of the log pools for dims (num_slots, num_heads,
- * dk, dv, decay_per_key, log_capacity, GDN_KLOG_FP32). Host only; no GPU needed.
- * residency equals (M-1) C_entry + C_decay of the DeltaLog notes' capacity
- * table (Sec. 2.5): 21.125 MiB for GDN at M = 8 and 17 MiB for KDA at M = 4
- * with 128 slots, 32 heads and dk = dv = 128.
+ * dk, dv, decay_per_key, log_capacity, GDN_KLOG_FP32, GDN_ULOG_BF16). Host only;
+ * no GPU needed. residency equals (M-1) C_entry + C_decay of the DeltaLog notes'
+ * capacity table (Sec. 2.5): 21.125 MiB for GDN at M = 8, 17 MiB for KDA at M = 4
+ * and 14 MiB for RWKV6 (bf16 U log) at M = 4, with 128 slots, 32 heads and
+ * dk = dv = 128.
  */
 int gdn_log_bytes(const gdn_dims *dims, gdn_log_sizes *out);
 

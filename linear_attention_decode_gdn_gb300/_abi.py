@@ -34,6 +34,7 @@ GATE_RAW = 1 << 3
 PLAIN_UPDATE = 1 << 4
 KLOG_FP32 = 1 << 5
 KLOG_PRENORM = 1 << 6
+ULOG_BF16 = 1 << 7
 TEST_STARVE_WAIT = 1 << 31
 
 # every symbol include/gdn.h declares

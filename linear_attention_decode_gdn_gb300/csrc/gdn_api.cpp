@@ -14,7 +14,7 @@ namespace {
 thread_local char g_last_error[512] = "";
 
 constexpr uint32_t kKnownFlags = GDN_QKV_BF16 | GDN_FUSE_CONV | GDN_NO_QK_L2NORM | GDN_GATE_RAW |
-                                 GDN_PLAIN_UPDATE | GDN_KLOG_FP32 | GDN_KLOG_PRENORM |
+                                 GDN_PLAIN_UPDATE | GDN_KLOG_FP32 | GDN_KLOG_PRENORM | GDN_ULOG_BF16 |
                                  GDN_TEST_STARVE_WAIT;
 constexpr int kMaxLogCapacity = 63;
 
@@ -53,8 +53,8 @@ int check_dims(const gdn_dims* d, bool log_call) {
 
 int check_inputs(const gdn_dims* d, const gdn_inputs* in) {
   if (in == nullptr) return fail(GDN_ERR_INVALID_ARG, "inputs is NULL");
-  if (in->slot == nullptr || in->log_decay == nullptr || in->beta == nullptr)
-    return fail(GDN_ERR_INVALID_ARG, "slot, log_decay and beta are required");
+  if (in->slot == nullptr || in->log_decay == nullptr)
+    return fail(GDN_ERR_INVALID_ARG, "slot and log_decay are required");
   if (d->flags & GDN_FUSE_CONV) {
     if (in->mixed_qkv == nullptr || in->conv_w == nullptr || in->conv_pool == nullptr)
       return fail(GDN_ERR_INVALID_ARG, "GDN_FUSE_CONV needs mixed_qkv, conv_w and conv_pool");
@@ -130,7 +130,7 @@ int decode_common(int mode, const gdn_dims* dims, const gdn_inputs* in, float* p
   if (gdn::decode_smem_bytes(mode, dims->dk, log_call ? dims->log_capacity : 0,
                              dims->decay_per_key ? dims->dk : 1,
                              (dims->flags & GDN_KLOG_FP32) ? 4 : 2,
-                             (dims->flags & GDN_QKV_BF16) ? 2 : 4) == 0)
+                             (dims->flags & GDN_ULOG_BF16) ? 2 : 4) == 0)
     return fail(GDN_ERR_UNSUPPORTED, "log_capacity %d does not fit in shared memory for this shape",
                 dims->log_capacity);
   gdn::DecodeParams p = make_params(dims, in);
@@ -217,7 +217,7 @@ int gdn_log_bytes(const gdn_dims* dims, gdn_log_sizes* out) {
   const size_t dlam = dims->decay_per_key ? static_cast<size_t>(dims->dk) : 1u;
   const size_t kb = (dims->flags & GDN_KLOG_FP32) ? 4u : 2u;
   out->k_log = sh * C * dims->dk * kb;
-  out->u_log = sh * C * dims->dv * 4u;
+  out->u_log = sh * C * dims->dv * ((dims->flags & GDN_ULOG_BF16) ? 2u : 4u);
   out->lam_log = sh * C * dlam * 4u;
   out->ell = sh * dlam * 4u;
   out->len = sh * 4u;

@@ -40,12 +40,14 @@ struct Layout {
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1u) / a * a; }
 
-__host__ __device__ inline Layout decode_layout(int mode, int D, int C, int klog_bytes) {
+__host__ __device__ inline Layout decode_layout(int mode, int D, int C, int klog_bytes, int ulog_bytes) {
   Layout L{};
   const bool has_log = mode != MODE_DENSE;
   const bool can_merge = mode == MODE_MERGE || mode == MODE_STEP;
   const bool writes_state = mode != MODE_APPEND;
-  L.cp = can_merge ? static_cast<int>(align_up(static_cast<uint32_t>(C + 1), 8u)) : 0;
+  // the merge folds the log in groups of 8 entries (zero-padded); the current token's
+  // term is applied on its own after them
+  L.cp = can_merge ? static_cast<int>(align_up(static_cast<uint32_t>(C > 0 ? C : 1), 8u)) : 0;
   uint32_t off = 0;
   L.tile = off;
   off += static_cast<uint32_t>(D * D * 4);
@@ -61,7 +63,7 @@ __host__ __device__ inline Layout decode_layout(int mode, int D, int C, int klog
   L.uni = off;
   off += align_up(kbytes > redbytes ? kbytes : redbytes, 16u);
   L.us = off;
-  off += has_log ? static_cast<uint32_t>((can_merge ? L.cp : C) * D * 4) : 0u;
+  off += has_log ? align_up(static_cast<uint32_t>((can_merge ? L.cp : C) * D * ulog_bytes), 16u) : 0u;
   L.kd = off;
   off += can_merge ? static_cast<uint32_t>(D * L.cp * 4) : 0u;
   L.coef = off;  // c^k | c^q | per-head decay snapshots Lambda_i
@@ -117,7 +119,8 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
   const int C = p.C, dlam = p.dlam;
   const uint32_t fl = p.flags;
   const int klb = (fl & GDN_KLOG_FP32) ? 4 : 2;
-  const Layout L = decode_layout(MODE, D, C, klb);
+  const int ulb = (fl & GDN_ULOG_BF16) ? 2 : 4;
+  const Layout L = decode_layout(MODE, D, C, klb, ulb);
   float* tile = reinterpret_cast<float*>(smem + L.tile);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   int* scal_i = reinterpret_cast<int*>(smem + L.scal);             // [0] L on entry, [1] status bits
@@ -131,7 +134,8 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
   float* dec_s = q_s + 5 * D;  // only when the state is written
   unsigned char* uni = smem + L.uni;
   float* red = reinterpret_cast<float*>(uni);
-  float* u_s = reinterpret_cast<float*>(smem + L.us);
+  float* u_s = reinterpret_cast<float*>(smem + L.us);  // U entries (fp32, or bf16 bits)
+  uint16_t* u16_s = reinterpret_cast<uint16_t*>(smem + L.us);
   float* kd_s = reinterpret_cast<float*>(smem + L.kd);
   float* ck_s = reinterpret_cast<float*>(smem + L.coef);
   float* cq_s = ck_s + C;
@@ -177,8 +181,9 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
       }
       const uint4* ksrc = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(p.k_log) +
                                                          sh * C * D * klb);
-      const uint4* usrc = reinterpret_cast<const uint4*>(p.u_log + sh * C * D);
-      const int kvec = nc * D * klb / 16, uvec = nc * D * 4 / 16;
+      const uint4* usrc = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(p.u_log) +
+                                                         sh * C * D * ulb);
+      const int kvec = nc * D * klb / 16, uvec = nc * D * ulb / 16;
       for (int i = lane; i < kvec; i += 32) cp_async16(reinterpret_cast<uint4*>(uni) + i, ksrc + i);
       for (int i = lane; i < uvec; i += 32) cp_async16(reinterpret_cast<uint4*>(u_s) + i, usrc + i);
       if (dlam == 1)
@@ -230,7 +235,7 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
     if (MODE != MODE_DENSE) ell_t = p.ell[sh * dlam + di];
   }
   if (!ctrl) {
-    beta = __ldg(p.beta + static_cast<size_t>(b) * p.H + h);
+    beta = p.beta ? __ldg(p.beta + static_cast<size_t>(b) * p.H + h) : 1.0f;
     load_token(p, b, h, slot, tid, &x, &vj);
     if (fl & GDN_GATE_RAW) {
       lam_t = log_sigmoidf_(lam_t);
@@ -295,16 +300,15 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
     // the merge tables only after it
     if (!mbar_wait(&bars[NCHUNK], 0u)) timeout = true;
     if (is_merge) {
-      // the current update enters the merge at weight D(0) = I with the normalised
-      // key; pad the tables with zeros
+      // pad the weight table and the U entries past L with zeros (the group of 8 that
+      // holds entry L-1 reads them; the current token's term is applied on its own)
       for (int idx = tid; idx < D * cp; idx += NT) {
         const int d = idx / cp, e = idx - d * cp;
-        if (e == n)
-          kd_s[idx] = k_s[d] * kinv;
-        else if (e > n)
-          kd_s[idx] = 0.0f;
+        if (e >= n) kd_s[d * cp + e] = 0.0f;
       }
-      for (int idx = tid; idx < (cp - n - 1) * D; idx += NT) u_s[(n + 1) * D + idx] = 0.0f;
+      const int pad_words = (cp - n) * D * ulb / 4;
+      uint32_t* upad = reinterpret_cast<uint32_t*>(smem + L.us + static_cast<size_t>(n) * D * ulb);
+      for (int idx = tid; idx < pad_words; idx += NT) upad[idx] = 0u;
     }
     for (int e = warp; e < n; e += NW) {
       const float* lam_e = p.lam_log + (sh * C + e) * dlam;
@@ -415,7 +419,7 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
     rk = __fmul_rn(rk, kinv);
     rq = __fmul_rn(rq, qsc);
     for (int e = 0; e < n; ++e) {
-      const float u = u_s[e * D + j];
+      const float u = (ulb == 2) ? bf16_bits_to_float(u16_s[e * D + j]) : u_s[e * D + j];
       rk = fmaf(ck_s[e], u, rk);
       rq = fmaf(cq_s[e], u, rq);
     }
@@ -423,9 +427,14 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
     const float oj = fmaf(scal_f[8] * qsc * kinv, bj, rq);
     p.o[(static_cast<size_t>(b) * p.H + h) * D + j] = oj;
     b_s[j] = bj;
-    if (is_append)
-      p.u_log[(sh * C + n) * D + j] = (fl & GDN_KLOG_PRENORM) ? bj * kinv : bj;
-    if (is_merge) u_s[n * D + j] = bj;
+    if (is_append) {
+      const float uval = (fl & GDN_KLOG_PRENORM) ? bj * kinv : bj;
+      const size_t at = (sh * C + n) * D + j;
+      if (ulb == 2)
+        reinterpret_cast<__nv_bfloat16*>(p.u_log)[at] = __float2bfloat16_rn(uval);
+      else
+        static_cast<float*>(p.u_log)[at] = uval;
+    }
   }
   if (is_append) {
     if (is_k) {
@@ -447,12 +456,63 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
   }
 
   // ---- phase 3: write the state (dense) or fold the log into the base (merge) ------
+  // S' = D(ell') S + sum_{i<L} (e^{ell' - Lambda_i} K_i) U_i^T + k b^T: the log terms in
+  // groups of 8 (zero-padded), then the current token's term, in that order; with L = 0
+  // this is the dense arithmetic exactly.
   if (MODE == MODE_DENSE || is_merge) {
-    consumer_sync();  // (F) b and the current entry are in shared memory
+    consumer_sync();  // (F) b and the padded tables are in shared memory
     float* out = p.state + sh * static_cast<size_t>(D * D);
     float4* tilew = reinterpret_cast<float4*>(tile);
-    if (MODE == MODE_DENSE) {
-      const float4 bb = reinterpret_cast<const float4*>(b_s)[c4];
+    const float4 bb = reinterpret_cast<const float4*>(b_s)[c4];
+    const int ng = (MODE == MODE_DENSE) ? 0 : (n + 7) / 8;
+    for (int g = 0; g < ng; ++g) {
+      float4 u[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (ulb == 2) {
+          const uint2 raw = reinterpret_cast<const uint2*>(u16_s + (g * 8 + e) * D)[c4];
+          u[e] = make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u),
+                             __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u));
+        } else {
+          u[e] = reinterpret_cast<const float4*>(u_s + (g * 8 + e) * D)[c4];
+        }
+      }
+#pragma unroll
+      for (int it = 0; it < NIT; ++it) {
+        const int r = it * RPI + warp * RPW + rsub;
+        if (r < D) {
+          float4 acc = tile4[r * VPR + c4];
+          if (g == 0) {
+            const float dc = dec_s[r];
+            acc.x *= dc;
+            acc.y *= dc;
+            acc.z *= dc;
+            acc.w *= dc;
+          }
+          const float4 w0 = *reinterpret_cast<const float4*>(kd_s + r * cp + g * 8);
+          const float4 w1 = *reinterpret_cast<const float4*>(kd_s + r * cp + g * 8 + 4);
+          const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            acc.x = fmaf(wv[e], u[e].x, acc.x);
+            acc.y = fmaf(wv[e], u[e].y, acc.y);
+            acc.z = fmaf(wv[e], u[e].z, acc.z);
+            acc.w = fmaf(wv[e], u[e].w, acc.w);
+          }
+          if (g == ng - 1) {  // the current token's term, then the write-back
+            const float kk = k_s[r] * kinv;
+            acc.x = fmaf(kk, bb.x, acc.x);
+            acc.y = fmaf(kk, bb.y, acc.y);
+            acc.z = fmaf(kk, bb.z, acc.z);
+            acc.w = fmaf(kk, bb.w, acc.w);
+            *reinterpret_cast<float4*>(out + r * D + c4 * 4) = acc;
+          } else {
+            tilew[r * VPR + c4] = acc;
+          }
+        }
+      }
+    }
+    if (ng == 0) {  // dense, or a merge of an empty log
 #pragma unroll
       for (int it = 0; it < NIT; ++it) {
         const int r = it * RPI + warp * RPW + rsub;
@@ -465,41 +525,6 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
           o4.z = fmaf(kk, bb.z, dc * s.z);
           o4.w = fmaf(kk, bb.w, dc * s.w);
           *reinterpret_cast<float4*>(out + r * D + c4 * 4) = o4;
-        }
-      }
-    } else {
-      const int ng = (n + 1 + 7) / 8;  // groups of 8 rank-1 terms (log entries + current)
-      for (int g = 0; g < ng; ++g) {
-        float4 u[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) u[e] = reinterpret_cast<const float4*>(u_s + (g * 8 + e) * D)[c4];
-#pragma unroll
-        for (int it = 0; it < NIT; ++it) {
-          const int r = it * RPI + warp * RPW + rsub;
-          if (r < D) {
-            float4 acc = tile4[r * VPR + c4];
-            if (g == 0) {
-              const float dc = dec_s[r];
-              acc.x *= dc;
-              acc.y *= dc;
-              acc.z *= dc;
-              acc.w *= dc;
-            }
-            const float4 w0 = *reinterpret_cast<const float4*>(kd_s + r * cp + g * 8);
-            const float4 w1 = *reinterpret_cast<const float4*>(kd_s + r * cp + g * 8 + 4);
-            const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              acc.x = fmaf(wv[e], u[e].x, acc.x);
-              acc.y = fmaf(wv[e], u[e].y, acc.y);
-              acc.z = fmaf(wv[e], u[e].z, acc.z);
-              acc.w = fmaf(wv[e], u[e].w, acc.w);
-            }
-            if (g == ng - 1)
-              *reinterpret_cast<float4*>(out + r * D + c4 * 4) = acc;
-            else
-              tilew[r * VPR + c4] = acc;
-          }
         }
       }
     }
@@ -528,7 +553,8 @@ template <int D, int MODE>
 cudaError_t launch_one(const DecodeParams& p, cudaStream_t stream) {
   static std::atomic<uint32_t> configured[kMaxDevices];
   const int klb = (p.flags & GDN_KLOG_FP32) ? 4 : 2;
-  const Layout L = decode_layout(MODE, D, p.C, klb);
+  const int ulb = (p.flags & GDN_ULOG_BF16) ? 2 : 4;
+  const Layout L = decode_layout(MODE, D, p.C, klb, ulb);
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
@@ -587,11 +613,10 @@ cudaError_t launch_d(int mode, const DecodeParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-size_t decode_smem_bytes(int mode, int D, int C, int dlam, int klog_bytes, int in_elem) {
+size_t decode_smem_bytes(int mode, int D, int C, int dlam, int klog_bytes, int ulog_bytes) {
   (void)dlam;
-  (void)in_elem;
   if (D != 16 && D != 32 && D != 64 && D != 128) return 0;
-  return decode_layout(mode, D, C, klog_bytes).total;
+  return decode_layout(mode, D, C, klog_bytes, ulog_bytes).total;
 }
 
 cudaError_t launch_decode(int mode, const DecodeParams& p, cudaStream_t stream) {

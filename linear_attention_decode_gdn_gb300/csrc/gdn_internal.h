@@ -35,7 +35,7 @@ struct DecodeParams {
   const int32_t* slot;
   float* state;  // dense: state pool; DeltaLog: base pool
   void* k_log;
-  float* u_log;
+  void* u_log;
   float* lam_log;
   float* ell;
   int32_t* len;
@@ -64,6 +64,6 @@ cudaError_t launch_conv_l2norm(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_slot_reset(const ResetParams& p, cudaStream_t stream);
 
 // Dynamic shared memory a decode launch needs (bytes); 0 if the shape is not built.
-size_t decode_smem_bytes(int mode, int D, int C, int dlam, int klog_bytes, int in_elem);
+size_t decode_smem_bytes(int mode, int D, int C, int dlam, int klog_bytes, int ulog_bytes);
 
 }  // namespace gdn

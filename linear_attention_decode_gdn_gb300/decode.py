@@ -129,7 +129,8 @@ class Pools:
             kdt = torch.float32 if dims.flags & _abi.KLOG_FP32 else torch.bfloat16
             c = max(C, 1)
             k_log = torch.zeros((S, H, c, dk), dtype=kdt, device=device)
-            u_log = torch.zeros((S, H, c, dv), dtype=torch.float32, device=device)
+            udt = torch.bfloat16 if dims.flags & _abi.ULOG_BF16 else torch.float32
+            u_log = torch.zeros((S, H, c, dv), dtype=udt, device=device)
             lam_log = torch.zeros((S, H, c, dlam), dtype=torch.float32, device=device)
             ell = torch.zeros((S, H, dlam), dtype=torch.float32, device=device)
             length = torch.zeros((S, H), dtype=torch.int32, device=device)

@@ -15,6 +15,9 @@ Draw recipe (per workload, per decode step t):
   * alpha = sigmoid(N(0,1) + 3), lambda = log(alpha) (per head, or per key
     channel for the per-key-decay workload); beta = sigmoid(N(0,1)); both fp32.
   * conv weights N(0,1) * 0.5 (standard deviation 0.5), fp32, no bias.
+  * raw-value workloads (the RWKV6 instantiation): the write-gate draw is made and
+    discarded, beta = 1; q and k are not L2-normalised, so they are drawn with
+    qk_mult = 1/sqrt(dk) (unit expected norm).
 """
 from __future__ import annotations
 
@@ -38,6 +41,8 @@ class Workload:
     seed: int
     qk_mult: float = 1.0
     conv_w_std: float = 0.5
+    raw_value: bool = False  # RWKV6 update S <- D(lambda) S + k v^T: beta = 1, no correction
+                             # and no L2 norm; K and U logs bf16
     description: str = field(default="", compare=False)
 
     @property
@@ -66,6 +71,10 @@ WORKLOADS = {
                  1004, description="B=512, H=32, dk=dv=128, fp32 state 1 GiB, 128 steps, M in {1,2,4,8,16}"),
         Workload("kda", 256, 32, 128, 128, 128, (8,), True, False, True, 1005,
                  description="B=256, H=32, dk=dv=128, per-key-channel log decay (width 128), 128 steps, M=8"),
+        Workload("rwkv6", 128, 32, 128, 128, 128, (1, 4), True, False, True, 1006, qk_mult=128 ** -0.5,
+                 raw_value=True,
+                 description="B=128, H=32, dk=dv=128, per-key-channel log decay, raw-value update "
+                             "(beta = 1, no correction, no L2 norm), bf16 K and U logs, 128 steps, M in {1, 4}"),
     )
 }
 
@@ -124,6 +133,8 @@ def step_inputs(w: Workload, t: int, batch: int | None = None) -> dict:
             else:
                 out[name] = arr
     lam, beta, a_raw, b_raw = _gates(rng, w, B)
+    if w.raw_value:
+        beta = np.ones_like(beta)
     out.update(lam=lam, beta=beta, a_raw=a_raw, b_raw=b_raw)
     return out
 

@@ -40,6 +40,8 @@ def base_flags(w: wl.Workload, gate_raw=False) -> int:
         f |= gdn.FUSE_CONV
     if gate_raw:
         f |= gdn.GATE_RAW
+    if w.raw_value:  # the RWKV6 instantiation: b = v, raw q/k, bf16 value log
+        f |= gdn.PLAIN_UPDATE | gdn.NO_QK_L2NORM | gdn.ULOG_BF16
     return f
 
 
@@ -134,7 +136,8 @@ class Lockstep:
         w = self.w
         lam = x["a_raw"] if self.gate_raw else x["lam"]
         beta = x["b_raw"] if self.gate_raw else x["beta"]
-        d = dict(log_decay=dev_f32(lam), beta=dev_f32(beta), slot=self.slot_dev)
+        # raw-value workloads pass no beta (NULL: beta = 1); the oracle gets ones
+        d = dict(log_decay=dev_f32(lam), beta=None if w.raw_value else dev_f32(beta), slot=self.slot_dev)
         if w.conv:
             d["mixed_qkv"] = dev_bf16(x["mixed_bits"]) if w.qkv_bf16 else dev_f32(x["mixed"])
             d["conv_w"] = self.conv_w_dev

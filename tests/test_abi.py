@@ -58,20 +58,21 @@ def test_strerror(gdn):
     assert lib.gdn_strerror(99) == b"unknown error code"
 
 
-@pytest.mark.parametrize("per_key,M,C_entry_bytes,expected_mib", [
-    (False, 8, 2 * 128 + 4 * 128 + 4, 21.125),   # GDN row of the capacity table
-    (True, 4, 2 * 128 + 4 * 128 + 4 * 128, 17.0),  # KDA row
+@pytest.mark.parametrize("per_key,M,bf16_u,C_entry_bytes,expected_mib,frac", [
+    (False, 8, False, 2 * 128 + 4 * 128 + 4, 21.125, 0.0825),      # GDN row of the capacity table
+    (True, 4, False, 2 * 128 + 4 * 128 + 4 * 128, 17.0, 0.0664),   # KDA row
+    (True, 4, True, 2 * 128 + 2 * 128 + 4 * 128, 14.0, 0.0547),    # RWKV6 row (bf16 U log)
 ])
-def test_log_bytes_matches_capacity_table(gdn, per_key, M, C_entry_bytes, expected_mib):
-    d = gdn.make_dims(128, 32, 128, num_slots=128, decay_per_key=per_key, log_capacity=M - 1)
+def test_log_bytes_matches_capacity_table(gdn, per_key, M, bf16_u, C_entry_bytes, expected_mib, frac):
+    d = gdn.make_dims(128, 32, 128, num_slots=128, decay_per_key=per_key, log_capacity=M - 1,
+                      flags=gdn.ULOG_BF16 if bf16_u else 0)
     s = gdn.log_bytes(d)
     assert s["residency"] == expected_mib * MiB
     B, H = 128, 32
     dlam = 128 if per_key else 1
     assert s["residency"] == (M - 1) * B * H * C_entry_bytes + 4 * B * H * dlam
     assert s["total"] == s["residency"] + 4 * B * H
-    assert s["residency"] / (4 * B * H * 128 * 128) == pytest.approx(
-        0.0825 if not per_key else 0.0664, abs=5e-4)
+    assert s["residency"] / (4 * B * H * 128 * 128) == pytest.approx(frac, abs=5e-4)
 
 
 def test_log_bytes_fp32_keys(gdn):

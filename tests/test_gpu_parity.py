@@ -2,7 +2,7 @@
 
 Bars (from the problem statement): max|err|/max|ref| <= 1e-4 for the dense
 path and <= 5e-3 for the DeltaLog append-merge path, over the whole output
-tensor of a rollout, on the five workloads of the benchmark suite, plus edge
+tensor of a rollout, on the workloads of the benchmark suite, plus edge
 cases: every head size, ragged batches, padding and permuted slots, M = 1,
 log contents, status bits, the timeout path, the standalone input stage.
 """
@@ -83,6 +83,19 @@ def test_kda():
     w = wl.WORKLOADS["kda"]
     _check(Lockstep(w, [Variant("dense"), Variant("deltalog", 8),
                         Variant("deltalog", 8, extra_flags=gdn.KLOG_PRENORM, name="M=8/prenorm")]).run())
+
+
+def test_rwkv6():
+    """The RWKV6 instantiation (DeltaLog notes Sec. 2.7): per-key decay, raw-value update
+    b = v (beta = 1 through a NULL pointer), raw q and k, bf16 K and U logs. With bf16
+    inputs the logged factors are the inputs themselves, so the append-merge path is
+    exact up to fp32 rounding and is held to the dense bar."""
+    w = wl.WORKLOADS["rwkv6"]
+    ls = Lockstep(w, [Variant("dense"), Variant("deltalog", 4), Variant("deltalog", 4, "step"),
+                      Variant("deltalog", 1, name="M=1/merge")]).run()
+    rep = _check(ls)
+    for v in ls.variants[1:]:
+        assert v.rel_err <= DENSE_TOL and v.state_rel_err <= DENSE_TOL, rep
 
 
 # ---------------------------------------------------------------- shapes and slots
