@@ -368,7 +368,9 @@ def run_gpu(args, rank, local_rank, world):
     if not args.no_e2e:
         e2e = run_e2e(args, w, M, dims_log, pools_l, host_ring, slot, conv_w, dev, stream, gdn)
 
-    launches = args.steps * M * 4 + (e2e["launches"] if e2e else 0)
+    verify = run_verify(args, w, flags, dev, stream, gdn, peak) if args.verify else None
+
+    launches = args.steps * M * 4 + (e2e["launches"] if e2e else 0) + (verify["launches"] if verify else 0)
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": lt / args.steps * 1e3, "higher_is_better": True,
@@ -387,6 +389,7 @@ def run_gpu(args, rank, local_rank, world):
         "kernels": kernels,
         "roofline": roofline,
         "e2e": e2e,
+        **({"verify": verify} if verify else {}),
         "gpu_launches": launches,
         "clocks": {k: v for k, v in clocks.summary().items()},
     }
@@ -405,6 +408,71 @@ def _packed(arrays: dict, align: int = 256):
 def _views(buf, offs, like: dict):
     return {k: buf[offs[k]:offs[k] + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
             for k, t in like.items()}
+
+
+def run_verify(args, w, flags, dev, stream, gdn, peak):
+    """Speculative-decoding verify on the same workload: T = args.verify positions per
+    request (the last token and T-1 drafts) through gdn_decode_verify, the state after
+    every position written to its own pool row, the initial row chosen by a seeded
+    acceptance count. Unit: positions x heads per second."""
+    import torch
+    B, H, D, T = w.batch, w.num_heads, w.dk, args.verify
+    if w.conv:
+        return {"unavailable": "the verify path runs the dense recurrence without the fused conv"}
+    vflags = flags & ~(gdn.KLOG_PRENORM | gdn.ULOG_BF16)
+    rng = np.random.default_rng(w.seed + 77)
+    ring = []
+    for t in range(RING):
+        x = {}
+        for n in ("q", "k", "v"):
+            a = rng.standard_normal((B, T, H, D), dtype=np.float32) * np.float32(1.0 if n == "v" else w.qk_mult)
+            bits, _ = wl_bf16(a)
+            x[n] = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16) if w.qkv_bf16 \
+                else torch.from_numpy(a).to(dev)
+        a_raw = rng.standard_normal((B, T, H, w.dlam), dtype=np.float32) + np.float32(3)
+        x["log_decay"] = torch.from_numpy((-np.log1p(np.exp(-a_raw))).astype(np.float32)).to(dev)
+        if not w.raw_value:
+            b_raw = rng.standard_normal((B, T, H), dtype=np.float32)
+            x["beta"] = torch.from_numpy((1 / (1 + np.exp(-b_raw))).astype(np.float32)).to(dev)
+        acc = torch.from_numpy(rng.integers(1, T + 1, size=B).astype(np.int32)).to(dev)
+        ring.append((gdn.make_inputs(**x), acc, x))
+    S = B * T
+    dims = gdn.make_dims(B, H, D, num_slots=S, decay_per_key=w.decay_per_key, flags=vflags)
+    pool = torch.zeros((S, H, D, D), dtype=torch.float32, device=dev)
+    idx = torch.arange(S, dtype=torch.int32, device=dev).view(B, T)
+    o = torch.zeros((B, T, H, D), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    calls = max(50, args.steps // 4)
+
+    def go(n, r0=0):
+        for i in range(n):
+            inp, acc, _ = ring[(r0 + i) % RING]
+            gdn.decode_verify(dims, T, inp, idx, acc, pool, o, status, stream=stream)
+
+    go(max(3, args.warmup))
+    torch.cuda.synchronize(dev)
+    barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    go(calls)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the verify run")
+    el, units = reduce_timing(t0.elapsed_time(t1) / 1e3, B * H * T * calls, device=dev)
+    e = 2 if w.qkv_bf16 else 4
+    per_head = 4 * D * D * (1 + T) + T * (3 * D * e + 4 * w.dlam + (0 if w.raw_value else 4) + 4 * D) + 8
+    gbs = B * H * per_head * calls / el / 1e9
+    return {"value": units / el, "unit": "positions x heads / s", "positions_per_request": T,
+            "us_per_call": el / calls * 1e6, "calls": calls, "launches": calls + max(3, args.warmup),
+            "algorithmic_bytes_per_call": B * H * per_head, "algorithmic_gbs": gbs, "frac_of_peak": gbs / peak,
+            "state_rows": "one read + T writes of the 64 KiB state per (request, head)"}
+
+
+def wl_bf16(a):
+    from linear_attention_decode_gdn_gb300 import workloads as wl
+    return wl.bf16_round(a)
 
 
 class _Cudart:
@@ -625,6 +693,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--verify", type=int, default=0,
+                    help="also time the speculative-decoding verify path with this many positions")
     args = ap.parse_args(argv)
 
     world, rank, local = dist_info()

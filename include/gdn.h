@@ -211,6 +211,34 @@ int gdn_decode_step(const gdn_dims *dims, const gdn_inputs *in, float *base_pool
                     const gdn_log *log, float *o, int32_t *status, void *stream);
 
 /*
+ * gdn_decode_verify -- speculative-decoding verification on the dense state
+ * (inference handbook, "推测解码：验证后如何恢复状态"). T = num_tokens input
+ * positions per request ([x0, d1, ..., d_{T-1}]: the last sampled token and the
+ * drafts) run through the dense step one after another. The state after every
+ * position is kept in its own pool row, so a rejected draft is rolled back by
+ * choosing a row, not by copying a state:
+ *   state_indices [B][T] int32: pool rows of request b; the state after position
+ *       t is written to row state_indices[b][t]. The rows of one request must be
+ *       distinct, and no two requests may share a row.
+ *   num_accepted [B] int32 in [1, T]: the initial state is read from row
+ *       state_indices[b][num_accepted[b] - 1], the column the previous round's
+ *       acceptance selects (1 for a request whose state sits in column 0). It is
+ *       read in full before any row is written, so it may be one of the rows this
+ *       call overwrites.
+ *   in->q, in->k, in->v [B][T][H][d] (bf16 or fp32), in->log_decay [B][T][H][dlam],
+ *   in->beta [B][T][H] (or NULL: beta = 1); in->slot is not used.
+ *   o [B][T][H][dv] fp32: the readout of every position.
+ * A request with state_indices[b][0] < 0 is padding and is skipped. A row outside
+ * [0, num_slots) skips the request with GDN_STATUS_BAD_SLOT; num_accepted outside
+ * [1, T] skips it with GDN_STATUS_BAD_LEN. Requires 1 <= num_tokens <= 16; the
+ * verify path is the dense recurrence, so GDN_FUSE_CONV and the DeltaLog flags are
+ * rejected with GDN_ERR_UNSUPPORTED.
+ */
+int gdn_decode_verify(const gdn_dims *dims, int32_t num_tokens, const gdn_inputs *in,
+                      const int32_t *state_indices, const int32_t *num_accepted,
+                      float *state_pool, float *o, int32_t *status, void *stream);
+
+/*
  * gdn_log_bytes -- byte sizes of the log pools for dims (num_slots, num_heads,
  * dk, dv, decay_per_key, log_capacity, GDN_KLOG_FP32, GDN_ULOG_BF16). Host only;
  * no GPU needed. residency equals (M-1) C_entry + C_decay of the DeltaLog notes'

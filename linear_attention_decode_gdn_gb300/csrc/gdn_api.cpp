@@ -26,6 +26,8 @@ int fail(int code, const char* fmt, ...) {
   return code;
 }
 
+constexpr int kMaxVerifyTokens = 16;  // positions per request in one verify call
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0u; }
 
 int check_dims(const gdn_dims* d, bool log_call) {
@@ -206,6 +208,36 @@ int gdn_decode_step(const gdn_dims* dims, const gdn_inputs* in, float* base_pool
                     const gdn_log* log, float* o, int32_t* status, void* stream) {
   return decode_common(gdn::MODE_STEP, dims, in, base_pool, log, o, status, stream,
                        "gdn_decode_step");
+}
+
+int gdn_decode_verify(const gdn_dims* dims, int32_t num_tokens, const gdn_inputs* in,
+                      const int32_t* state_indices, const int32_t* num_accepted, float* state_pool,
+                      float* o, int32_t* status, void* stream) {
+  int rc = check_dims(dims, false);
+  if (rc != GDN_OK) return rc;
+  if (num_tokens < 1 || num_tokens > kMaxVerifyTokens)
+    return fail(GDN_ERR_UNSUPPORTED, "num_tokens %d outside [1, %d]", num_tokens, kMaxVerifyTokens);
+  if (dims->flags & (GDN_FUSE_CONV | GDN_KLOG_FP32 | GDN_KLOG_PRENORM | GDN_ULOG_BF16 | GDN_TEST_STARVE_WAIT))
+    return fail(GDN_ERR_UNSUPPORTED, "verify runs the dense recurrence: no fused conv, no log flags");
+  if (static_cast<long long>(dims->batch) * num_tokens * dims->num_heads > 0x7fffffffLL)
+    return fail(GDN_ERR_INVALID_ARG, "batch * num_tokens * num_heads too large");
+  if (dims->batch == 0) return GDN_OK;
+  if (in == nullptr || in->log_decay == nullptr || in->q == nullptr || in->k == nullptr || in->v == nullptr)
+    return fail(GDN_ERR_INVALID_ARG, "q, k, v and log_decay are required");
+  if (!aligned16(in->q) || !aligned16(in->k) || !aligned16(in->v))
+    return fail(GDN_ERR_UNSUPPORTED, "q, k and v must be 16-byte aligned");
+  if (state_indices == nullptr || num_accepted == nullptr || state_pool == nullptr || o == nullptr)
+    return fail(GDN_ERR_INVALID_ARG, "state_indices, num_accepted, state_pool and o are required");
+  if (!aligned16(state_pool) || !aligned16(o))
+    return fail(GDN_ERR_UNSUPPORTED, "state_pool and o must be 16-byte aligned");
+  gdn::DecodeParams p = make_params(dims, in);
+  p.T = num_tokens;
+  p.state_indices = state_indices;
+  p.num_accepted = num_accepted;
+  p.state = state_pool;
+  p.o = o;
+  p.status = status;
+  return launched(gdn::launch_verify(p, static_cast<cudaStream_t>(stream)), "gdn_decode_verify");
 }
 
 int gdn_log_bytes(const gdn_dims* dims, gdn_log_sizes* out) {

@@ -41,6 +41,10 @@ struct DecodeParams {
   int32_t* len;
   float* o;
   int32_t* status;
+  // verify: positions per request, [B][T] pool rows, [B] accepted counts
+  int32_t T;
+  const int32_t* state_indices;
+  const int32_t* num_accepted;
   // conv_l2norm outputs
   float* q_out;
   float* k_out;
@@ -62,6 +66,7 @@ struct ResetParams {
 cudaError_t launch_decode(int mode, const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_conv_l2norm(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_slot_reset(const ResetParams& p, cudaStream_t stream);
+cudaError_t launch_verify(const DecodeParams& p, cudaStream_t stream);
 
 // Dynamic shared memory a decode launch needs (bytes); 0 if the shape is not built.
 size_t decode_smem_bytes(int mode, int D, int C, int dlam, int klog_bytes, int ulog_bytes);

@@ -86,6 +86,17 @@ def decode_step(dims, inputs, base_pool, log, o, status=None, stream=None):
     _log_call("gdn_decode_step", dims, inputs, base_pool, log, o, status, stream)
 
 
+def decode_verify(dims: Dims, num_tokens: int, inputs: Inputs, state_indices, num_accepted, state_pool, o,
+                  status=None, stream=None):
+    """Speculative-decoding verify: num_tokens positions per request through the dense
+    step; the state after position t goes to pool row state_indices[b, t]; the initial
+    state is row state_indices[b, num_accepted[b] - 1]. Inputs [B, T, H, d], o [B, T, H, dv]."""
+    lib = _abi.load()
+    check(lib.gdn_decode_verify(ctypes.byref(dims), int(num_tokens), ctypes.byref(inputs), _ptr(state_indices),
+                                _ptr(num_accepted), _ptr(state_pool), _ptr(o), _ptr(status), _stream(stream)),
+          "gdn_decode_verify")
+
+
 def log_bytes(dims: Dims) -> dict:
     lib = _abi.load()
     out = LogSizes()

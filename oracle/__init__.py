@@ -10,6 +10,9 @@ Contents:
     (request, head): short conv + SiLU, L2 normalisation, the dense gated
     delta-rule step and the DeltaLog base+log emulation. Built with gcc by
     :func:`build`, loaded with ctypes.
+  * ``verify_batch`` -- speculative-decoding verify: T positions per request
+    through the dense step, one pool row per position (composition of the
+    pinned dense step with the row routing of the inference handbook).
   * ``chunked.py``   -- numpy fp64 chunkwise forms (gated linear attention
     with a decay mask; the WY/UT form of the gated delta rule) used only to
     pin the recurrence against an independent algorithm.
@@ -237,4 +240,35 @@ def step_batch(cfg: dict, mode: str, st: BatchState, slot, *, q=None, k=None, v=
                             _ptr(st.lamlog), _ptr(st.len, ctypes.c_int32), _ptr(o))
     if rc != 0:
         raise ValueError(f"oracle step_batch: {ERRORS.get(rc, rc)}")
+    return o
+
+
+def verify_batch(cfg: dict, pool, state_indices, num_accepted, *, q, k, v, lam, beta, lib=None):
+    """Speculative-decoding verify, written from the inference handbook's passage
+    "推测解码：验证后如何恢复状态": a request feeds T positions (the last sampled token,
+    then the drafts) through the recurrence; the initial state is the pool row of column
+    num_accepted - 1 of its index row, and the state after position t is kept in the row
+    of column t. Every initial state is read before any row is written.
+
+    ``pool`` [num_slots, H, dk, dv] float64 is updated in place; ``state_indices`` [B, T]
+    (row 0 < 0: padding request, skipped), ``num_accepted`` [B] in [1, T]; q, k [B,T,H,dk],
+    v [B,T,H,dv], lam [B,T,H,dlam], beta [B,T,H]. ``cfg`` as for :func:`step_batch`
+    (flags L2NORM / PLAIN / GATE_RAW, q_scale, l2_eps). Each position is one dense step of
+    :func:`step_batch`. Returns o [B, T, H, dv]."""
+    idx = np.asarray(state_indices, dtype=np.int64)
+    na = np.asarray(num_accepted, dtype=np.int64)
+    B, T = idx.shape
+    H, dk, dv, dlam = cfg["num_heads"], cfg["dk"], cfg["dv"], cfg.get("dlam", 1)
+    live = [b for b in range(B) if idx[b, 0] >= 0]
+    run = BatchState(B, H, dk, dv, dlam)
+    for b in live:
+        run.S[b] = pool[idx[b, na[b] - 1]]
+    slot = np.array([b if idx[b, 0] >= 0 else -1 for b in range(B)], dtype=np.int32)
+    c = dict(cfg, batch=B, num_slots=B, log_capacity=0)
+    o = np.zeros((B, T, H, dv))
+    for t in range(T):
+        o[:, t] = step_batch(c, "dense", run, slot, q=q[:, t], k=k[:, t], v=v[:, t],
+                             lam=lam[:, t], beta=beta[:, t], lib=lib)
+        for b in live:
+            pool[idx[b, t]] = run.S[b]
     return o

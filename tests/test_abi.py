@@ -144,3 +144,24 @@ def lib_call(lib, name, dims, inputs, pool, log, o):
     rc = getattr(lib, name)(ctypes.byref(dims), ctypes.byref(inputs), pool,
                             None if log is None else ctypes.byref(log), o, None, None)
     _abi.check(rc, name)
+
+
+def test_verify_validation_rejects_before_launch(gdn):
+    from linear_attention_decode_gdn_gb300 import _abi
+    fake = 1 << 20  # never dereferenced: every call below fails validation first
+    ins = gdn.make_inputs(q=fake, k=fake, v=fake, log_decay=fake)
+    d = gdn.make_dims(2, 2, 64, num_slots=8)
+    for T in (0, 17):
+        _expect(gdn, lambda: gdn.decode_verify(d, T, ins, fake, fake, fake, fake, stream=0),
+                _abi.GDN_ERR_UNSUPPORTED)
+    for flag in (gdn.FUSE_CONV, gdn.KLOG_FP32, gdn.ULOG_BF16):
+        dd = gdn.make_dims(2, 2, 64, num_slots=8, flags=flag)
+        _expect(gdn, lambda: gdn.decode_verify(dd, 4, ins, fake, fake, fake, fake, stream=0),
+                _abi.GDN_ERR_UNSUPPORTED)
+    _expect(gdn, lambda: gdn.decode_verify(d, 4, ins, None, fake, fake, fake, stream=0), _abi.GDN_ERR_INVALID_ARG)
+    _expect(gdn, lambda: gdn.decode_verify(d, 4, gdn.make_inputs(q=fake, k=fake, v=fake), fake, fake, fake,
+                                           fake, stream=0), _abi.GDN_ERR_INVALID_ARG)
+    _expect(gdn, lambda: gdn.decode_verify(d, 4, ins, fake, fake, fake + 4, fake, stream=0),
+            _abi.GDN_ERR_UNSUPPORTED)
+    # an empty batch is a no-op
+    gdn.decode_verify(gdn.make_dims(0, 2, 64, num_slots=8), 4, ins, fake, fake, fake, fake, stream=0)

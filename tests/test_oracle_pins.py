@@ -323,10 +323,44 @@ def pin_prenorm_log(lib, seed=7):
                     assert np.array_equal(sl.klog[b, h, n], k[b, h])
 
 
+def pin_verify_routing(lib, seed=11):
+    """Speculative-decoding verify (inference handbook, "推测解码：验证后如何恢复状态") on a
+    closed form: with lambda = 0, beta = 1 and the plain update, S_t = S_{t-1} + k_t v_t^T, and
+    with orthonormal keys every row is a hand-summed matrix. Checks the row routing: the
+    initial state is column num_accepted - 1 (read before that row is overwritten), the
+    state after position t lands in column t, padding requests and other rows are untouched,
+    o_t = S_t^T q_t."""
+    r = _rng(seed)
+    S, H, d, T = 10, 1, 8, 3
+    pool = r.standard_normal((S, H, d, d))
+    init = pool.copy()
+    idx = np.array([[5, 2, 7], [-1, -1, -1], [0, 9, 3]], dtype=np.int32)
+    na = np.array([2, 1, 3], dtype=np.int32)
+    B = idx.shape[0]
+    eye = np.eye(d)
+    k = np.zeros((B, T, H, d))
+    for b in range(B):
+        for t in range(T):
+            k[b, t, 0] = eye[(t + 2 * b) % d]
+    q, v = r.standard_normal((B, T, H, d)), r.standard_normal((B, T, H, d))
+    lam, beta = np.zeros((B, T, H, 1)), np.ones((B, T, H))
+    cfg = _batch_cfg(B, H, d, d, S, 1, 0, oracle.PLAIN)
+    o = oracle.verify_batch(cfg, pool, idx, na, q=q, k=k, v=v, lam=lam, beta=beta, lib=lib)
+    for b in (0, 2):
+        state = init[idx[b, na[b] - 1], 0].copy()
+        for t in range(T):
+            state = state + np.outer(k[b, t, 0], v[b, t, 0])
+            assert np.max(np.abs(pool[idx[b, t], 0] - state)) <= 1e-12
+            assert np.max(np.abs(o[b, t, 0] - state.T @ q[b, t, 0])) <= 1e-12
+    assert np.all(o[1] == 0)
+    for row in (1, 4, 6, 8):
+        assert np.array_equal(pool[row], init[row])
+
+
 PINS = [pin_teaching_dense, pin_teaching_deltalog, pin_gla_chunked, pin_delta_wy,
         lambda lib: pin_delta_wy(lib, per_key=True), lambda lib: pin_delta_wy(lib, T=50, dk=8, dv=12, C=16),
         pin_transition_form, pin_invariants, pin_conv, pin_l2norm, pin_deltalog_equals_dense,
-        pin_batch_glue, pin_prenorm_log]
+        pin_batch_glue, pin_prenorm_log, pin_verify_routing]
 
 
 # ----------------------------------------------------------------------------
@@ -397,6 +431,10 @@ def test_batch_glue(oracle_lib):
 
 def test_prenorm_log(oracle_lib):
     pin_prenorm_log(oracle_lib)
+
+
+def test_verify_routing(oracle_lib):
+    pin_verify_routing(oracle_lib)
 
 
 def test_batch_errors(oracle_lib):
