@@ -42,6 +42,8 @@ L2NORM = 2
 PLAIN = 4
 GATE_RAW = 8
 KLOG_PRENORM = 16
+GATE_KDA = 32
+OUT_NORM_GATE = 64
 
 ERRORS = {0: "ok", 1: "bad argument", 2: "slot out of range", 3: "log length out of range"}
 
@@ -63,6 +65,12 @@ class OrcCfg(ctypes.Structure):
 
 _lock = threading.Lock()
 _lib = None
+
+
+class OrcKda(ctypes.Structure):
+    _fields_ = [("a_log", ctypes.POINTER(ctypes.c_double)), ("dt_bias", ctypes.POINTER(ctypes.c_double)),
+                ("out_gate", ctypes.POINTER(ctypes.c_double)), ("out_norm_w", ctypes.POINTER(ctypes.c_double)),
+                ("lower_bound", ctypes.c_double), ("out_eps", ctypes.c_double)]
 
 
 def build(force: bool = False, src: str | None = None, out_path: str | None = None) -> str:
@@ -101,6 +109,13 @@ def _declare(lib):
     lib.orc_step_batch.argtypes = [ctypes.POINTER(OrcCfg), ctypes.c_int, ip] + [dp] * 3 + \
         [dp] * 4 + [dp, dp] + [dp] * 5 + [ip, dp]
     lib.orc_step_batch.restype = ctypes.c_int
+    lib.orc_step_batch_ex.argtypes = [ctypes.POINTER(OrcCfg), ctypes.c_int, ip] + [dp] * 3 + \
+        [dp] * 4 + [dp, dp] + [dp] * 5 + [ip, ctypes.POINTER(OrcKda), dp]
+    lib.orc_step_batch_ex.restype = ctypes.c_int
+    lib.orc_kda_log_decay.argtypes = [ctypes.c_double] * 4
+    lib.orc_kda_log_decay.restype = ctypes.c_double
+    lib.orc_out_norm_gate.argtypes = [ctypes.c_int, dp, dp, dp, ctypes.c_double, dp]
+    lib.orc_out_norm_gate.restype = None
     return lib
 
 
@@ -215,8 +230,26 @@ class BatchState:
         self.conv = np.zeros((num_slots, nch, 3))
 
 
+def kda_log_decay(f, a_log, dt_bias, lower_bound, lib=None) -> float:
+    """KDA forget-gate parametrisation for one channel (see gdn_oracle.c)."""
+    lib = lib or load()
+    return lib.orc_kda_log_decay(float(f), float(a_log), float(dt_bias), float(lower_bound))
+
+
+def out_norm_gate(o, g, w=None, eps=1e-6, lib=None):
+    """KDA output epilogue for one head: RMSNorm over dv, weight w, output gate sigmoid(g)."""
+    lib = lib or load()
+    o, g = (_f64(np.ascontiguousarray(a, dtype=np.float64)) for a in (o, g))
+    w = None if w is None else _f64(np.ascontiguousarray(w, dtype=np.float64))
+    y = np.empty_like(o)
+    lib.orc_out_norm_gate(o.size, _ptr(o), _ptr(g), _ptr(w), float(eps), _ptr(y))
+    return y
+
+
 def step_batch(cfg: dict, mode: str, st: BatchState, slot, *, q=None, k=None, v=None,
-               mixed=None, conv_w=None, conv_b=None, lam=None, beta=None, o=None, lib=None):
+               mixed=None, conv_w=None, conv_b=None, lam=None, beta=None, o=None, lib=None,
+               a_log=None, dt_bias=None, out_gate=None, out_norm_w=None, lower_bound=-5.0,
+               out_eps=1e-6):
     """One decode step for a whole batch. ``mode`` is 'dense' or 'deltalog'.
 
     ``cfg`` keys: batch, num_heads, dk, dv, num_slots, dlam, log_capacity, flags,
@@ -233,11 +266,16 @@ def step_batch(cfg: dict, mode: str, st: BatchState, slot, *, q=None, k=None, v=
     q, k, v, mixed, conv_w, conv_b, lam, beta = map(
         lambda a: None if a is None else _f64(np.ascontiguousarray(a, dtype=np.float64)),
         (q, k, v, mixed, conv_w, conv_b, lam, beta))
-    rc = lib.orc_step_batch(ctypes.byref(c), {"dense": 0, "deltalog": 1}[mode],
-                            _ptr(slot, ctypes.c_int32), _ptr(q), _ptr(k), _ptr(v), _ptr(mixed),
-                            _ptr(conv_w), _ptr(conv_b), _ptr(st.conv), _ptr(lam), _ptr(beta),
-                            _ptr(st.S), _ptr(st.ell), _ptr(st.klog), _ptr(st.ulog),
-                            _ptr(st.lamlog), _ptr(st.len, ctypes.c_int32), _ptr(o))
+    a_log, dt_bias, out_gate, out_norm_w = map(
+        lambda a: None if a is None else _f64(np.ascontiguousarray(a, dtype=np.float64)),
+        (a_log, dt_bias, out_gate, out_norm_w))
+    kda = OrcKda(_ptr(a_log), _ptr(dt_bias), _ptr(out_gate), _ptr(out_norm_w), float(lower_bound),
+                 float(out_eps))
+    rc = lib.orc_step_batch_ex(ctypes.byref(c), {"dense": 0, "deltalog": 1}[mode],
+                               _ptr(slot, ctypes.c_int32), _ptr(q), _ptr(k), _ptr(v), _ptr(mixed),
+                               _ptr(conv_w), _ptr(conv_b), _ptr(st.conv), _ptr(lam), _ptr(beta),
+                               _ptr(st.S), _ptr(st.ell), _ptr(st.klog), _ptr(st.ulog),
+                               _ptr(st.lamlog), _ptr(st.len, ctypes.c_int32), ctypes.byref(kda), _ptr(o))
     if rc != 0:
         raise ValueError(f"oracle step_batch: {ERRORS.get(rc, rc)}")
     return o

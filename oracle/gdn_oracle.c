@@ -55,6 +55,8 @@
 #define ORC_PLAIN 4u        /* additive update: b = beta * v, no delta correction */
 #define ORC_GATE_RAW 8u     /* lambda = logsigmoid(a), beta = sigmoid(b_raw) */
 #define ORC_KLOG_PRENORM 16u /* log key factor = pre-normalisation key, value factor scaled */
+#define ORC_GATE_KDA 32u     /* lambda from the KDA gate parametrisation, beta = sigmoid(logit) */
+#define ORC_OUT_NORM_GATE 64u /* o <- RMSNorm(o) * w * sigmoid(g) per head */
 
 #define ORC_OK 0
 #define ORC_ERR_ARG 1
@@ -71,6 +73,16 @@ typedef struct {
   double q_scale, l2_eps;
 } orc_cfg;
 
+/* Optional per-head inputs of the KDA gate and output epilogue ([EVO] "KDA实现逻辑概述"). */
+typedef struct {
+  const double *a_log;      /* [H] */
+  const double *dt_bias;    /* [H][dlam] */
+  const double *out_gate;   /* [B][H][dv] output-gate logits */
+  const double *out_norm_w; /* [dv] RMSNorm weight, or NULL (1) */
+  double lower_bound;       /* lambda lies in (lower_bound, 0) */
+  double out_eps;           /* RMSNorm epsilon */
+} orc_kda;
+
 int orc_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();
@@ -81,6 +93,26 @@ int orc_num_threads(void) {
 
 static double orc_silu(double z) { return z / (1.0 + exp(-z)); }
 static double orc_sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
+
+/* KDA forget-gate parametrisation ([EVO] "KDA实现逻辑概述", the forget-gate block):
+ *   x = f + dt_bias,  z = exp(A_log) * x,  lambda = lower_bound * sigmoid(z),
+ * so lambda lies in (lower_bound, 0) and alpha = exp(lambda) in (e^lower_bound, 1). */
+double orc_kda_log_decay(double f, double a_log, double dt_bias, double lower_bound) {
+  const double x = f + dt_bias;
+  const double z = exp(a_log) * x;
+  return lower_bound * orc_sigmoid(z);
+}
+
+/* KDA output epilogue ([EVO] "KDA实现逻辑概述": o <- RMSNorm(o) (.) gamma with the output
+ * gate gamma = sigmoid(g)): y_j = o_j / sqrt(mean_j(o_j^2) + eps) * w_j * sigmoid(g_j),
+ * the mean over the dv channels of one head; w = NULL means w_j = 1. y may alias o. */
+void orc_out_norm_gate(int dv, const double *o, const double *g, const double *w, double eps,
+                       double *y) {
+  double ss = 0.0;
+  for (int j = 0; j < dv; ++j) ss += o[j] * o[j];
+  const double inv = 1.0 / sqrt(ss / dv + eps);
+  for (int j = 0; j < dv; ++j) y[j] = o[j] * inv * (w ? w[j] : 1.0) * orc_sigmoid(g[j]);
+}
 static double orc_log_sigmoid(double z) {
   return z < 0.0 ? z - log1p(exp(z)) : -log1p(exp(-z));
 }
@@ -240,25 +272,30 @@ int orc_deltalog_step(int dk, int dv, int dlam, int C, double *Sbar, double *ell
  *   q, k      [B][H][dk], v [B][H][dv]      (ignored with ORC_CONV)
  *   mixed     [B][nch], nch = 2*H*dk + H*dv; channel order [q heads | k heads | v heads]
  *   conv_w    [nch][4], conv_b [nch] or NULL, conv_pool [num_slots][nch][3]
- *   lam       [B][H][dlam] (raw gate logits with ORC_GATE_RAW), beta [B][H]
+ *   lam       [B][H][dlam] (raw gate logits with ORC_GATE_RAW, the forget pre-activation f
+ *             with ORC_GATE_KDA), beta [B][H] (logits with either)
  *   S_pool    [num_slots][H][dk][dv]  dense: the state; deltalog: the base
  *   ell       [num_slots][H][dlam], klog [num_slots][H][C][dk],
  *   ulog      [num_slots][H][C][dv], lamlog [num_slots][H][C][dlam], len [num_slots][H]
+ *   kda       optional KDA gate and epilogue inputs (ORC_GATE_KDA, ORC_OUT_NORM_GATE)
  *   o         [B][H][dv]           rows of padding requests are left untouched
  * mode 0 = dense, 1 = DeltaLog (append if the log has room, else merge).
  * ------------------------------------------------------------------------- */
-int orc_step_batch(const orc_cfg *cfg, int mode, const int32_t *slot,
-                   const double *q, const double *k, const double *v,
-                   const double *mixed, const double *conv_w, const double *conv_b,
-                   double *conv_pool, const double *lam, const double *beta,
-                   double *S_pool, double *ell, double *klog, double *ulog,
-                   double *lamlog, int32_t *len, double *o) {
+int orc_step_batch_ex(const orc_cfg *cfg, int mode, const int32_t *slot,
+                      const double *q, const double *k, const double *v,
+                      const double *mixed, const double *conv_w, const double *conv_b,
+                      double *conv_pool, const double *lam, const double *beta,
+                      double *S_pool, double *ell, double *klog, double *ulog,
+                      double *lamlog, int32_t *len, const orc_kda *kda, double *o) {
   const int B = cfg->batch, H = cfg->num_heads, dk = cfg->dk, dv = cfg->dv;
   const int dlam = cfg->dlam, C = cfg->log_capacity;
   const uint32_t fl = cfg->flags;
   if (B < 0 || H <= 0 || dk <= 0 || dv <= 0 || (dlam != 1 && dlam != dk) || C < 0)
     return ORC_ERR_ARG;
   if ((fl & ORC_KLOG_PRENORM) && ((fl & ORC_CONV) || !(fl & ORC_L2NORM))) return ORC_ERR_ARG;
+  if ((fl & ORC_GATE_KDA) && ((fl & ORC_GATE_RAW) || !kda || !kda->a_log || !kda->dt_bias))
+    return ORC_ERR_ARG;
+  if ((fl & ORC_OUT_NORM_GATE) && (!kda || !kda->out_gate)) return ORC_ERR_ARG;
   for (int b = 0; b < B; ++b)
     if (slot[b] >= cfg->num_slots) return ORC_ERR_SLOT;
   if (mode == 1)
@@ -314,6 +351,11 @@ int orc_step_batch(const orc_cfg *cfg, int mode, const int32_t *slot,
       if (fl & ORC_GATE_RAW) {
         for (int e = 0; e < dlam; ++e) lh[e] = orc_log_sigmoid(lr[e]);
         bh = orc_sigmoid(bh);
+      } else if (fl & ORC_GATE_KDA) {
+        for (int e = 0; e < dlam; ++e)
+          lh[e] = orc_kda_log_decay(lr[e], kda->a_log[h], kda->dt_bias[(size_t)h * dlam + e],
+                                    kda->lower_bound);
+        bh = orc_sigmoid(bh);
       } else {
         for (int e = 0; e < dlam; ++e) lh[e] = lr[e];
       }
@@ -333,6 +375,9 @@ int orc_step_batch(const orc_cfg *cfg, int mode, const int32_t *slot,
           err = rc;
         }
       }
+      if (fl & ORC_OUT_NORM_GATE)
+        orc_out_norm_gate(dv, oh, kda->out_gate + ((size_t)b * H + h) * dv, kda->out_norm_w,
+                          kda->out_eps, oh);
       free(qh);
       free(kh);
       free(lh);
@@ -340,4 +385,15 @@ int orc_step_batch(const orc_cfg *cfg, int mode, const int32_t *slot,
   }
   free(y);
   return err;
+}
+
+/* orc_step_batch_ex without the KDA gate / epilogue inputs. */
+int orc_step_batch(const orc_cfg *cfg, int mode, const int32_t *slot,
+                   const double *q, const double *k, const double *v,
+                   const double *mixed, const double *conv_w, const double *conv_b,
+                   double *conv_pool, const double *lam, const double *beta,
+                   double *S_pool, double *ell, double *klog, double *ulog,
+                   double *lamlog, int32_t *len, double *o) {
+  return orc_step_batch_ex(cfg, mode, slot, q, k, v, mixed, conv_w, conv_b, conv_pool, lam, beta,
+                           S_pool, ell, klog, ulog, lamlog, len, NULL, o);
 }

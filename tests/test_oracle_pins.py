@@ -357,10 +357,76 @@ def pin_verify_routing(lib, seed=11):
         assert np.array_equal(pool[row], init[row])
 
 
+def pin_kda_gate(lib):
+    """KDA forget-gate parametrisation (evolution article, "KDA实现逻辑概述"):
+    lambda = lower_bound * sigmoid(exp(A_log) (f + dt_bias)). Pinned by closed forms and
+    identities, not by retyping it: z = 0 gives lower_bound / 2; sigmoid(z) + sigmoid(-z) = 1
+    gives lambda(z) + lambda(-z) = lower_bound; A_log = log 2 equals doubling x; the range is
+    (lower_bound, 0) and lambda falls as f grows."""
+    lb = -5.0
+    for a, dt in ((0.0, -0.5), (1.7, 2.25), (-1.3, 0.0)):
+        assert oracle.kda_log_decay(-dt, a, dt, lb, lib) == lb / 2
+    r = _rng(12)
+    for _ in range(50):
+        f, a, dt = r.normal(0, 2), r.uniform(-2, 2), r.normal(0, 1)
+        lam = oracle.kda_log_decay(f, a, dt, lb, lib)
+        mirror = oracle.kda_log_decay(-f - 2 * dt, a, dt, lb, lib)  # x -> -x
+        assert lb < lam < 0 and abs(lam + mirror - lb) <= 1e-12
+        assert abs(oracle.kda_log_decay(f, np.log(2.0), dt, lb, lib)
+                   - oracle.kda_log_decay(2 * f + dt, 0.0, dt, lb, lib)) <= 1e-12
+        assert oracle.kda_log_decay(f + 0.1, a, dt, lb, lib) < lam
+
+
+def pin_out_norm_gate(lib):
+    """KDA output epilogue o <- RMSNorm(o) (.) sigmoid(g): the worked value for o = (3, 4)
+    at g = 0 is 1.5/sqrt(12.5) and 2/sqrt(12.5); with the gate open the output has unit
+    RMS; it is invariant to scaling o; the weight multiplies channel-wise; flipping the
+    gate's sign divides channel j by e^{g_j}."""
+    y = oracle.out_norm_gate([3.0, 4.0], [0.0, 0.0], eps=0.0, lib=lib)
+    assert np.max(np.abs(y - np.array([1.5, 2.0]) / np.sqrt(12.5))) <= 1e-15
+    r = _rng(13)
+    o, g, w = r.standard_normal(64), r.standard_normal(64), 1 + 0.1 * r.standard_normal(64)
+    open_gate = oracle.out_norm_gate(o, np.full(64, 40.0), eps=0.0, lib=lib)
+    assert abs(np.mean(open_gate ** 2) - 1.0) <= 1e-12
+    assert np.max(np.abs(oracle.out_norm_gate(7.5 * o, g, eps=0.0, lib=lib)
+                         - oracle.out_norm_gate(o, g, eps=0.0, lib=lib))) <= 1e-14
+    y1 = oracle.out_norm_gate(o, g, None, 1e-6, lib)
+    assert np.max(np.abs(oracle.out_norm_gate(o, g, w, 1e-6, lib) - w * y1)) <= 1e-14
+    assert np.max(np.abs(y1 / oracle.out_norm_gate(o, -g, None, 1e-6, lib) - np.exp(g))) <= 1e-12
+
+
+def pin_kda_batch_glue(lib, seed=14):
+    """The batch step with the KDA gate and epilogue flags equals the plain batch step fed
+    the gate function's lambda and sigmoid(beta), followed by the epilogue per head."""
+    r = _rng(seed)
+    B, H, d, M = 2, 2, 8, 3
+    slot = np.arange(B, dtype=np.int32)
+    a_log, dt = r.uniform(0, 2.7, H), -4 + 0.5 * r.standard_normal((H, d))
+    w = 1 + 0.1 * r.standard_normal(d)
+    for mode, C in (("dense", 0), ("deltalog", M - 1)):
+        cfg_k = _batch_cfg(B, H, d, d, B, d, C, oracle.L2NORM | oracle.GATE_KDA | oracle.OUT_NORM_GATE)
+        cfg_p = _batch_cfg(B, H, d, d, B, d, C, oracle.L2NORM)
+        sk, sp = oracle.BatchState(B, H, d, d, d, C), oracle.BatchState(B, H, d, d, d, C)
+        for t in range(7):
+            q, k, v = r.standard_normal((B, H, d)), r.standard_normal((B, H, d)), r.standard_normal((B, H, d))
+            f, logit, g = r.standard_normal((B, H, d)), r.standard_normal((B, H)), r.standard_normal((B, H, d))
+            ok = oracle.step_batch(cfg_k, mode, sk, slot, q=q, k=k, v=v, lam=f, beta=logit, lib=lib,
+                                   a_log=a_log, dt_bias=dt, out_gate=g, out_norm_w=w, lower_bound=-5.0)
+            lam = np.array([[[oracle.kda_log_decay(f[b, h, c], a_log[h], dt[h, c], -5.0, lib)
+                              for c in range(d)] for h in range(H)] for b in range(B)])
+            op = oracle.step_batch(cfg_p, mode, sp, slot, q=q, k=k, v=v, lam=lam,
+                                   beta=1 / (1 + np.exp(-logit)), lib=lib)
+            for b in range(B):
+                for h in range(H):
+                    ref = oracle.out_norm_gate(op[b, h], g[b, h], w, 1e-6, lib)
+                    assert np.max(np.abs(ok[b, h] - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
+
+
 PINS = [pin_teaching_dense, pin_teaching_deltalog, pin_gla_chunked, pin_delta_wy,
         lambda lib: pin_delta_wy(lib, per_key=True), lambda lib: pin_delta_wy(lib, T=50, dk=8, dv=12, C=16),
         pin_transition_form, pin_invariants, pin_conv, pin_l2norm, pin_deltalog_equals_dense,
-        pin_batch_glue, pin_prenorm_log, pin_verify_routing]
+        pin_batch_glue, pin_prenorm_log, pin_verify_routing, pin_kda_gate, pin_out_norm_gate,
+        pin_kda_batch_glue]
 
 
 # ----------------------------------------------------------------------------
@@ -437,6 +503,18 @@ def test_verify_routing(oracle_lib):
     pin_verify_routing(oracle_lib)
 
 
+def test_kda_gate(oracle_lib):
+    pin_kda_gate(oracle_lib)
+
+
+def test_out_norm_gate(oracle_lib):
+    pin_out_norm_gate(oracle_lib)
+
+
+def test_kda_batch_glue(oracle_lib):
+    pin_kda_batch_glue(oracle_lib)
+
+
 def test_batch_errors(oracle_lib):
     st = oracle.BatchState(2, 1, 4, 4, 1, 2)
     z = np.zeros((1, 1, 4))
@@ -497,6 +575,21 @@ MUTANTS = [
     ("raw decay gate uses sigmoid instead of logsigmoid",
      "lh[e] = orc_log_sigmoid(lr[e]);",
      "lh[e] = orc_sigmoid(lr[e]);"),
+    ("KDA gate: A_log not exponentiated",
+     "const double z = exp(a_log) * x;",
+     "const double z = a_log * x;"),
+    ("KDA gate: dt_bias subtracted",
+     "const double x = f + dt_bias;",
+     "const double x = f - dt_bias;"),
+    ("output RMSNorm over the sum instead of the mean",
+     "const double inv = 1.0 / sqrt(ss / dv + eps);",
+     "const double inv = 1.0 / sqrt(ss + eps);"),
+    ("output gate sign flipped",
+     "y[j] = o[j] * inv * (w ? w[j] : 1.0) * orc_sigmoid(g[j]);",
+     "y[j] = o[j] * inv * (w ? w[j] : 1.0) * orc_sigmoid(-g[j]);"),
+    ("epilogue not applied in the batch step",
+     "      if (fl & ORC_OUT_NORM_GATE)\n        orc_out_norm_gate(",
+     "      if (0)\n        orc_out_norm_gate("),
 ]
 
 
