@@ -173,6 +173,8 @@ def head_bytes(mode: str, n: int, w, klb=2, conv=False, ulb=4) -> int:
     e = 2 if w.qkv_bf16 else 4
     dlam = w.dlam
     common = 3 * D * e + 4 * dlam + (0 if w.raw_value else 4) + 4 * D  # q,k,v + lambda + beta + o
+    if w.kda_full:
+        common += 4 * D                                 # output-gate logits
     if conv:
         common += 3 * D * 3 * e * 2 + 3 * D * 16       # conv cache read + write, weights
     state = 4 * D * D
@@ -204,6 +206,11 @@ def run_gpu(args, rank, local_rank, world):
         flags |= gdn.KLOG_PRENORM
     if w.raw_value:  # the RWKV6 instantiation: b = v (beta NULL), raw q/k, bf16 value log
         flags |= gdn.PLAIN_UPDATE | gdn.NO_QK_L2NORM | gdn.ULOG_BF16
+    kda_dev = {}
+    if w.kda_full:   # the KDA gate parametrisation and output epilogue
+        flags |= gdn.GATE_KDA | gdn.OUT_NORM_GATE
+        kp = wl.kda_gate_params(w)
+        kda_dev = {n: torch.from_numpy(kp[n]).to(dev) for n in ("a_log", "dt_bias", "out_norm_w")}
     lib = gdn._abi.load()
     stream = torch.cuda.current_stream(dev)
     sptr = ctypes.c_void_p(stream.cuda_stream)
@@ -220,9 +227,14 @@ def run_gpu(args, rank, local_rank, world):
             for n_ in ("q", "k", "v"):
                 d[n_] = (torch.from_numpy(x[n_ + "_bits"].view(np.int16)).view(torch.bfloat16)
                          if w.qkv_bf16 else torch.from_numpy(x[n_]))
-        d["log_decay"] = torch.from_numpy(x["lam"])
-        if not w.raw_value:
-            d["beta"] = torch.from_numpy(x["beta"])
+        if w.kda_full:
+            d["log_decay"] = torch.from_numpy(x["f"])
+            d["beta"] = torch.from_numpy(x["b_raw"])
+            d["out_gate"] = torch.from_numpy(x["out_gate"])
+        else:
+            d["log_decay"] = torch.from_numpy(x["lam"])
+            if not w.raw_value:
+                d["beta"] = torch.from_numpy(x["beta"])
         host_ring.append({k: v.pin_memory() for k, v in d.items()})
         ring.append({k: v.to(dev) for k, v in d.items()})
     slot = torch.arange(B, dtype=torch.int32, device=dev)
@@ -241,7 +253,7 @@ def run_gpu(args, rank, local_rank, world):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def inputs_for(r, pools):
-        d = dict(ring[r])
+        d = dict(ring[r], **kda_dev)
         if w.conv:
             d.update(conv_w=conv_w, conv_pool=pools.conv)
         return gdn.make_inputs(slot=slot, **d)
@@ -366,7 +378,7 @@ def run_gpu(args, rank, local_rank, world):
     # ---- end to end through the public API: pinned host inputs in, o back to pinned host
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, M, dims_log, pools_l, host_ring, slot, conv_w, dev, stream, gdn)
+        e2e = run_e2e(args, w, M, dims_log, pools_l, host_ring, slot, conv_w, dev, stream, gdn, kda_dev)
 
     verify = run_verify(args, w, flags, dev, stream, gdn, peak) if args.verify else None
 
@@ -419,7 +431,7 @@ def run_verify(args, w, flags, dev, stream, gdn, peak):
     B, H, D, T = w.batch, w.num_heads, w.dk, args.verify
     if w.conv:
         return {"unavailable": "the verify path runs the dense recurrence without the fused conv"}
-    vflags = flags & ~(gdn.KLOG_PRENORM | gdn.ULOG_BF16)
+    vflags = flags & ~(gdn.KLOG_PRENORM | gdn.ULOG_BF16 | gdn.GATE_KDA | gdn.OUT_NORM_GATE)
     rng = np.random.default_rng(w.seed + 77)
     ring = []
     for t in range(RING):
@@ -504,7 +516,7 @@ class _Cudart:
             raise RuntimeError(f"{what} failed with CUDA error {rc}")
 
 
-def run_e2e(args, w, M, dims, pools, host_ring, slot, conv_w, dev, stream, gdn):
+def run_e2e(args, w, M, dims, pools, host_ring, slot, conv_w, dev, stream, gdn, kda_dev=None):
     """Same metric through the C ABI with host buffers. Every decode step copies its
     inputs (one packed pinned buffer: q/k/v or the conv input, log-decay, beta) host ->
     device, runs the decode call, and copies o back to pinned host memory. The copies
@@ -526,6 +538,7 @@ def run_e2e(args, w, M, dims, pools, host_ring, slot, conv_w, dev, stream, gdn):
     o_host = [torch.empty_like(o[0], device="cpu").pin_memory() for _ in range(2)]
     log = pools.log()
     extra = dict(conv_w=conv_w, conv_pool=pools.conv) if w.conv else {}
+    extra.update(kda_dev or {})  # per-head parameters stay resident; per-step inputs are copied
     inputs = [gdn.make_inputs(slot=slot, **_views(stage[b], offs, host_ring[0]), **extra)
               for b in range(2)]
     h2d = nbytes
@@ -617,6 +630,10 @@ def oracle_sample(w, steps_budget_s: float, max_steps: int, batch: int, warm=1):
     lib = oracle.load()
     H, D = w.num_heads, w.dk
     flags = (oracle.PLAIN if w.raw_value else oracle.L2NORM) | (oracle.CONV if w.conv else 0)
+    kp = None
+    if w.kda_full:
+        flags |= oracle.GATE_KDA | oracle.OUT_NORM_GATE
+        kp = wl.kda_gate_params(w)
     cfg = dict(batch=batch, num_heads=H, dk=D, dv=w.dv, num_slots=batch, dlam=w.dlam,
                log_capacity=0, flags=flags, q_scale=1.0, l2_eps=1e-6)
     st = oracle.BatchState(batch, H, D, w.dv, w.dlam, 0, nch=w.channels)
@@ -626,6 +643,10 @@ def oracle_sample(w, steps_budget_s: float, max_steps: int, batch: int, warm=1):
     for t in range(min(max_steps, RING)):
         x = wl.step_inputs(w, t, batch=batch)
         kw = dict(lam=x["lam"].astype(np.float64), beta=x["beta"].astype(np.float64))
+        if kp is not None:
+            kw = dict(lam=x["f"].astype(np.float64), beta=x["b_raw"].astype(np.float64),
+                      out_gate=x["out_gate"].astype(np.float64), lower_bound=kp["lower_bound"],
+                      **{n: kp[n].astype(np.float64) for n in ("a_log", "dt_bias", "out_norm_w")})
         if w.conv:
             kw.update(mixed=x["mixed"].astype(np.float64), conv_w=cw)
         else:

@@ -66,7 +66,7 @@
 extern "C" {
 #endif
 
-#define GDN_API_VERSION 1
+#define GDN_API_VERSION 2
 
 /* Synchronous return codes. */
 #define GDN_OK 0
@@ -95,6 +95,14 @@ extern "C" {
                                       of the DeltaLog notes, Sec. 2.7: a raw-value update has no
                                       correction to protect, so both logs are bf16). Exact when
                                       b = v of bf16 inputs (GDN_PLAIN_UPDATE, beta == NULL) */
+#define GDN_GATE_KDA (1u << 8)     /* the KDA gate parametrisation (evolution article, "KDA实现逻辑概述"):
+                                      log_decay holds the forget pre-activation f, beta the write
+                                      logit; lambda = gate_lower_bound * sigmoid(exp(a_log[h]) *
+                                      (f + dt_bias[h])), beta = sigmoid(logit). Needs in->a_log and
+                                      in->dt_bias; excludes GDN_GATE_RAW */
+#define GDN_OUT_NORM_GATE (1u << 9) /* output epilogue of the same section: o <- RMSNorm(o) (.) w (.)
+                                      sigmoid(g) per head over dv, RMSNorm(o) = o / sqrt(mean(o^2) +
+                                      out_eps); g = in->out_gate, w = in->out_norm_w (NULL: 1) */
 #define GDN_TEST_STARVE_WAIT (1u << 31) /* test only: the decode kernels expect 16 bytes more than
                                            the first tile copy delivers, so that bounded wait runs
                                            out (about a second) and the call reports
@@ -113,6 +121,8 @@ typedef struct gdn_dims {
   uint32_t flags;        /* GDN_* flags above */
   float q_scale;         /* multiplies q after normalisation (1.0: o = S^T q exactly) */
   float l2_eps;          /* x / sqrt(sum x^2 + l2_eps) */
+  float gate_lower_bound; /* GDN_GATE_KDA: lambda lies in (gate_lower_bound, 0) */
+  float out_eps;          /* GDN_OUT_NORM_GATE: epsilon of the RMSNorm */
 } gdn_dims;
 
 /* Per-token inputs of one decode step. dlam = decay_per_key ? dk : 1. */
@@ -130,6 +140,10 @@ typedef struct gdn_inputs {
                              NULL: beta = 1 for every head (the RWKV6 update k v^T with
                              GDN_PLAIN_UPDATE) */
   const int32_t *slot;    /* [B] pool row of each request; < 0 = padding */
+  const float *a_log;     /* GDN_GATE_KDA: [H] */
+  const float *dt_bias;   /* GDN_GATE_KDA: [H][dlam] */
+  const float *out_gate;  /* GDN_OUT_NORM_GATE: [B][H][dv] output-gate logits ([B][T][H][dv] for verify) */
+  const float *out_norm_w; /* GDN_OUT_NORM_GATE: [dv] RMSNorm weight shared by the heads, or NULL */
 } gdn_inputs;
 
 /* DeltaLog log pools (all [num_slots][H][...], updated in place). */

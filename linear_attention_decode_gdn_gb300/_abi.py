@@ -35,6 +35,8 @@ PLAIN_UPDATE = 1 << 4
 KLOG_FP32 = 1 << 5
 KLOG_PRENORM = 1 << 6
 ULOG_BF16 = 1 << 7
+GATE_KDA = 1 << 8
+OUT_NORM_GATE = 1 << 9
 TEST_STARVE_WAIT = 1 << 31
 
 # every symbol include/gdn.h declares
@@ -47,14 +49,17 @@ class Dims(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("num_heads", ctypes.c_int32), ("dk", ctypes.c_int32),
                 ("dv", ctypes.c_int32), ("num_slots", ctypes.c_int32),
                 ("decay_per_key", ctypes.c_int32), ("log_capacity", ctypes.c_int32),
-                ("flags", ctypes.c_uint32), ("q_scale", ctypes.c_float), ("l2_eps", ctypes.c_float)]
+                ("flags", ctypes.c_uint32), ("q_scale", ctypes.c_float), ("l2_eps", ctypes.c_float),
+                ("gate_lower_bound", ctypes.c_float), ("out_eps", ctypes.c_float)]
 
 
 class Inputs(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
                 ("mixed_qkv", ctypes.c_void_p), ("conv_w", ctypes.c_void_p),
                 ("conv_b", ctypes.c_void_p), ("conv_pool", ctypes.c_void_p),
-                ("log_decay", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("slot", ctypes.c_void_p)]
+                ("log_decay", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("slot", ctypes.c_void_p),
+                ("a_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p), ("out_gate", ctypes.c_void_p),
+                ("out_norm_w", ctypes.c_void_p)]
 
 
 class Log(ctypes.Structure):

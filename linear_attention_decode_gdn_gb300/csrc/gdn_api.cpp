@@ -15,6 +15,7 @@ thread_local char g_last_error[512] = "";
 
 constexpr uint32_t kKnownFlags = GDN_QKV_BF16 | GDN_FUSE_CONV | GDN_NO_QK_L2NORM | GDN_GATE_RAW |
                                  GDN_PLAIN_UPDATE | GDN_KLOG_FP32 | GDN_KLOG_PRENORM | GDN_ULOG_BF16 |
+                                 GDN_GATE_KDA | GDN_OUT_NORM_GATE |
                                  GDN_TEST_STARVE_WAIT;
 constexpr int kMaxLogCapacity = 63;
 
@@ -50,11 +51,22 @@ int check_dims(const gdn_dims* d, bool log_call) {
   if ((d->flags & GDN_KLOG_PRENORM) &&
       ((d->flags & GDN_FUSE_CONV) || (d->flags & GDN_NO_QK_L2NORM)))
     return fail(GDN_ERR_UNSUPPORTED, "GDN_KLOG_PRENORM needs L2 normalisation and no fused conv");
+  if ((d->flags & GDN_GATE_KDA) && (d->flags & GDN_GATE_RAW))
+    return fail(GDN_ERR_INVALID_ARG, "GDN_GATE_KDA and GDN_GATE_RAW exclude each other");
+  return GDN_OK;
+}
+
+int check_gate_inputs(const gdn_dims* d, const gdn_inputs* in) {
+  if ((d->flags & GDN_GATE_KDA) && (in->a_log == nullptr || in->dt_bias == nullptr))
+    return fail(GDN_ERR_INVALID_ARG, "GDN_GATE_KDA needs a_log and dt_bias");
+  if ((d->flags & GDN_OUT_NORM_GATE) && in->out_gate == nullptr)
+    return fail(GDN_ERR_INVALID_ARG, "GDN_OUT_NORM_GATE needs out_gate");
   return GDN_OK;
 }
 
 int check_inputs(const gdn_dims* d, const gdn_inputs* in) {
   if (in == nullptr) return fail(GDN_ERR_INVALID_ARG, "inputs is NULL");
+  if (int rc = check_gate_inputs(d, in)) return rc;
   if (in->slot == nullptr || in->log_decay == nullptr)
     return fail(GDN_ERR_INVALID_ARG, "slot and log_decay are required");
   if (d->flags & GDN_FUSE_CONV) {
@@ -106,6 +118,12 @@ gdn::DecodeParams make_params(const gdn_dims* d, const gdn_inputs* in) {
   p.lam = in->log_decay;
   p.beta = in->beta;
   p.slot = in->slot;
+  p.a_log = in->a_log;
+  p.dt_bias = in->dt_bias;
+  p.out_gate = in->out_gate;
+  p.out_norm_w = in->out_norm_w;
+  p.lower_bound = d->gate_lower_bound;
+  p.out_eps = d->out_eps;
   return p;
 }
 
@@ -224,6 +242,7 @@ int gdn_decode_verify(const gdn_dims* dims, int32_t num_tokens, const gdn_inputs
   if (dims->batch == 0) return GDN_OK;
   if (in == nullptr || in->log_decay == nullptr || in->q == nullptr || in->k == nullptr || in->v == nullptr)
     return fail(GDN_ERR_INVALID_ARG, "q, k, v and log_decay are required");
+  if ((rc = check_gate_inputs(dims, in)) != GDN_OK) return rc;
   if (!aligned16(in->q) || !aligned16(in->k) || !aligned16(in->v))
     return fail(GDN_ERR_UNSUPPORTED, "q, k and v must be 16-byte aligned");
   if (state_indices == nullptr || num_accepted == nullptr || state_pool == nullptr || o == nullptr)

@@ -73,8 +73,9 @@ __host__ __device__ inline Layout decode_layout(int mode, int D, int C, int klog
 }
 
 // The auto step carries both paths; its register cap keeps two CTAs per SM (its shared
-// memory allows two).  The other modes take no minimum (0: none).
-template <int D, int MODE>
+// memory allows two).  The other modes take no minimum (0: none).  EXT instances carry the
+// KDA gate parametrisation and output epilogue; the others compile them out.
+template <int D, int MODE, bool EXT>
 __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
 
@@ -124,7 +125,8 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
   float* tile = reinterpret_cast<float*>(smem + L.tile);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   int* scal_i = reinterpret_cast<int*>(smem + L.scal);             // [0] L on entry, [1] status bits
-  float* scal_f = reinterpret_cast<float*>(smem + L.scal + 16);    // [0..7] norm partials, [8] q.k
+  float* scal_f = reinterpret_cast<float*>(smem + L.scal + 16);    // [0..7] norm partials, [8] q.k,
+                                                                   // [12..15] output-norm partials
   float* q_s = reinterpret_cast<float*>(smem + L.vec);
   float* b_s = q_s;  // b takes q's place once the prologue is done
   float* k_s = q_s + D;
@@ -228,18 +230,27 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
   // both owners of key row ii form its decay exp(ell'), ell' = ell + lambda (closure
   // of the decays; a per-head decay reads entry 0).  The gate loads are issued before
   // the token loads so that the two latencies overlap.
-  float lam_t = 0.0f, ell_t = 0.0f, beta = 0.0f;
+  float lam_t = 0.0f, ell_t = 0.0f, beta = 0.0f, ga = 0.0f, gdt = 0.0f, og = 0.0f;
   if (is_q || is_k) {
     const int di = dlam == 1 ? 0 : ii;
     lam_t = __ldg(p.lam + (static_cast<size_t>(b) * p.H + h) * dlam + di);
     if (MODE != MODE_DENSE) ell_t = p.ell[sh * dlam + di];
+    if (EXT && (fl & GDN_GATE_KDA)) {
+      ga = __ldg(p.a_log + h);
+      gdt = __ldg(p.dt_bias + static_cast<size_t>(h) * dlam + di);
+    }
   }
+  if ((EXT && (fl & GDN_OUT_NORM_GATE)) && is_q) og = __ldg(p.out_gate + (static_cast<size_t>(b) * p.H + h) * D + ii);
   if (!ctrl) {
     beta = p.beta ? __ldg(p.beta + static_cast<size_t>(b) * p.H + h) : 1.0f;
     load_token(p, b, h, slot, tid, &x, &vj);
     if (fl & GDN_GATE_RAW) {
       lam_t = log_sigmoidf_(lam_t);
-      beta = sigmoidf_(beta);
+      if (p.beta) beta = sigmoidf_(beta);
+    } else if (EXT && (fl & GDN_GATE_KDA)) {
+      // KDA gate parametrisation: lambda in (lower_bound, 0), beta = sigmoid(logit)
+      lam_t = p.lower_bound * sigmoidf_(expf(ga) * (lam_t + gdt));
+      if (p.beta) beta = sigmoidf_(beta);
     }
     const float ss = warp_sum(x * x);
     if (lane == 0) scal_f[warp] = ss;
@@ -404,6 +415,7 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
   }
 
   // ---- phase 2: residual, write strength, readout, log commit ----------------------
+  float oj = 0.0f;
   if (is_q) {
     const int j = tid;
     float rk = red[j];
@@ -424,8 +436,8 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
       rq = fmaf(cq_s[e], u, rq);
     }
     const float bj = (fl & GDN_PLAIN_UPDATE) ? beta * vj : beta * (vj - rk);
-    const float oj = fmaf(scal_f[8] * qsc * kinv, bj, rq);
-    p.o[(static_cast<size_t>(b) * p.H + h) * D + j] = oj;
+    oj = fmaf(scal_f[8] * qsc * kinv, bj, rq);
+    if (!(EXT && (fl & GDN_OUT_NORM_GATE))) p.o[(static_cast<size_t>(b) * p.H + h) * D + j] = oj;
     b_s[j] = bj;
     if (is_append) {
       const float uval = (fl & GDN_KLOG_PRENORM) ? bj * kinv : bj;
@@ -434,6 +446,18 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
         reinterpret_cast<__nv_bfloat16*>(p.u_log)[at] = __float2bfloat16_rn(uval);
       else
         static_cast<float*>(p.u_log)[at] = uval;
+    }
+  }
+  if (EXT && (fl & GDN_OUT_NORM_GATE)) {
+    // KDA output epilogue: o <- o / sqrt(mean(o^2) + eps) * w * sigmoid(g) over the head's
+    // dv channels (the q-owning warps 0..3 hold them; the other lanes add zero)
+    const float ss = warp_sum(oj * oj);
+    if (lane == 0 && warp < 4) scal_f[12 + warp] = ss;
+    consumer_sync();
+    if (is_q) {
+      const float ms = (scal_f[12] + scal_f[13] + scal_f[14] + scal_f[15]) / static_cast<float>(D);
+      const float w = p.out_norm_w ? __ldg(p.out_norm_w + tid) : 1.0f;
+      p.o[(static_cast<size_t>(b) * p.H + h) * D + tid] = oj * (1.0f / sqrtf(ms + p.out_eps)) * w * sigmoidf_(og);
     }
   }
   if (is_append) {
@@ -549,7 +573,7 @@ int sm_count(int dev) {
 }
 
 
-template <int D, int MODE>
+template <int D, int MODE, bool EXT>
 cudaError_t launch_one(const DecodeParams& p, cudaStream_t stream) {
   static std::atomic<uint32_t> configured[kMaxDevices];
   const int klb = (p.flags & GDN_KLOG_FP32) ? 4 : 2;
@@ -560,12 +584,12 @@ cudaError_t launch_one(const DecodeParams& p, cudaStream_t stream) {
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (configured[dev].load(std::memory_order_relaxed) < L.total) {
-    err = cudaFuncSetAttribute(gdn_decode_kernel<D, MODE>,
+    err = cudaFuncSetAttribute(gdn_decode_kernel<D, MODE, EXT>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(L.total));
     if (err != cudaSuccess) return err;
     // several 64 KiB-tile CTAs per SM only fit with the whole L1/shared array as shared memory
-    err = cudaFuncSetAttribute(gdn_decode_kernel<D, MODE>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    err = cudaFuncSetAttribute(gdn_decode_kernel<D, MODE, EXT>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                static_cast<int>(cudaSharedmemCarveoutMaxShared));
     if (err != cudaSuccess) return err;
     configured[dev].store(L.total, std::memory_order_relaxed);
@@ -576,7 +600,7 @@ cudaError_t launch_one(const DecodeParams& p, cudaStream_t stream) {
   uint64_t rc = resident[dev].load(std::memory_order_relaxed);
   if ((rc >> 32) != L.total) {
     int per_sm = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gdn_decode_kernel<D, MODE>, NT_DECODE,
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gdn_decode_kernel<D, MODE, EXT>, NT_DECODE,
                                                         L.total);
     if (err != cudaSuccess) return err;
     rc = (static_cast<uint64_t>(L.total) << 32) | static_cast<uint32_t>(per_sm > 0 ? per_sm : 1);
@@ -595,20 +619,26 @@ cudaError_t launch_one(const DecodeParams& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, gdn_decode_kernel<D, MODE>, q);
+  err = cudaLaunchKernelEx(&cfg, gdn_decode_kernel<D, MODE, EXT>, q);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
-template <int D>
-cudaError_t launch_d(int mode, const DecodeParams& p, cudaStream_t stream) {
+template <int D, bool EXT>
+cudaError_t launch_de(int mode, const DecodeParams& p, cudaStream_t stream) {
   switch (mode) {
-    case MODE_DENSE: return launch_one<D, MODE_DENSE>(p, stream);
-    case MODE_APPEND: return launch_one<D, MODE_APPEND>(p, stream);
-    case MODE_MERGE: return launch_one<D, MODE_MERGE>(p, stream);
-    case MODE_STEP: return launch_one<D, MODE_STEP>(p, stream);
+    case MODE_DENSE: return launch_one<D, MODE_DENSE, EXT>(p, stream);
+    case MODE_APPEND: return launch_one<D, MODE_APPEND, EXT>(p, stream);
+    case MODE_MERGE: return launch_one<D, MODE_MERGE, EXT>(p, stream);
+    case MODE_STEP: return launch_one<D, MODE_STEP, EXT>(p, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+template <int D>
+cudaError_t launch_d(int mode, const DecodeParams& p, cudaStream_t stream) {
+  if (p.flags & (GDN_GATE_KDA | GDN_OUT_NORM_GATE)) return launch_de<D, true>(mode, p, stream);
+  return launch_de<D, false>(mode, p, stream);
 }
 
 }  // namespace

@@ -41,6 +41,12 @@ struct DecodeParams {
   int32_t* len;
   float* o;
   int32_t* status;
+  // KDA gate parametrisation and output epilogue
+  const float* a_log;
+  const float* dt_bias;
+  const float* out_gate;
+  const float* out_norm_w;
+  float lower_bound, out_eps;
   // verify: positions per request, [B][T] pool rows, [B] accepted counts
   int32_t T;
   const int32_t* state_indices;

@@ -31,8 +31,8 @@ __host__ __device__ inline VerifyLayout verify_layout(int D) {
   off += static_cast<uint32_t>(D * D * 4);
   L.bars = off;
   off += 64;
-  L.scal = off;  // int rows[16], int flags, then floats: partials[8], q.k
-  off += 128;
+  L.scal = off;  // int rows[16], int flags, then floats: partials[8], q.k, output-norm partials
+  off += 192;
   L.vec = off;   // per position parity: q (later b), k, q*dec, k*dec, dec
   off += static_cast<uint32_t>(2 * 5 * D * 4);
   L.red = off;   // cross-warp partial sums, [4 warps][2][D]
@@ -68,7 +68,8 @@ __global__ void __launch_bounds__(NT_DECODE) gdn_verify_kernel(const DecodeParam
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   int* rows_s = reinterpret_cast<int*>(smem + L.scal);            // [T] pool rows
   int* flags_s = rows_s + kMaxVerifyTokens;                       // 0 ok, 1 skip
-  float* scal_f = reinterpret_cast<float*>(smem + L.scal + 80);   // [0..7] partials, [8] q.k
+  float* scal_f = reinterpret_cast<float*>(smem + L.scal + 68);   // [0..7] partials, [8] q.k,
+                                                                  // [12..15] output-norm partials
   float* red = reinterpret_cast<float*>(smem + L.red);
 
   // the next launch may schedule once every CTA is resident; nothing is read before the
@@ -129,13 +130,24 @@ __global__ void __launch_bounds__(NT_DECODE) gdn_verify_kernel(const DecodeParam
     float* dec_s = vec + 4 * D;
 
     // ---- position t: gates, token, decays, norm partials -----------------------------
-    float x = 0.0f, vj = 0.0f, lam = 0.0f, beta = 1.0f;
+    float x = 0.0f, vj = 0.0f, lam = 0.0f, beta = 1.0f, ga = 0.0f, gdt = 0.0f, og = 0.0f;
     if (!ctrl) {
-      if (is_q || is_k) lam = __ldg(p.lam + (static_cast<size_t>(bt) * p.H + h) * dlam + (dlam == 1 ? 0 : ii));
+      const int di = dlam == 1 ? 0 : ii;
+      if (is_q || is_k) {
+        lam = __ldg(p.lam + (static_cast<size_t>(bt) * p.H + h) * dlam + di);
+        if (fl & GDN_GATE_KDA) {
+          ga = __ldg(p.a_log + h);
+          gdt = __ldg(p.dt_bias + static_cast<size_t>(h) * dlam + di);
+        }
+      }
+      if ((fl & GDN_OUT_NORM_GATE) && is_q) og = __ldg(p.out_gate + (static_cast<size_t>(bt) * p.H + h) * D + ii);
       if (p.beta) beta = __ldg(p.beta + static_cast<size_t>(bt) * p.H + h);
       load_token(p, bt, h, 0, tid, &x, &vj);
       if (fl & GDN_GATE_RAW) {
         lam = log_sigmoidf_(lam);
+        if (p.beta) beta = sigmoidf_(beta);
+      } else if (fl & GDN_GATE_KDA) {
+        lam = p.lower_bound * sigmoidf_(expf(ga) * (lam + gdt));
         if (p.beta) beta = sigmoidf_(beta);
       }
       const float ss = warp_sum(x * x);
@@ -226,6 +238,7 @@ __global__ void __launch_bounds__(NT_DECODE) gdn_verify_kernel(const DecodeParam
     }
 
     // ---- phase 2: residual, write strength, readout of position t -------------------
+    float oj = 0.0f;
     if (is_q) {
       const int j = tid;
       float rk = red[j] + red[2 * D + j];
@@ -237,8 +250,19 @@ __global__ void __launch_bounds__(NT_DECODE) gdn_verify_kernel(const DecodeParam
       rk = __fmul_rn(rk, kinv);
       rq = __fmul_rn(rq, qsc);
       const float bj = (fl & GDN_PLAIN_UPDATE) ? beta * vj : beta * (vj - rk);
-      p.o[(static_cast<size_t>(bt) * p.H + h) * D + j] = fmaf(scal_f[8] * qsc * kinv, bj, rq);
+      oj = fmaf(scal_f[8] * qsc * kinv, bj, rq);
+      if (!(fl & GDN_OUT_NORM_GATE)) p.o[(static_cast<size_t>(bt) * p.H + h) * D + j] = oj;
       b_s[j] = bj;
+    }
+    if (fl & GDN_OUT_NORM_GATE) {  // KDA output epilogue, as in the decode kernel
+      const float ss = warp_sum(oj * oj);
+      if (lane == 0 && warp < 4) scal_f[12 + warp] = ss;
+      consumer_sync();
+      if (is_q) {
+        const float ms = (scal_f[12] + scal_f[13] + scal_f[14] + scal_f[15]) / static_cast<float>(D);
+        const float w = p.out_norm_w ? __ldg(p.out_norm_w + tid) : 1.0f;
+        p.o[(static_cast<size_t>(bt) * p.H + h) * D + tid] = oj * (1.0f / sqrtf(ms + p.out_eps)) * w * sigmoidf_(og);
+      }
     }
     consumer_sync();  // (F) b is in shared memory; the sums have been read
 

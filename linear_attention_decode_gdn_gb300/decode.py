@@ -33,19 +33,23 @@ def _stream(stream):
 
 
 def make_dims(batch, num_heads, dk, dv=None, num_slots=None, *, decay_per_key=False,
-              log_capacity=0, flags=0, q_scale=1.0, l2_eps=1e-6) -> Dims:
+              log_capacity=0, flags=0, q_scale=1.0, l2_eps=1e-6, gate_lower_bound=-5.0,
+              out_eps=1e-6) -> Dims:
     dv = dk if dv is None else dv
     num_slots = batch if num_slots is None else num_slots
     return Dims(batch, num_heads, dk, dv, num_slots, int(bool(decay_per_key)), log_capacity, flags,
-                q_scale, l2_eps)
+                q_scale, l2_eps, gate_lower_bound, out_eps)
 
 
 def make_inputs(*, q=None, k=None, v=None, mixed_qkv=None, conv_w=None, conv_b=None,
-                conv_pool=None, log_decay=None, beta=None, slot=None) -> Inputs:
+                conv_pool=None, log_decay=None, beta=None, slot=None, a_log=None, dt_bias=None,
+                out_gate=None, out_norm_w=None) -> Inputs:
     inputs = Inputs(_ptr(q), _ptr(k), _ptr(v), _ptr(mixed_qkv), _ptr(conv_w), _ptr(conv_b),
-                    _ptr(conv_pool), _ptr(log_decay), _ptr(beta), _ptr(slot))
+                    _ptr(conv_pool), _ptr(log_decay), _ptr(beta), _ptr(slot), _ptr(a_log),
+                    _ptr(dt_bias), _ptr(out_gate), _ptr(out_norm_w))
     # the struct keeps the tensors alive for as long as it holds their addresses
-    inputs._keep = (q, k, v, mixed_qkv, conv_w, conv_b, conv_pool, log_decay, beta, slot)
+    inputs._keep = (q, k, v, mixed_qkv, conv_w, conv_b, conv_pool, log_decay, beta, slot, a_log,
+                    dt_bias, out_gate, out_norm_w)
     return inputs
 
 

@@ -18,6 +18,12 @@ Draw recipe (per workload, per decode step t):
   * raw-value workloads (the RWKV6 instantiation): the write-gate draw is made and
     discarded, beta = 1; q and k are not L2-normalised, so they are drawn with
     qk_mult = 1/sqrt(dk) (unit expected norm).
+  * workloads with the full KDA gate and output epilogue: the forget pre-activation
+    is f = (decay draw) - 3 ~ N(0,1), the write logit is the raw write-gate draw, and
+    the output-gate logits g ~ N(0,1) [B,H,dv] are drawn after them. Per-head
+    parameters come once from SeedSequence([seed, 2 << 20]): A_log = log U(1, 16)
+    [H], dt_bias = -4 + 0.5 N(0,1) [H, dlam], RMSNorm weight 1 + 0.1 N(0,1) [dv];
+    lower bound -5. With these, alpha = exp(lambda) lies mostly in (0.9, 1).
 """
 from __future__ import annotations
 
@@ -43,6 +49,7 @@ class Workload:
     conv_w_std: float = 0.5
     raw_value: bool = False  # RWKV6 update S <- D(lambda) S + k v^T: beta = 1, no correction
                              # and no L2 norm; K and U logs bf16
+    kda_full: bool = False   # KDA gate parametrisation and output epilogue (RMSNorm, gate)
     description: str = field(default="", compare=False)
 
     @property
@@ -71,6 +78,10 @@ WORKLOADS = {
                  1004, description="B=512, H=32, dk=dv=128, fp32 state 1 GiB, 128 steps, M in {1,2,4,8,16}"),
         Workload("kda", 256, 32, 128, 128, 128, (8,), True, False, True, 1005,
                  description="B=256, H=32, dk=dv=128, per-key-channel log decay (width 128), 128 steps, M=8"),
+        Workload("kda_full", 256, 32, 128, 128, 128, (8,), True, False, True, 1007, kda_full=True,
+                 description="B=256, H=32, dk=dv=128, KDA with its gate parametrisation "
+                             "(lower_bound sigmoid(exp(A_log)(f + dt_bias))) and output epilogue "
+                             "(RMSNorm, sigmoid output gate), 128 steps, M=8"),
         Workload("rwkv6", 128, 32, 128, 128, 128, (1, 4), True, False, True, 1006, qk_mult=128 ** -0.5,
                  raw_value=True,
                  description="B=128, H=32, dk=dv=128, per-key-channel log decay, raw-value update "
@@ -136,7 +147,21 @@ def step_inputs(w: Workload, t: int, batch: int | None = None) -> dict:
     if w.raw_value:
         beta = np.ones_like(beta)
     out.update(lam=lam, beta=beta, a_raw=a_raw, b_raw=b_raw)
+    if w.kda_full:
+        out["f"] = (a_raw - np.float32(3)).astype(np.float32)
+        out["out_gate"] = rng.standard_normal((B, w.num_heads, w.dv), dtype=np.float32)
     return out
+
+
+def kda_gate_params(w: Workload) -> dict:
+    """Per-head KDA gate and epilogue parameters (fp32), drawn once per workload."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([w.seed, 2 << 20])))
+    return {
+        "a_log": np.log(rng.uniform(1.0, 16.0, size=w.num_heads)).astype(np.float32),
+        "dt_bias": (-4.0 + 0.5 * rng.standard_normal((w.num_heads, w.dlam))).astype(np.float32),
+        "out_norm_w": (1.0 + 0.1 * rng.standard_normal(w.dv)).astype(np.float32),
+        "lower_bound": -5.0,
+    }
 
 
 def conv_weights(w: Workload) -> np.ndarray:

@@ -281,7 +281,8 @@ def step_batch(cfg: dict, mode: str, st: BatchState, slot, *, q=None, k=None, v=
     return o
 
 
-def verify_batch(cfg: dict, pool, state_indices, num_accepted, *, q, k, v, lam, beta, lib=None):
+def verify_batch(cfg: dict, pool, state_indices, num_accepted, *, q, k, v, lam, beta, lib=None,
+                 out_gate=None, **kda):
     """Speculative-decoding verify, written from the inference handbook's passage
     "推测解码：验证后如何恢复状态": a request feeds T positions (the last sampled token,
     then the drafts) through the recurrence; the initial state is the pool row of column
@@ -292,7 +293,9 @@ def verify_batch(cfg: dict, pool, state_indices, num_accepted, *, q, k, v, lam, 
     (row 0 < 0: padding request, skipped), ``num_accepted`` [B] in [1, T]; q, k [B,T,H,dk],
     v [B,T,H,dv], lam [B,T,H,dlam], beta [B,T,H]. ``cfg`` as for :func:`step_batch`
     (flags L2NORM / PLAIN / GATE_RAW, q_scale, l2_eps). Each position is one dense step of
-    :func:`step_batch`. Returns o [B, T, H, dv]."""
+    :func:`step_batch`; the KDA gate / epilogue inputs (``out_gate`` [B,T,H,dv], and
+    ``a_log``, ``dt_bias``, ``out_norm_w``, ``lower_bound``) pass through to it.
+    Returns o [B, T, H, dv]."""
     idx = np.asarray(state_indices, dtype=np.int64)
     na = np.asarray(num_accepted, dtype=np.int64)
     B, T = idx.shape
@@ -306,7 +309,8 @@ def verify_batch(cfg: dict, pool, state_indices, num_accepted, *, q, k, v, lam, 
     o = np.zeros((B, T, H, dv))
     for t in range(T):
         o[:, t] = step_batch(c, "dense", run, slot, q=q[:, t], k=k[:, t], v=v[:, t],
-                             lam=lam[:, t], beta=beta[:, t], lib=lib)
+                             lam=lam[:, t], beta=beta[:, t], lib=lib,
+                             out_gate=None if out_gate is None else out_gate[:, t], **kda)
         for b in live:
             pool[idx[b, t]] = run.S[b]
     return o

@@ -42,6 +42,8 @@ def base_flags(w: wl.Workload, gate_raw=False) -> int:
         f |= gdn.GATE_RAW
     if w.raw_value:  # the RWKV6 instantiation: b = v, raw q/k, bf16 value log
         f |= gdn.PLAIN_UPDATE | gdn.NO_QK_L2NORM | gdn.ULOG_BF16
+    if w.kda_full:   # the KDA gate parametrisation and output epilogue
+        f |= gdn.GATE_KDA | gdn.OUT_NORM_GATE
     return f
 
 
@@ -55,6 +57,10 @@ def oracle_flags(w: wl.Workload, gpu_flags: int) -> int:
         f |= oracle.PLAIN
     if gpu_flags & gdn.GATE_RAW:
         f |= oracle.GATE_RAW
+    if gpu_flags & gdn.GATE_KDA:
+        f |= oracle.GATE_KDA
+    if gpu_flags & gdn.OUT_NORM_GATE:
+        f |= oracle.OUT_NORM_GATE
     return f
 
 
@@ -129,13 +135,23 @@ class Lockstep:
             cw = wl.conv_weights(w)
             self.conv_w = cw.astype(F64)
             self.conv_w_dev = dev_f32(cw)
+        self.kda = wl.kda_gate_params(w) if w.kda_full else None
+        if self.kda:
+            self.kda_dev = {n: dev_f32(self.kda[n]) for n in ("a_log", "dt_bias", "out_norm_w")}
         self.t = 0
         self.ref_outputs = []
 
+    def gates(self, x):
+        """(log_decay input, beta input) as both sides receive them."""
+        if self.w.kda_full:
+            return x["f"], x["b_raw"]
+        if self.gate_raw:
+            return x["a_raw"], x["b_raw"]
+        return x["lam"], x["beta"]
+
     def device_inputs(self, x, v: Variant):
         w = self.w
-        lam = x["a_raw"] if self.gate_raw else x["lam"]
-        beta = x["b_raw"] if self.gate_raw else x["beta"]
+        lam, beta = self.gates(x)
         # raw-value workloads pass no beta (NULL: beta = 1); the oracle gets ones
         d = dict(log_decay=dev_f32(lam), beta=None if w.raw_value else dev_f32(beta), slot=self.slot_dev)
         if w.conv:
@@ -145,14 +161,19 @@ class Lockstep:
         else:
             for n in ("q", "k", "v"):
                 d[n] = dev_bf16(x[n + "_bits"]) if w.qkv_bf16 else dev_f32(x[n])
+        if w.kda_full:
+            d.update(self.kda_dev, out_gate=dev_f32(x["out_gate"]))
         return d
 
     def step(self):
         w = self.w
         x = wl.step_inputs(w, self.t, batch=self.B)
-        lam = x["a_raw"] if self.gate_raw else x["lam"]
-        beta = x["b_raw"] if self.gate_raw else x["beta"]
+        lam, beta = self.gates(x)
         kw = dict(lam=lam.astype(F64), beta=beta.astype(F64))
+        if w.kda_full:
+            kw.update(a_log=self.kda["a_log"].astype(F64), dt_bias=self.kda["dt_bias"].astype(F64),
+                      out_norm_w=self.kda["out_norm_w"].astype(F64), out_gate=x["out_gate"].astype(F64),
+                      lower_bound=self.kda["lower_bound"])
         if w.conv:
             kw.update(mixed=x["mixed"].astype(F64), conv_w=self.conv_w)
         else:

@@ -48,7 +48,7 @@ def test_library_exports_every_declared_symbol(gdn):
                          text=True, check=True).stdout
     exported = set(re.findall(r"\bT (gdn_\w+)", out))
     assert set(declared_functions()) <= exported
-    assert lib.gdn_version() == 1
+    assert lib.gdn_version() == 2
 
 
 def test_strerror(gdn):

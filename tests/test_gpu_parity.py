@@ -24,6 +24,7 @@ pytestmark = pytest.mark.gpu
 
 DENSE_TOL = 1e-4
 LOG_TOL = 5e-3
+EPILOGUE_BF16_KEY_TOL = 3e-2  # RMS-normalised output of the bf16-key log path (test_kda_full)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -83,6 +84,25 @@ def test_kda():
     w = wl.WORKLOADS["kda"]
     _check(Lockstep(w, [Variant("dense"), Variant("deltalog", 8),
                         Variant("deltalog", 8, extra_flags=gdn.KLOG_PRENORM, name="M=8/prenorm")]).run())
+
+
+def test_kda_full():
+    """KDA with its gate parametrisation, lambda = -5 sigmoid(exp(A_log)(f + dt_bias)) and
+    beta = sigmoid(logit), and its output epilogue o <- RMSNorm(o) w sigmoid(g) (evolution
+    article, "KDA实现逻辑概述"), fused into every decode mode."""
+    w = wl.WORKLOADS["kda_full"]
+    ls = Lockstep(w, [Variant("dense"), Variant("deltalog", 1, name="M=1/merge"),
+                      Variant("deltalog", 8, extra_flags=gdn.KLOG_PRENORM, name="M=8/prenorm"),
+                      Variant("deltalog", 8, "step", extra_flags=gdn.KLOG_PRENORM, name="M=8/step/prenorm"),
+                      Variant("deltalog", 8, name="M=8/bf16 keys")], batch=64).run()
+    # exact key factors: the composition is held to the dense bar. With bf16 keys the
+    # epilogue divides each head's core output by its own RMS, so a head whose core output
+    # is small by cancellation in S^T q shows the key rounding (2^-9 relative, replayed over
+    # up to 7 entries) at several times the global relative bar; the core output of the
+    # same path is held to 5e-3 in test_kda.
+    rep = _check(ls, tol_log=EPILOGUE_BF16_KEY_TOL)
+    for v in ls.variants[:4]:
+        assert v.rel_err <= DENSE_TOL, rep
 
 
 def test_rwkv6():

@@ -29,7 +29,7 @@ def _gpu():
 class Round:
     """One verify call's seeded inputs ([B, T, H, ...]) in both precisions."""
 
-    def __init__(self, B, T, H, D, per_key, bf16, seed, gate_raw=False, raw_value=False):
+    def __init__(self, B, T, H, D, per_key, bf16, seed, gate_raw=False, raw_value=False, kda=None):
         r = np.random.default_rng(seed)
         dlam = D if per_key else 1
         qkm = D ** -0.5 if raw_value else 1.0
@@ -48,6 +48,10 @@ class Round:
         if raw_value:
             self.beta[...] = 1
         self.gate_in = (a_raw, b_raw) if gate_raw else (self.lam, self.beta)
+        self.kda = kda
+        if kda is not None:  # the KDA gate takes the forget pre-activation and the write logit
+            self.gate_in = (a_raw - np.float32(3), b_raw)
+            self.out_gate = r.standard_normal((B, T, H, D), dtype=np.float32)
         self.q, self.k, self.v = q, k, v
         self.bf16, self.raw_value = bf16, raw_value
 
@@ -58,22 +62,34 @@ class Round:
             d[n] = dev_bf16(self.bits[n].reshape(a.shape)) if self.bf16 else dev_f32(a)
         d["log_decay"] = dev_f32(self.gate_in[0])
         d["beta"] = None if self.raw_value else dev_f32(self.gate_in[1])
+        if self.kda is not None:
+            d.update({n: dev_f32(self.kda[n]) for n in ("a_log", "dt_bias", "out_norm_w")},
+                     out_gate=dev_f32(self.out_gate))
         return d
 
     def oracle_inputs(self):
         f = lambda a: np.ascontiguousarray(a, dtype=np.float64)  # noqa: E731
-        return dict(q=f(self.q), k=f(self.k), v=f(self.v), lam=f(self.gate_in[0]), beta=f(self.gate_in[1]))
+        d = dict(q=f(self.q), k=f(self.k), v=f(self.v), lam=f(self.gate_in[0]), beta=f(self.gate_in[1]))
+        if self.kda is not None:
+            d.update(a_log=f(self.kda["a_log"]), dt_bias=f(self.kda["dt_bias"]),
+                     out_norm_w=f(self.kda["out_norm_w"]), out_gate=f(self.out_gate),
+                     lower_bound=self.kda["lower_bound"])
+        return d
 
 
-def _flags(bf16, gate_raw, raw_value):
+def _flags(bf16, gate_raw, raw_value, kda=False):
     f = (gdn.QKV_BF16 if bf16 else 0) | (gdn.GATE_RAW if gate_raw else 0)
     if raw_value:
         f |= gdn.PLAIN_UPDATE | gdn.NO_QK_L2NORM
+    if kda:
+        f |= gdn.GATE_KDA | gdn.OUT_NORM_GATE
     return f
 
 
-def _oracle_flags(gate_raw, raw_value):
+def _oracle_flags(gate_raw, raw_value, kda=False):
     f = oracle.GATE_RAW if gate_raw else 0
+    if kda:
+        f |= oracle.GATE_KDA | oracle.OUT_NORM_GATE
     return f | (oracle.PLAIN if raw_value else oracle.L2NORM)
 
 
@@ -86,7 +102,7 @@ def _rows(B, T, S, seed, pad=()):
 
 
 def _run(D, per_key, T, bf16=True, gate_raw=False, raw_value=False, B=6, H=3, seed=0, pad=(1,),
-         na=None, rounds=1):
+         na=None, rounds=1, kda=False):
     S = B * T + 5
     dlam = D if per_key else 1
     r = np.random.default_rng(seed + 99)
@@ -94,9 +110,13 @@ def _run(D, per_key, T, bf16=True, gate_raw=False, raw_value=False, B=6, H=3, se
     pool_dev = dev_f32(pool0)
     pool_ref = pool0.astype(np.float64)
     dims = gdn.make_dims(B, H, D, num_slots=S, decay_per_key=per_key,
-                         flags=_flags(bf16, gate_raw, raw_value), q_scale=D ** -0.5)
+                         flags=_flags(bf16, gate_raw, raw_value, kda), q_scale=D ** -0.5)
     cfg = dict(batch=B, num_heads=H, dk=D, dv=D, num_slots=S, dlam=dlam, log_capacity=0,
-               flags=_oracle_flags(gate_raw, raw_value), q_scale=D ** -0.5, l2_eps=1e-6)
+               flags=_oracle_flags(gate_raw, raw_value, kda), q_scale=D ** -0.5, l2_eps=1e-6)
+    params = None
+    if kda:
+        w = wl.Workload("verify_kda", B, H, D, D, 1, (1,), bf16, False, per_key, seed + 5, kda_full=True)
+        params = wl.kda_gate_params(w)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     rng = np.random.default_rng(seed + 7)
     idx = _rows(B, T, S, seed, pad)
@@ -104,7 +124,7 @@ def _run(D, per_key, T, bf16=True, gate_raw=False, raw_value=False, B=6, H=3, se
     for rd in range(rounds):
         acc = (np.asarray(na, dtype=np.int32) if na is not None and rd == 0
                else rng.integers(1, T + 1, size=B).astype(np.int32))
-        x = Round(B, T, H, D, per_key, bf16, seed + 1000 * rd, gate_raw, raw_value)
+        x = Round(B, T, H, D, per_key, bf16, seed + 1000 * rd, gate_raw, raw_value, params)
         o = torch.full((B, T, H, D), 7.0, dtype=torch.float32, device="cuda")
         keep = x.device_inputs()
         gdn.decode_verify(dims, T, gdn.make_inputs(**keep), dev_i32(idx), dev_i32(acc), pool_dev, o, status)
@@ -141,6 +161,13 @@ def test_verify_raw_value_update():
     """The RWKV6 form (beta NULL = 1, plain update, raw q/k) through the verify path."""
     e_o, e_s, _, _ = _run(128, True, 4, raw_value=True, seed=4)
     assert e_o <= TOL and e_s <= TOL, (e_o, e_s)
+
+
+def test_verify_kda_gate_and_epilogue():
+    """The KDA gate parametrisation and output epilogue through the verify path."""
+    for per_key in (True, False):
+        e_o, e_s, _, _ = _run(128, per_key, 4, kda=True, seed=8 + int(per_key))
+        assert e_o <= TOL and e_s <= TOL, (per_key, e_o, e_s)
 
 
 def test_verify_rollback_chain():
