@@ -13,6 +13,8 @@ Contents:
   * ``verify_batch`` -- speculative-decoding verify: T positions per request
     through the dense step, one pool row per position (composition of the
     pinned dense step with the row routing of the inference handbook).
+  * ``prefill_batch`` -- the prompt of every request through the dense step,
+    token by token, masked past each prompt length.
   * ``chunked.py``   -- numpy fp64 chunkwise forms (gated linear attention
     with a decay mask; the WY/UT form of the gated delta rule) used only to
     pin the recurrence against an independent algorithm.
@@ -313,4 +315,26 @@ def verify_batch(cfg: dict, pool, state_indices, num_accepted, *, q, k, v, lam, 
                              out_gate=None if out_gate is None else out_gate[:, t], **kda)
         for b in live:
             pool[idx[b, t]] = run.S[b]
+    return o
+
+
+def prefill_batch(cfg: dict, pool, slot, seq_lens, *, q, k, v, lam, beta, lib=None):
+    """The prompt through the recurrence, token by token: position t of request b is one dense
+    step of :func:`step_batch` on its pool row when t < seq_lens[b] (a prefill seeds the state
+    a decode continues from; evolution article, "Prefill中的Chunk微观并行", states the same
+    result for the chunked form). ``pool`` [num_slots, H, dk, dv] float64 is updated in place;
+    q, k [B,T,H,dk], v [B,T,H,dv], lam [B,T,H,dlam], beta [B,T,H]. Returns o [B,T,H,dv]
+    (zero past each prompt)."""
+    slot = np.asarray(slot, dtype=np.int32)
+    B, T = q.shape[0], q.shape[1]
+    H, dk, dv, dlam = cfg["num_heads"], cfg["dk"], cfg["dv"], cfg.get("dlam", 1)
+    lens = np.full(B, T) if seq_lens is None else np.asarray(seq_lens)
+    st = BatchState(cfg["num_slots"], H, dk, dv, dlam)
+    st.S = pool  # the step updates the caller's pool in place
+    c = dict(cfg, batch=B, log_capacity=0)
+    o = np.zeros((B, T, H, dv))
+    for t in range(T):
+        live = np.where((lens > t) & (slot >= 0), slot, -1).astype(np.int32)
+        o[:, t] = step_batch(c, "dense", st, live, q=q[:, t], k=k[:, t], v=v[:, t],
+                             lam=lam[:, t], beta=beta[:, t], lib=lib)
     return o

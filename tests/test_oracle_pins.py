@@ -422,11 +422,44 @@ def pin_kda_batch_glue(lib, seed=14):
                     assert np.max(np.abs(ok[b, h] - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
 
 
+def pin_prefill_batch(lib, seed=15):
+    """The batched prompt pass equals the independent WY/UT chunked algebra per (request,
+    head) from the same initial state, for both decay widths, with ragged prompt lengths
+    (rows past a prompt stay zero; padding requests and other pool rows stay untouched)."""
+    r = _rng(seed)
+    B, H, d, T, S = 3, 2, 8, 23, 5
+    slot = np.array([4, -1, 1], dtype=np.int32)
+    lens = np.array([23, 9, 11])
+    for dlam in (1, d):
+        pool = 0.3 * r.standard_normal((S, H, d, d))
+        init = pool.copy()
+        q, k = r.standard_normal((B, T, H, d)), r.standard_normal((B, T, H, d))
+        v = r.standard_normal((B, T, H, d))
+        lam = -np.log1p(np.exp(-(r.standard_normal((B, T, H, dlam)) + 3)))
+        beta = 1 / (1 + np.exp(-r.standard_normal((B, T, H))))
+        cfg = _batch_cfg(B, H, d, d, S, dlam, 0, oracle.L2NORM)
+        o = oracle.prefill_batch(cfg, pool, slot, lens, q=q, k=k, v=v, lam=lam, beta=beta, lib=lib)
+        for b in (0, 2):
+            n = lens[b]
+            for h in range(H):
+                qn = np.array([x / np.sqrt(x @ x + 1e-6) for x in q[b, :n, h]])  # eps as in the step
+                kn = np.array([x / np.sqrt(x @ x + 1e-6) for x in k[b, :n, h]])
+                g = np.repeat(lam[b, :n, h], d // dlam, axis=1) if dlam == 1 else lam[b, :n, h]
+                oc, Sc = chunked.delta_chunked_wy(qn, kn, v[b, :n, h], beta[b, :n, h], g, C=7,
+                                                  S0=init[slot[b], h])
+                assert np.max(np.abs(o[b, :n, h] - oc)) <= 1e-10 * max(1.0, np.max(np.abs(oc)))
+                assert np.max(np.abs(pool[slot[b], h] - Sc)) <= 1e-10 * max(1.0, np.max(np.abs(Sc)))
+            assert np.all(o[b, n:] == 0)
+        assert np.all(o[1] == 0)
+        for row in (0, 2, 3):
+            assert np.array_equal(pool[row], init[row])
+
+
 PINS = [pin_teaching_dense, pin_teaching_deltalog, pin_gla_chunked, pin_delta_wy,
         lambda lib: pin_delta_wy(lib, per_key=True), lambda lib: pin_delta_wy(lib, T=50, dk=8, dv=12, C=16),
         pin_transition_form, pin_invariants, pin_conv, pin_l2norm, pin_deltalog_equals_dense,
         pin_batch_glue, pin_prenorm_log, pin_verify_routing, pin_kda_gate, pin_out_norm_gate,
-        pin_kda_batch_glue]
+        pin_kda_batch_glue, pin_prefill_batch]
 
 
 # ----------------------------------------------------------------------------
@@ -501,6 +534,10 @@ def test_prenorm_log(oracle_lib):
 
 def test_verify_routing(oracle_lib):
     pin_verify_routing(oracle_lib)
+
+
+def test_prefill_batch(oracle_lib):
+    pin_prefill_batch(oracle_lib)
 
 
 def test_kda_gate(oracle_lib):
