@@ -253,6 +253,28 @@ int gdn_decode_verify(const gdn_dims *dims, int32_t num_tokens, const gdn_inputs
                       float *state_pool, float *o, int32_t *status, void *stream);
 
 /*
+ * gdn_prefill -- the prompt of every request through the recurrence, evaluated chunk by
+ * chunk with the WY/UT algebra (evolution article, "Prefill中的Chunk微观并行"; same
+ * arithmetic per token as gdn_decode_dense). The initial state is the request's pool row
+ * (zero it with gdn_slot_reset for a new request); the final state is written back there:
+ * the base a DeltaLog decode continues from (DeltaLog notes Sec. 2.8 -- reset the log of
+ * the slot as well).
+ *   num_tokens T: positions per request in the input arrays.
+ *   in->q, in->k, in->v [B][T][H][d] (bf16 or fp32), in->log_decay [B][T][H][dlam],
+ *   in->beta [B][T][H] (or NULL: beta = 1), in->slot [B] (< 0: padding).
+ *   seq_lens [B] int32 in [0, T]: the prompt length of each request, or NULL (all T).
+ *       Positions past it are not read and their o rows are left unchanged; a length
+ *       outside [0, T] skips the request with GDN_STATUS_BAD_LEN.
+ *   state_pool [num_slots][H][dk][dv] fp32, read and overwritten.
+ *   o [B][T][H][dv] fp32: the readout of every position.
+ * Flags: GDN_QKV_BF16, GDN_NO_QK_L2NORM, GDN_GATE_RAW, GDN_PLAIN_UPDATE and decay_per_key;
+ * GDN_FUSE_CONV, the log flags and the KDA gate / epilogue flags are rejected with
+ * GDN_ERR_UNSUPPORTED. Requires num_tokens >= 0.
+ */
+int gdn_prefill(const gdn_dims *dims, int32_t num_tokens, const gdn_inputs *in,
+                const int32_t *seq_lens, float *state_pool, float *o, int32_t *status, void *stream);
+
+/*
  * gdn_log_bytes -- byte sizes of the log pools for dims (num_slots, num_heads,
  * dk, dv, decay_per_key, log_capacity, GDN_KLOG_FP32, GDN_ULOG_BF16). Host only;
  * no GPU needed. residency equals (M-1) C_entry + C_decay of the DeltaLog notes'

@@ -42,7 +42,7 @@ TEST_STARVE_WAIT = 1 << 31
 # every symbol include/gdn.h declares
 EXPORTS = ("gdn_version", "gdn_strerror", "gdn_last_error", "gdn_conv_l2norm", "gdn_decode_dense",
            "gdn_decode_append", "gdn_decode_merge", "gdn_decode_step", "gdn_decode_verify",
-           "gdn_log_bytes", "gdn_slot_reset")
+           "gdn_prefill", "gdn_log_bytes", "gdn_slot_reset")
 
 
 class Dims(ctypes.Structure):
@@ -96,6 +96,8 @@ def _declare(lib):
         fn.argtypes = [P(Dims), P(Inputs), vp, P(Log), vp, vp, vp]
     lib.gdn_decode_verify.restype = ctypes.c_int
     lib.gdn_decode_verify.argtypes = [P(Dims), ctypes.c_int32, P(Inputs), vp, vp, vp, vp, vp, vp]
+    lib.gdn_prefill.restype = ctypes.c_int
+    lib.gdn_prefill.argtypes = [P(Dims), ctypes.c_int32, P(Inputs), vp, vp, vp, vp, vp]
     lib.gdn_log_bytes.restype = ctypes.c_int
     lib.gdn_log_bytes.argtypes = [P(Dims), P(LogSizes)]
     lib.gdn_slot_reset.restype = ctypes.c_int

@@ -259,6 +259,31 @@ int gdn_decode_verify(const gdn_dims* dims, int32_t num_tokens, const gdn_inputs
   return launched(gdn::launch_verify(p, static_cast<cudaStream_t>(stream)), "gdn_decode_verify");
 }
 
+int gdn_prefill(const gdn_dims* dims, int32_t num_tokens, const gdn_inputs* in, const int32_t* seq_lens,
+                float* state_pool, float* o, int32_t* status, void* stream) {
+  int rc = check_dims(dims, false);
+  if (rc != GDN_OK) return rc;
+  if (num_tokens < 0) return fail(GDN_ERR_INVALID_ARG, "num_tokens < 0");
+  if (dims->flags & (GDN_FUSE_CONV | GDN_KLOG_FP32 | GDN_KLOG_PRENORM | GDN_ULOG_BF16 | GDN_GATE_KDA |
+                     GDN_OUT_NORM_GATE | GDN_TEST_STARVE_WAIT))
+    return fail(GDN_ERR_UNSUPPORTED, "prefill: no fused conv, log or KDA epilogue flags");
+  if (static_cast<long long>(dims->batch) * num_tokens * dims->num_heads > 0x7fffffffLL)
+    return fail(GDN_ERR_INVALID_ARG, "batch * num_tokens * num_heads too large");
+  if (dims->batch == 0 || num_tokens == 0) return GDN_OK;
+  if (in == nullptr || in->slot == nullptr || in->log_decay == nullptr || in->q == nullptr ||
+      in->k == nullptr || in->v == nullptr)
+    return fail(GDN_ERR_INVALID_ARG, "q, k, v, log_decay and slot are required");
+  if (state_pool == nullptr || o == nullptr) return fail(GDN_ERR_INVALID_ARG, "state_pool and o are required");
+  if (!aligned16(state_pool)) return fail(GDN_ERR_UNSUPPORTED, "state_pool must be 16-byte aligned");
+  gdn::DecodeParams p = make_params(dims, in);
+  p.T = num_tokens;
+  p.seq_lens = seq_lens;
+  p.state = state_pool;
+  p.o = o;
+  p.status = status;
+  return launched(gdn::launch_prefill(p, static_cast<cudaStream_t>(stream)), "gdn_prefill");
+}
+
 int gdn_log_bytes(const gdn_dims* dims, gdn_log_sizes* out) {
   int rc = check_dims(dims, true);
   if (rc != GDN_OK) return rc;

@@ -51,6 +51,8 @@ struct DecodeParams {
   int32_t T;
   const int32_t* state_indices;
   const int32_t* num_accepted;
+  // prefill: [B] prompt lengths (NULL: all T)
+  const int32_t* seq_lens;
   // conv_l2norm outputs
   float* q_out;
   float* k_out;
@@ -73,6 +75,10 @@ cudaError_t launch_decode(int mode, const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_conv_l2norm(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_slot_reset(const ResetParams& p, cudaStream_t stream);
 cudaError_t launch_verify(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_prefill(const DecodeParams& p, cudaStream_t stream);
+
+// Dynamic shared memory of a prefill CTA (bytes).
+size_t prefill_smem_bytes(int D, int dlam);
 
 // Dynamic shared memory a decode launch needs (bytes); 0 if the shape is not built.
 size_t decode_smem_bytes(int mode, int D, int C, int dlam, int klog_bytes, int ulog_bytes);

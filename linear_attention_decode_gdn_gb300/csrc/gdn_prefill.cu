@@ -1,0 +1,370 @@
+// gdn_prefill.cu -- the prompt through the recurrence, chunk by chunk (WY/UT form).
+//
+// Evolution article, "Prefill中的Chunk微观并行" (its six-step order): inside a chunk of
+// C tokens with in-chunk cumulative log-decays gamma_t (per key channel),
+//   A_ts = beta_t k_t^T D(gamma_t - gamma_s) k_s   (s < t),   P_ts = q_t^T D(gamma_t - gamma_s) k_s  (s <= t)
+//   (I + A) B = diag(beta) (V - Ktil S0),   Ktil_t = e^{gamma_t} k_t       (the new values b_t)
+//   O_t = (Qtil S0)_t + sum_{s<=t} P_ts B_s,  Qtil_t = e^{gamma_t} q_t
+//   S_C = D(gamma_C) S0 + Khat^T B,          Khat_s = e^{gamma_C - gamma_s} k_s
+// which reproduces, token for token, the decode step's recurrence (decay first, residual on
+// the decayed state, outer-product write, post-update readout; S[dk][dv], o = S^T q).  The
+// plain update (b = beta v) has no A.  One CTA owns one (request, head) and keeps its state
+// in shared memory across the chunks; the products run on FP32 CUDA cores (fp32 keeps the
+// state at decode precision; the state leaves for the pool row at the end: the base a
+// DeltaLog decode continues from, DeltaLog notes Sec. 2.8).
+#include <atomic>
+
+#include "gdn_device.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int PC = 32;  // tokens per chunk (one warp's width: the pair reductions map s to lanes)
+
+struct PrefillLayout {
+  uint32_t S, Kn, Qn, V, Kt, Y, A, P, gam, bet, total;
+};
+
+__host__ __device__ inline PrefillLayout prefill_layout(int D, int dlam) {
+  PrefillLayout L{};
+  uint32_t off = 0;
+  L.S = off;    // state [D][D]
+  off += static_cast<uint32_t>(D * D * 4);
+  L.Kn = off;   // normalised keys [PC][D]
+  off += static_cast<uint32_t>(PC * D * 4);
+  L.Qn = off;   // normalised, scaled queries; then Qtil
+  off += static_cast<uint32_t>(PC * D * 4);
+  L.V = off;    // values; then R; then B
+  off += static_cast<uint32_t>(PC * D * 4);
+  L.Kt = off;   // Ktil; then Khat
+  off += static_cast<uint32_t>(PC * D * 4);
+  L.Y = off;    // Qtil S0
+  off += static_cast<uint32_t>(PC * D * 4);
+  L.A = off;    // [PC][PC]
+  off += static_cast<uint32_t>(PC * PC * 4);
+  L.P = off;
+  off += static_cast<uint32_t>(PC * PC * 4);
+  L.gam = off;  // cumulative log-decays [PC][dlam]
+  off += static_cast<uint32_t>(PC * dlam * 4);
+  L.bet = off;  // [PC]
+  off += static_cast<uint32_t>(PC * 4);
+  L.total = off;
+  return L;
+}
+
+// v[i] of every lane -> lane l holds the sum over lanes of v[l] (32 values, 31 shuffles).
+__device__ __forceinline__ float transpose_reduce(float (&v)[PC], int lane) {
+#pragma unroll
+  for (int k = PC / 2; k >= 1; k >>= 1) {
+    const bool upper = (lane & k) != 0;
+#pragma unroll
+    for (int i = 0; i < k; ++i) {
+      const float send = upper ? v[i] : v[i + k];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, k);
+      v[i] = (upper ? v[i + k] : v[i]) + recv;
+    }
+  }
+  return v[0];
+}
+
+template <int D>
+__global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int TCOL = D / 16;  // product tiles: 16 x 16 thread grid
+  constexpr int NI = (D + 31) / 32;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x / p.H;
+  const int h = blockIdx.x - b * p.H;
+  const int dlam = p.dlam;
+  const uint32_t fl = p.flags;
+  const bool bf16 = (fl & GDN_QKV_BF16) != 0u;
+  const bool plain = (fl & GDN_PLAIN_UPDATE) != 0u;
+  const bool l2 = (fl & GDN_NO_QK_L2NORM) == 0u;
+  const int T = p.T;
+
+  griddep_launch_dependents();
+  griddep_wait();
+
+  const int slot = __ldg(p.slot + b);
+  if (slot < 0) return;  // padding request
+  if (slot >= p.num_slots) {
+    if (tid == 0) atomic_status(p.status, GDN_STATUS_BAD_SLOT);
+    return;
+  }
+  const int n_tok = p.seq_lens ? __ldg(p.seq_lens + b) : T;
+  if (n_tok < 0 || n_tok > T) {
+    if (tid == 0) atomic_status(p.status, GDN_STATUS_BAD_LEN);
+    return;
+  }
+
+  const PrefillLayout L = prefill_layout(D, dlam);
+  float* S = reinterpret_cast<float*>(smem + L.S);
+  float* Kn = reinterpret_cast<float*>(smem + L.Kn);
+  float* Qn = reinterpret_cast<float*>(smem + L.Qn);
+  float* V = reinterpret_cast<float*>(smem + L.V);
+  float* Kt = reinterpret_cast<float*>(smem + L.Kt);
+  float* Y = reinterpret_cast<float*>(smem + L.Y);
+  float* A = reinterpret_cast<float*>(smem + L.A);
+  float* P = reinterpret_cast<float*>(smem + L.P);
+  float* gam = reinterpret_cast<float*>(smem + L.gam);
+  float* bet = reinterpret_cast<float*>(smem + L.bet);
+
+  float* Sg = p.state + (static_cast<size_t>(slot) * p.H + h) * static_cast<size_t>(D * D);
+  for (int i = tid; i < D * D / 4; i += NT)
+    reinterpret_cast<float4*>(S)[i] = reinterpret_cast<const float4*>(Sg)[i];
+
+  const int rg = tid >> 4, cg = tid & 15;  // product tile coordinates
+
+  for (int t0 = 0; t0 < n_tok; t0 += PC) {
+    const int n = (n_tok - t0 < PC) ? n_tok - t0 : PC;
+    __syncthreads();  // the previous chunk is done with every buffer
+
+    // ---- tokens: one warp per token; per-token L2 norms; positions >= n are zero --------
+    for (int tt = warp; tt < PC; tt += NW) {
+      const bool live = tt < n;
+      const size_t tokrow = (static_cast<size_t>(b) * T + t0 + tt) * p.H + h;
+      float qv[NI], kv[NI], vv[NI];
+      float sq = 0.0f, sk = 0.0f;
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        const int c = lane + 32 * i;
+        qv[i] = kv[i] = vv[i] = 0.0f;
+        if (live && c < D) {
+          qv[i] = load_elem(p.q, tokrow * D + c, bf16);
+          kv[i] = load_elem(p.k, tokrow * D + c, bf16);
+          vv[i] = load_elem(p.v, tokrow * D + c, bf16);
+        }
+        sq = fmaf(qv[i], qv[i], sq);
+        sk = fmaf(kv[i], kv[i], sk);
+      }
+      sq = warp_sum(sq);
+      sk = warp_sum(sk);
+      const float qsc = (l2 ? 1.0f / sqrtf(sq + p.l2_eps) : 1.0f) * p.q_scale;
+      const float kinv = l2 ? 1.0f / sqrtf(sk + p.l2_eps) : 1.0f;
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        const int c = lane + 32 * i;
+        if (c < D) {
+          Qn[tt * D + c] = qv[i] * qsc;
+          Kn[tt * D + c] = kv[i] * kinv;
+          V[tt * D + c] = vv[i];
+        }
+      }
+      for (int c = lane; c < dlam; c += 32) {
+        float lam = live ? __ldg(p.lam + tokrow * dlam + c) : 0.0f;
+        if (live && (fl & GDN_GATE_RAW)) lam = log_sigmoidf_(lam);
+        gam[tt * dlam + c] = lam;
+      }
+      if (lane == 0) {
+        float be = 0.0f;
+        if (live) {
+          be = p.beta ? __ldg(p.beta + tokrow) : 1.0f;
+          if (p.beta && (fl & GDN_GATE_RAW)) be = sigmoidf_(be);
+        }
+        bet[tt] = be;
+      }
+    }
+    __syncthreads();
+
+    // ---- cumulative log-decays inside the chunk --------------------------------------
+    for (int c = tid; c < dlam; c += NT) {
+      float acc = 0.0f;
+      for (int tt = 0; tt < PC; ++tt) {
+        acc += gam[tt * dlam + c];
+        gam[tt * dlam + c] = acc;
+      }
+    }
+    __syncthreads();
+
+    // ---- A (strictly lower, times beta_t) and P (lower with the diagonal) --------------
+    // warp w takes rows t = w, w + 8, ...; lane = key channel; the pair sums end in lane s
+    for (int t = warp; t < PC; t += NW) {
+      float ak[PC], aq[PC];
+#pragma unroll
+      for (int s = 0; s < PC; ++s) ak[s] = aq[s] = 0.0f;
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        const int c = lane + 32 * i;
+        if (c < D) {
+          const float kt = Kn[t * D + c], qt = Qn[t * D + c];
+          const float gt = (dlam > 1) ? gam[t * dlam + c] : 0.0f;
+#pragma unroll
+          for (int s = 0; s < PC; ++s) {
+            const float ks = Kn[s * D + c];
+            const float w = (dlam > 1) ? expf(gt - gam[s * dlam + c]) * ks : ks;
+            ak[s] = fmaf(kt, w, ak[s]);
+            aq[s] = fmaf(qt, w, aq[s]);
+          }
+        }
+      }
+      const float a_ts = transpose_reduce(ak, lane);
+      const float p_ts = transpose_reduce(aq, lane);
+      const float r = (dlam == 1) ? expf(gam[t] - gam[lane]) : 1.0f;  // per-head decay ratio
+      A[t * PC + lane] = (lane < t) ? bet[t] * (a_ts * r) : 0.0f;
+      P[t * PC + lane] = (lane <= t) ? p_ts * r : 0.0f;
+    }
+    __syncthreads();
+
+    // ---- Ktil = e^{gamma} k, Qtil = e^{gamma} q ----------------------------------------
+    for (int i = tid; i < PC * D; i += NT) {
+      const int tt = i / D, c = i - tt * D;
+      const float e = expf(gam[tt * dlam + (dlam > 1 ? c : 0)]);
+      Kt[i] = Kn[i] * e;
+      Qn[i] *= e;
+    }
+    __syncthreads();
+
+    // ---- [Ktil; Qtil] S0: R = diag(beta)(V - Ktil S0), Y = Qtil S0 ---------------------
+    // 64 rows (16 groups of 4) x D columns (16 groups of D/16); the Ktil rows are skipped
+    // under the plain update
+    if (!plain || rg >= 8) {
+      const float* Ain = (rg < 8) ? Kt : Qn;
+      const int r0 = (rg & 7) * 4;
+      float acc[4][TCOL];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < TCOL; ++j) acc[i][j] = 0.0f;
+#pragma unroll 4
+      for (int c = 0; c < D; ++c) {
+        float a[4], bv[TCOL];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = Ain[(r0 + i) * D + c];
+#pragma unroll
+        for (int j = 0; j < TCOL; ++j) bv[j] = S[c * D + cg * TCOL + j];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < TCOL; ++j) acc[i][j] = fmaf(a[i], bv[j], acc[i][j]);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int tt = r0 + i;
+#pragma unroll
+        for (int j = 0; j < TCOL; ++j) {
+          const int col = cg * TCOL + j;
+          if (rg < 8)
+            V[tt * D + col] = bet[tt] * (V[tt * D + col] - acc[i][j]);
+          else
+            Y[tt * D + col] = acc[i][j];
+        }
+      }
+    }
+    if (plain) {  // B = diag(beta) V
+      for (int i = tid; i < PC * D; i += NT) V[i] *= bet[i / D];
+    }
+    __syncthreads();
+
+    // ---- (I + A) B = R by forward substitution, then the readout; column-parallel -------
+    if (tid < D) {
+      const int j = tid;
+      float bc[PC];
+#pragma unroll
+      for (int t = 0; t < PC; ++t) {
+        float x = V[t * D + j];
+        if (!plain) {
+#pragma unroll
+          for (int s = 0; s < t; ++s) x = fmaf(-A[t * PC + s], bc[s], x);
+        }
+        bc[t] = x;
+      }
+#pragma unroll
+      for (int t = 0; t < PC; ++t) {
+        V[t * D + j] = bc[t];  // B for the state update
+        float y = Y[t * D + j];
+#pragma unroll
+        for (int s = 0; s <= t; ++s) y = fmaf(P[t * PC + s], bc[s], y);
+        if (t < n) p.o[((static_cast<size_t>(b) * T + t0 + t) * p.H + h) * D + j] = y;
+      }
+    }
+    // Khat = e^{gamma_C - gamma_s} k_s (rows past n hold zero keys)
+    for (int i = tid; i < PC * D; i += NT) {
+      const int tt = i / D, c = i - tt * D;
+      const int gc = (dlam > 1) ? c : 0;
+      Kt[i] = Kn[i] * expf(gam[(PC - 1) * dlam + gc] - gam[tt * dlam + gc]);
+    }
+    __syncthreads();
+
+    // ---- S <- D(gamma_C) S + Khat^T B ---------------------------------------------------
+    {
+      float acc[TCOL][TCOL];
+#pragma unroll
+      for (int i = 0; i < TCOL; ++i)
+#pragma unroll
+        for (int j = 0; j < TCOL; ++j) acc[i][j] = 0.0f;
+#pragma unroll 4
+      for (int s = 0; s < PC; ++s) {
+        float a[TCOL], bv[TCOL];
+#pragma unroll
+        for (int i = 0; i < TCOL; ++i) a[i] = Kt[s * D + rg * TCOL + i];
+#pragma unroll
+        for (int j = 0; j < TCOL; ++j) bv[j] = V[s * D + cg * TCOL + j];
+#pragma unroll
+        for (int i = 0; i < TCOL; ++i)
+#pragma unroll
+          for (int j = 0; j < TCOL; ++j) acc[i][j] = fmaf(a[i], bv[j], acc[i][j]);
+      }
+#pragma unroll
+      for (int i = 0; i < TCOL; ++i) {
+        const int r = rg * TCOL + i;
+        const float dC = expf(gam[(PC - 1) * dlam + (dlam > 1 ? r : 0)]);
+#pragma unroll
+        for (int j = 0; j < TCOL; ++j) {
+          const int col = cg * TCOL + j;
+          S[r * D + col] = fmaf(dC, S[r * D + col], acc[i][j]);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < D * D / 4; i += NT)
+    reinterpret_cast<float4*>(Sg)[i] = reinterpret_cast<const float4*>(S)[i];
+}
+
+constexpr int kMaxDevices = 64;
+
+template <int D>
+cudaError_t launch_prefill_d(const DecodeParams& p, cudaStream_t stream) {
+  static std::atomic<uint32_t> configured[kMaxDevices];
+  const PrefillLayout L = prefill_layout(D, p.dlam);
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (configured[dev].load(std::memory_order_relaxed) < L.total) {
+    err = cudaFuncSetAttribute(gdn_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(L.total));
+    if (err != cudaSuccess) return err;
+    configured[dev].store(L.total, std::memory_order_relaxed);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.B * p.H));
+  cfg.blockDim = dim3(NT);
+  cfg.dynamicSmemBytes = L.total;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, gdn_prefill_kernel<D>, p);
+  if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t prefill_smem_bytes(int D, int dlam) { return prefill_layout(D, dlam).total; }
+
+cudaError_t launch_prefill(const DecodeParams& p, cudaStream_t stream) {
+  switch (p.D) {
+    case 16: return launch_prefill_d<16>(p, stream);
+    case 32: return launch_prefill_d<32>(p, stream);
+    case 64: return launch_prefill_d<64>(p, stream);
+    case 128: return launch_prefill_d<128>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace gdn

@@ -101,6 +101,15 @@ def decode_verify(dims: Dims, num_tokens: int, inputs: Inputs, state_indices, nu
           "gdn_decode_verify")
 
 
+def prefill(dims: Dims, num_tokens: int, inputs: Inputs, state_pool, o, seq_lens=None, status=None,
+            stream=None):
+    """Chunked prefill: the prompt positions [B, T, H, d] through the recurrence from each
+    request's pool row; the final state is written back there. o [B, T, H, dv]."""
+    lib = _abi.load()
+    check(lib.gdn_prefill(ctypes.byref(dims), int(num_tokens), ctypes.byref(inputs), _ptr(seq_lens),
+                          _ptr(state_pool), _ptr(o), _ptr(status), _stream(stream)), "gdn_prefill")
+
+
 def log_bytes(dims: Dims) -> dict:
     lib = _abi.load()
     out = LogSizes()

@@ -1,0 +1,175 @@
+"""GPU parity of the chunked prefill (gdn_prefill) against the fp64 oracle's token-by-token
+prompt pass (which is pinned against the WY/UT chunked algebra): every position's readout,
+the final state in the pool row, ragged prompt lengths, and a decode that continues from
+the prefilled state."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+import linear_attention_decode_gdn_gb300 as gdn  # noqa: E402
+from linear_attention_decode_gdn_gb300 import workloads as wl  # noqa: E402
+
+from gpu_harness import dev_bf16, dev_f32, dev_i32  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-4  # the dense bar: per token the arithmetic is the dense step's
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from linear_attention_decode_gdn_gb300 import build
+    build.build()
+
+
+def _inputs(B, T, H, D, dlam, bf16, seed, raw_value=False, gate_raw=False):
+    r = np.random.default_rng(seed)
+    m = np.float32(D ** -0.5 if raw_value else 1.0)
+    x = {n: r.standard_normal((B, T, H, D), dtype=np.float32) * (m if n != "v" else np.float32(1))
+         for n in ("q", "k", "v")}
+    bits = {}
+    if bf16:
+        for n in x:
+            bits[n], x[n] = wl.bf16_round(x[n])
+    a_raw = r.standard_normal((B, T, H, dlam), dtype=np.float32) + np.float32(3)
+    b_raw = r.standard_normal((B, T, H), dtype=np.float32)
+    lam = (-np.log1p(np.exp(-a_raw.astype(np.float64)))).astype(np.float32)
+    beta = np.ones_like(b_raw) if raw_value else (1 / (1 + np.exp(-b_raw.astype(np.float64)))).astype(np.float32)
+    gin = (a_raw, b_raw) if gate_raw else (lam, beta)
+    dev = {n: (dev_bf16(bits[n]) if bf16 else dev_f32(x[n])) for n in x}
+    dev["log_decay"] = dev_f32(gin[0])
+    dev["beta"] = None if raw_value else dev_f32(gin[1])
+    ref = {n: x[n].astype(np.float64) for n in x}
+    ref.update(lam=gin[0].astype(np.float64), beta=gin[1].astype(np.float64))
+    return dev, ref
+
+
+def _run(D, per_key, T, lens, bf16=True, raw_value=False, gate_raw=False, H=3, seed=0,
+         slot=None, init_scale=0.1):
+    B = len(lens)
+    slot = np.arange(B, dtype=np.int32)[::-1].copy() if slot is None else np.asarray(slot, np.int32)
+    S = int(max(slot.max(), 0)) + 2
+    dlam = D if per_key else 1
+    flags = (gdn.QKV_BF16 if bf16 else 0) | (gdn.GATE_RAW if gate_raw else 0)
+    oflags = oracle.GATE_RAW if gate_raw else 0
+    if raw_value:
+        flags |= gdn.PLAIN_UPDATE | gdn.NO_QK_L2NORM
+        oflags |= oracle.PLAIN
+    else:
+        oflags |= oracle.L2NORM
+    r = np.random.default_rng(seed + 1)
+    pool0 = (init_scale * r.standard_normal((S, H, D, D))).astype(np.float32)
+    pool = dev_f32(pool0)
+    pool_ref = pool0.astype(np.float64)
+    dev, ref = _inputs(B, T, H, D, dlam, bf16, seed, raw_value, gate_raw)
+    dims = gdn.make_dims(B, H, D, num_slots=S, decay_per_key=per_key, flags=flags, q_scale=D ** -0.5)
+    cfg = dict(batch=B, num_heads=H, dk=D, dv=D, num_slots=S, dlam=dlam, log_capacity=0, flags=oflags,
+               q_scale=D ** -0.5, l2_eps=1e-6)
+    o = torch.full((B, T, H, D), 5.0, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gdn.prefill(dims, T, gdn.make_inputs(slot=dev_i32(slot), **dev), pool, o, seq_lens=dev_i32(lens), status=status)
+    o_ref = oracle.prefill_batch(cfg, pool_ref, slot, lens, **ref)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    og = o.cpu().numpy().astype(np.float64)
+    err = ref_max = 0.0
+    for b in range(B):
+        n = lens[b] if slot[b] >= 0 else 0
+        err = max(err, float(np.max(np.abs(og[b, :n] - o_ref[b, :n]), initial=0.0)))
+        ref_max = max(ref_max, float(np.max(np.abs(o_ref[b, :n]), initial=0.0)))
+        assert np.all(og[b, n:] == 5.0)  # positions past the prompt (and padding rows) untouched
+    pg = pool.cpu().numpy().astype(np.float64)
+    serr = float(np.max(np.abs(pg - pool_ref))) / float(np.max(np.abs(pool_ref)))
+    return err / ref_max, serr, pg
+
+
+@pytest.mark.parametrize("D", [16, 64, 128])
+@pytest.mark.parametrize("per_key", [False, True])
+def test_prefill_matches_oracle(D, per_key):
+    # lengths across the chunk boundaries: 0, 1, 31, 32, 33, 70 (ragged, 3 chunks)
+    e_o, e_s, _ = _run(D, per_key, 70, np.array([0, 1, 31, 32, 33, 70]), seed=D + int(per_key))
+    assert e_o <= TOL and e_s <= TOL, (e_o, e_s)
+
+
+def test_prefill_padding_fp32_raw_gates():
+    e_o, e_s, _ = _run(128, False, 40, np.array([40, 17, 40, 5]), bf16=False, gate_raw=True,
+                       slot=[2, -1, 0, 4], seed=3)
+    assert e_o <= TOL and e_s <= TOL, (e_o, e_s)
+
+
+def test_prefill_raw_value_update():
+    """The RWKV6 form: per-key decay, b = v (beta NULL), raw q and k."""
+    e_o, e_s, _ = _run(128, True, 64, np.array([64, 40, 3]), raw_value=True, seed=4)
+    assert e_o <= TOL and e_s <= TOL, (e_o, e_s)
+
+
+def test_prefill_long_prompt_from_zero():
+    """A fresh request (zero state) over a long prompt of many chunks."""
+    e_o, e_s, _ = _run(128, False, 300, np.array([300, 257]), H=4, seed=5, init_scale=0.0)
+    assert e_o <= TOL and e_s <= TOL, (e_o, e_s)
+
+
+def test_prefill_then_decode():
+    """Prefill seeds the state; a dense decode and a DeltaLog cycle continue from it, and
+    both match the oracle's token-by-token pass over prompt + generated tokens."""
+    w = wl.WORKLOADS["headline"]
+    B, H, D, T, M = 8, 4, 128, 45, 4
+    lens = np.full(B, T)
+    slot = np.arange(B, dtype=np.int32)
+    dev, ref = _inputs(B, T, H, D, 1, True, 11)
+    cfg = dict(batch=B, num_heads=H, dk=D, dv=D, num_slots=B, dlam=1, log_capacity=0,
+               flags=oracle.L2NORM, q_scale=1.0, l2_eps=1e-6)
+    pool_ref = np.zeros((B, H, D, D))
+    oracle.prefill_batch(cfg, pool_ref, slot, lens, **ref)
+    st = oracle.BatchState(B, H, D, D)
+    st.S = pool_ref
+    dims_d = gdn.make_dims(B, H, D, num_slots=B, flags=gdn.QKV_BF16)
+    dims_l = gdn.make_dims(B, H, D, num_slots=B, flags=gdn.QKV_BF16, log_capacity=M - 1)
+    pd = gdn.Pools.allocate(dims_d)
+    pl = gdn.Pools.allocate(dims_l, deltalog=True)
+    o_pf = torch.zeros((B, T, H, D), device="cuda")
+    slot_dev = dev_i32(slot)
+    for pools in (pd, pl):
+        gdn.prefill(dims_d, T, gdn.make_inputs(slot=slot_dev, **dev), pools.state, o_pf)
+    gdn.slot_reset(dims_l, slot_dev, B, pl.log())  # a prefilled base starts with an empty log
+    o_d = torch.zeros((B, H, D), device="cuda")
+    o_l = torch.zeros((B, H, D), device="cuda")
+    err_d = err_l = ref_max = 0.0
+    for t in range(2 * M):
+        x = wl.step_inputs(w, 500 + t, batch=B)
+        d = dict(slot=slot_dev, log_decay=dev_f32(x["lam"]), beta=dev_f32(x["beta"]),
+                 **{n: dev_bf16(x[n + "_bits"]) for n in ("q", "k", "v")})
+        gdn.decode_dense(dims_d, gdn.make_inputs(**d), pd.state, o_d)
+        call = gdn.decode_merge if (t + 1) % M == 0 else gdn.decode_append
+        call(dims_l, gdn.make_inputs(**d), pl.state, pl.log(), o_l)
+        o_ref = oracle.step_batch(cfg, "dense", st, slot, q=x["q"].astype(np.float64), k=x["k"].astype(np.float64),
+                                  v=x["v"].astype(np.float64), lam=x["lam"].astype(np.float64),
+                                  beta=x["beta"].astype(np.float64))
+        torch.cuda.synchronize()
+        err_d = max(err_d, float(np.max(np.abs(o_d.cpu().numpy() - o_ref))))
+        err_l = max(err_l, float(np.max(np.abs(o_l.cpu().numpy() - o_ref))))
+        ref_max = max(ref_max, float(np.max(np.abs(o_ref))))
+    assert err_d / ref_max <= TOL, err_d / ref_max
+    assert err_l / ref_max <= 5e-3, err_l / ref_max
+
+
+def test_prefill_status_and_skips():
+    B, H, D, T = 3, 2, 64, 10
+    dims = gdn.make_dims(B, H, D, num_slots=4, flags=gdn.QKV_BF16)
+    dev, _ = _inputs(B, T, H, D, 1, True, 21)
+    pool0 = np.random.default_rng(22).standard_normal((4, H, D, D)).astype(np.float32)
+    pool = dev_f32(pool0)
+    o = torch.full((B, T, H, D), 9.0, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gdn.prefill(dims, T, gdn.make_inputs(slot=dev_i32([0, 7, 2]), **dev), pool, o,
+                seq_lens=dev_i32([10, 10, 11]), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == gdn.STATUS_BAD_SLOT | gdn.STATUS_BAD_LEN
+    pg = pool.cpu().numpy()
+    assert np.array_equal(pg[2], pool0[2]) and np.array_equal(pg[1], pool0[1]) and np.array_equal(pg[3], pool0[3])
+    assert not np.array_equal(pg[0], pool0[0])
+    assert torch.all(o[1] == 9.0) and torch.all(o[2] == 9.0)
