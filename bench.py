@@ -381,8 +381,10 @@ def run_gpu(args, rank, local_rank, world):
         e2e = run_e2e(args, w, M, dims_log, pools_l, host_ring, slot, conv_w, dev, stream, gdn, kda_dev)
 
     verify = run_verify(args, w, flags, dev, stream, gdn, peak) if args.verify else None
+    prefill = run_prefill(args, w, flags, dev, stream, gdn) if args.prefill else None
 
-    launches = args.steps * M * 4 + (e2e["launches"] if e2e else 0) + (verify["launches"] if verify else 0)
+    launches = (args.steps * M * 4 + (e2e["launches"] if e2e else 0) + (verify["launches"] if verify else 0)
+                + (prefill.get("launches", 0) if prefill else 0))
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": lt / args.steps * 1e3, "higher_is_better": True,
@@ -402,6 +404,7 @@ def run_gpu(args, rank, local_rank, world):
         "roofline": roofline,
         "e2e": e2e,
         **({"verify": verify} if verify else {}),
+        **({"prefill": prefill} if prefill else {}),
         "gpu_launches": launches,
         "clocks": {k: v for k, v in clocks.summary().items()},
     }
@@ -480,6 +483,76 @@ def run_verify(args, w, flags, dev, stream, gdn, peak):
             "us_per_call": el / calls * 1e6, "calls": calls, "launches": calls + max(3, args.warmup),
             "algorithmic_bytes_per_call": B * H * per_head, "algorithmic_gbs": gbs, "frac_of_peak": gbs / peak,
             "state_rows": "one read + T writes of the 64 KiB state per (request, head)"}
+
+
+FP32_FMA_PER_SM_CLK = 128   # GB300 SM: 4 partitions x 32 FP32 lanes
+GB300_SMS = 152
+GB300_MAX_SM_MHZ = 2070.0
+
+
+def prefill_chunk_fmas(D: int, C: int, plain: bool) -> int:
+    """Algorithmic FMAs of one chunk of C positions of one head in the WY/UT prefill:
+    pair sums (A strictly lower unless plain, P lower with the diagonal), [Ktil; Qtil] S0
+    (only Qtil under the plain update), the forward substitution, the readout P B and
+    Khat^T B. Elementwise scalings are left out."""
+    pairs_p = C * (C + 1) // 2
+    pairs_a = 0 if plain else C * (C - 1) // 2
+    gemm1 = (1 if plain else 2) * C * D * D
+    subst = 0 if plain else C * (C - 1) // 2 * D
+    return (pairs_a + pairs_p) * D + gemm1 + subst + pairs_p * D + D * D * C
+
+
+def run_prefill(args, w, flags, dev, stream, gdn):
+    """Chunked prefill on the workload's batch shape: T = args.prefill positions per request
+    from a zero state, through gdn_prefill. Compute-bound: reported against the FP32 ALU peak
+    derived from the SM count, the FP32 lanes per SM and the maximum SM clock."""
+    import torch
+    B, H, D, T = w.batch, w.num_heads, w.dk, args.prefill
+    if w.conv:
+        return {"unavailable": "the prefill path does not fuse the conv"}
+    pflags = flags & (gdn.QKV_BF16 | gdn.NO_QK_L2NORM | gdn.PLAIN_UPDATE)
+    rng = np.random.default_rng(w.seed + 99)
+    x = {}
+    for n in ("q", "k", "v"):
+        a = rng.standard_normal((B, T, H, D), dtype=np.float32) * np.float32(1.0 if n == "v" else w.qk_mult)
+        bits, _ = wl_bf16(a)
+        x[n] = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16) if w.qkv_bf16 \
+            else torch.from_numpy(a).to(dev)
+    a_raw = rng.standard_normal((B, T, H, w.dlam), dtype=np.float32) + np.float32(3)
+    x["log_decay"] = torch.from_numpy((-np.log1p(np.exp(-a_raw))).astype(np.float32)).to(dev)
+    if not w.raw_value:
+        b_raw = rng.standard_normal((B, T, H), dtype=np.float32)
+        x["beta"] = torch.from_numpy((1 / (1 + np.exp(-b_raw))).astype(np.float32)).to(dev)
+    slot = torch.arange(B, dtype=torch.int32, device=dev)
+    inp = gdn.make_inputs(slot=slot, **x)
+    dims = gdn.make_dims(B, H, D, num_slots=B, decay_per_key=w.decay_per_key, flags=pflags)
+    pool = torch.zeros((B, H, D, D), dtype=torch.float32, device=dev)
+    o = torch.zeros((B, T, H, D), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    calls = max(3, min(20, args.steps // 100))
+    for _ in range(max(2, args.warmup // 2)):
+        gdn.prefill(dims, T, inp, pool, o, status=status, stream=stream)
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(calls):
+        gdn.prefill(dims, T, inp, pool, o, status=status, stream=stream)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the prefill run")
+    el, units = reduce_timing(t0.elapsed_time(t1) / 1e3, B * H * T * calls, device=dev)
+    chunks = -(-T // 32)
+    flops = 2.0 * prefill_chunk_fmas(D, 32, bool(pflags & gdn.PLAIN_UPDATE)) * chunks * B * H
+    tflops = flops * calls / el / 1e12
+    peak = GB300_SMS * FP32_FMA_PER_SM_CLK * 2 * GB300_MAX_SM_MHZ * 1e6 / 1e12
+    return {"value": units / el, "unit": "positions x heads / s", "positions_per_request": T,
+            "ms_per_call": el / calls * 1e3, "calls": calls, "launches": calls + max(2, args.warmup // 2),
+            "roofline": {"bound": "alu", "achieved": tflops, "peak": peak, "unit": "TFLOP/s (fp32)",
+                         "frac": tflops / peak,
+                         "peak_derivation": "152 SMs x 128 FP32 FMA/clk x 2 FLOP x 2070 MHz",
+                         "algorithmic_flops_per_call": flops}}
 
 
 def wl_bf16(a):
@@ -714,6 +787,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill", type=int, default=0,
+                    help="also time the chunked prefill with this many positions per request")
     ap.add_argument("--verify", type=int, default=0,
                     help="also time the speculative-decoding verify path with this many positions")
     args = ap.parse_args(argv)
