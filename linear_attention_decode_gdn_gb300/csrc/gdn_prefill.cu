@@ -121,48 +121,80 @@ __global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
     __syncthreads();  // the previous chunk is done with every buffer
 
     // ---- tokens: one warp per token; per-token L2 norms; positions >= n are zero --------
-    for (int tt = warp; tt < PC; tt += NW) {
-      const bool live = tt < n;
-      const size_t tokrow = (static_cast<size_t>(b) * T + t0 + tt) * p.H + h;
-      float qv[NI], kv[NI], vv[NI];
-      float sq = 0.0f, sk = 0.0f;
+    // every load of the warp's tokens is issued before any is used, so the chunk waits for
+    // one round trip rather than one per token
+    {
+      constexpr int TPW = PC / NW;  // tokens per warp
+      float qv[TPW][NI], kv[TPW][NI], vv[TPW][NI], lv[TPW][NI], bv[TPW];
+      // raw loads first (the dtype branch outside the loops), conversions after them
+      uint32_t qr[TPW][NI], kr[TPW][NI], vr[TPW][NI];
 #pragma unroll
-      for (int i = 0; i < NI; ++i) {
-        const int c = lane + 32 * i;
-        qv[i] = kv[i] = vv[i] = 0.0f;
-        if (live && c < D) {
-          qv[i] = load_elem(p.q, tokrow * D + c, bf16);
-          kv[i] = load_elem(p.k, tokrow * D + c, bf16);
-          vv[i] = load_elem(p.v, tokrow * D + c, bf16);
-        }
-        sq = fmaf(qv[i], qv[i], sq);
-        sk = fmaf(kv[i], kv[i], sk);
-      }
-      sq = warp_sum(sq);
-      sk = warp_sum(sk);
-      const float qsc = (l2 ? 1.0f / sqrtf(sq + p.l2_eps) : 1.0f) * p.q_scale;
-      const float kinv = l2 ? 1.0f / sqrtf(sk + p.l2_eps) : 1.0f;
+      for (int u = 0; u < TPW; ++u) {
+        const int tt = warp + NW * u;
+        const bool live = tt < n;
+        const size_t tokrow = (static_cast<size_t>(b) * T + t0 + tt) * p.H + h;
 #pragma unroll
-      for (int i = 0; i < NI; ++i) {
-        const int c = lane + 32 * i;
-        if (c < D) {
-          Qn[tt * D + c] = qv[i] * qsc;
-          Kn[tt * D + c] = kv[i] * kinv;
-          V[tt * D + c] = vv[i];
+        for (int i = 0; i < NI; ++i) {
+          const int c = lane + 32 * i;
+          qr[u][i] = kr[u][i] = vr[u][i] = 0u;
+          lv[u][i] = 0.0f;
+          if (live && c < D) {
+            const size_t at = tokrow * D + c;
+            if (bf16) {
+              qr[u][i] = __ldg(static_cast<const uint16_t*>(p.q) + at);
+              kr[u][i] = __ldg(static_cast<const uint16_t*>(p.k) + at);
+              vr[u][i] = __ldg(static_cast<const uint16_t*>(p.v) + at);
+            } else {
+              qr[u][i] = __float_as_uint(__ldg(static_cast<const float*>(p.q) + at));
+              kr[u][i] = __float_as_uint(__ldg(static_cast<const float*>(p.k) + at));
+              vr[u][i] = __float_as_uint(__ldg(static_cast<const float*>(p.v) + at));
+            }
+          }
+          if (live && c < dlam) lv[u][i] = __ldg(p.lam + tokrow * dlam + c);
         }
+        bv[u] = live ? (p.beta ? __ldg(p.beta + tokrow) : 1.0f) : 0.0f;
       }
-      for (int c = lane; c < dlam; c += 32) {
-        float lam = live ? __ldg(p.lam + tokrow * dlam + c) : 0.0f;
-        if (live && (fl & GDN_GATE_RAW)) lam = log_sigmoidf_(lam);
-        gam[tt * dlam + c] = lam;
-      }
-      if (lane == 0) {
-        float be = 0.0f;
-        if (live) {
-          be = p.beta ? __ldg(p.beta + tokrow) : 1.0f;
-          if (p.beta && (fl & GDN_GATE_RAW)) be = sigmoidf_(be);
+#pragma unroll
+      for (int u = 0; u < TPW; ++u)
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+          qv[u][i] = bf16 ? __uint_as_float(qr[u][i] << 16) : __uint_as_float(qr[u][i]);
+          kv[u][i] = bf16 ? __uint_as_float(kr[u][i] << 16) : __uint_as_float(kr[u][i]);
+          vv[u][i] = bf16 ? __uint_as_float(vr[u][i] << 16) : __uint_as_float(vr[u][i]);
         }
-        bet[tt] = be;
+#pragma unroll
+      for (int u = 0; u < TPW; ++u) {
+        const int tt = warp + NW * u;
+        const bool live = tt < n;
+        float sq = 0.0f, sk = 0.0f;
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+          sq = fmaf(qv[u][i], qv[u][i], sq);
+          sk = fmaf(kv[u][i], kv[u][i], sk);
+        }
+        sq = warp_sum(sq);
+        sk = warp_sum(sk);
+        const float qsc = (l2 ? 1.0f / sqrtf(sq + p.l2_eps) : 1.0f) * p.q_scale;
+        const float kinv = l2 ? 1.0f / sqrtf(sk + p.l2_eps) : 1.0f;
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+          const int c = lane + 32 * i;
+          if (c < D) {
+            Qn[tt * D + c] = qv[u][i] * qsc;
+            Kn[tt * D + c] = kv[u][i] * kinv;
+            V[tt * D + c] = vv[u][i];
+          }
+          if (c < dlam) {
+            float lam = lv[u][i];
+            if (live && (fl & GDN_GATE_RAW)) lam = log_sigmoidf_(lam);
+            gam[tt * dlam + c] = lam;
+          }
+        }
+        if (lane == 0) {
+          float be = bv[u];
+          if (live && p.beta && (fl & GDN_GATE_RAW)) be = sigmoidf_(be);
+          bet[tt] = be;
+        }
       }
     }
     __syncthreads();
@@ -260,22 +292,23 @@ __global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
     if (tid < D) {
       const int j = tid;
       float bc[PC];
+      // four partial sums per row shorten the dependent FMA chains
 #pragma unroll
       for (int t = 0; t < PC; ++t) {
-        float x = V[t * D + j];
+        float x[4] = {V[t * D + j], 0.0f, 0.0f, 0.0f};
         if (!plain) {
 #pragma unroll
-          for (int s = 0; s < t; ++s) x = fmaf(-A[t * PC + s], bc[s], x);
+          for (int s = 0; s < t; ++s) x[s & 3] = fmaf(-A[t * PC + s], bc[s], x[s & 3]);
         }
-        bc[t] = x;
+        bc[t] = (x[0] + x[1]) + (x[2] + x[3]);
       }
 #pragma unroll
       for (int t = 0; t < PC; ++t) {
         V[t * D + j] = bc[t];  // B for the state update
-        float y = Y[t * D + j];
+        float y[4] = {Y[t * D + j], 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int s = 0; s <= t; ++s) y = fmaf(P[t * PC + s], bc[s], y);
-        if (t < n) p.o[((static_cast<size_t>(b) * T + t0 + t) * p.H + h) * D + j] = y;
+        for (int s = 0; s <= t; ++s) y[s & 3] = fmaf(P[t * PC + s], bc[s], y[s & 3]);
+        if (t < n) p.o[((static_cast<size_t>(b) * T + t0 + t) * p.H + h) * D + j] = (y[0] + y[1]) + (y[2] + y[3]);
       }
     }
     // Khat = e^{gamma_C - gamma_s} k_s (rows past n hold zero keys)
