@@ -173,3 +173,51 @@ def test_prefill_status_and_skips():
     assert np.array_equal(pg[2], pool0[2]) and np.array_equal(pg[1], pool0[1]) and np.array_equal(pg[3], pool0[3])
     assert not np.array_equal(pg[0], pool0[0])
     assert torch.all(o[1] == 9.0) and torch.all(o[2] == 9.0)
+
+
+def test_back_to_back_launches_match_oracle():
+    """A prefill and 12 decode steps (dense and DeltaLog M=4) queued back to back with no
+    host synchronisation between them, each step writing its own output row: every launch
+    may start while the previous grid drains (programmatic launch), and the results must
+    still equal the oracle's sequential pass."""
+    w = wl.WORKLOADS["headline"]
+    B, H, D, T, M, steps = 16, 8, 128, 40, 4, 12
+    slot = np.arange(B, dtype=np.int32)
+    slot_dev = dev_i32(slot)
+    dev, ref = _inputs(B, T, H, D, 1, True, 31)
+    cfg = dict(batch=B, num_heads=H, dk=D, dv=D, num_slots=B, dlam=1, log_capacity=0,
+               flags=oracle.L2NORM, q_scale=1.0, l2_eps=1e-6)
+    pool_ref = np.zeros((B, H, D, D))
+    o_pf_ref = oracle.prefill_batch(cfg, pool_ref, slot, None, **ref)
+    st = oracle.BatchState(B, H, D, D)
+    st.S = pool_ref
+    xs = [wl.step_inputs(w, 700 + t, batch=B) for t in range(steps)]
+    ins = [dict(slot=slot_dev, log_decay=dev_f32(x["lam"]), beta=dev_f32(x["beta"]),
+                **{n: dev_bf16(x[n + "_bits"]) for n in ("q", "k", "v")}) for x in xs]
+    dims_d = gdn.make_dims(B, H, D, num_slots=B, flags=gdn.QKV_BF16)
+    dims_l = gdn.make_dims(B, H, D, num_slots=B, flags=gdn.QKV_BF16, log_capacity=M - 1)
+    pd, pl = gdn.Pools.allocate(dims_d), gdn.Pools.allocate(dims_l, deltalog=True)
+    o_pf = torch.zeros((2, B, T, H, D), device="cuda")
+    o_d = torch.zeros((steps, B, H, D), device="cuda")
+    o_l = torch.zeros((steps, B, H, D), device="cuda")
+    torch.cuda.synchronize()
+    inputs = [gdn.make_inputs(**d) for d in ins]
+    gdn.prefill(dims_d, T, gdn.make_inputs(slot=slot_dev, **dev), pd.state, o_pf[0])
+    gdn.prefill(dims_d, T, gdn.make_inputs(slot=slot_dev, **dev), pl.state, o_pf[1])
+    for t in range(steps):  # queued without synchronisation
+        gdn.decode_dense(dims_d, inputs[t], pd.state, o_d[t])
+        call = gdn.decode_merge if (t + 1) % M == 0 else gdn.decode_append
+        call(dims_l, inputs[t], pl.state, pl.log(), o_l[t])
+    torch.cuda.synchronize()
+    ref_o = [oracle.step_batch(cfg, "dense", st, slot, q=x["q"].astype(np.float64), k=x["k"].astype(np.float64),
+                               v=x["v"].astype(np.float64), lam=x["lam"].astype(np.float64),
+                               beta=x["beta"].astype(np.float64)) for x in xs]
+    ref_o = np.stack(ref_o)
+    scale = float(np.max(np.abs(ref_o)))
+    assert float(np.max(np.abs(o_d.cpu().numpy() - ref_o))) / scale <= TOL
+    assert float(np.max(np.abs(o_l.cpu().numpy() - ref_o))) / scale <= 5e-3
+    for i in range(2):
+        assert float(np.max(np.abs(o_pf[i].cpu().numpy() - o_pf_ref))) / float(np.max(np.abs(o_pf_ref))) <= TOL
+    S_ref = st.S
+    assert float(np.max(np.abs(pd.state.cpu().numpy() - S_ref))) / float(np.max(np.abs(S_ref))) <= TOL
+    assert float(np.max(np.abs(pl.state.cpu().numpy() - S_ref))) / float(np.max(np.abs(S_ref))) <= 5e-3
