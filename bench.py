@@ -195,7 +195,9 @@ def run_gpu(args, rank, local_rank, world):
     from linear_attention_decode_gdn_gb300 import build as gbuild
     from linear_attention_decode_gdn_gb300 import workloads as wl
 
-    gbuild.build()
+    if local_rank == 0:  # one build per node; the other ranks wait for it
+        gbuild.build()
+    barrier()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     w = wl.WORKLOADS[args.workload]
