@@ -190,6 +190,8 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
       for (int i = lane; i < uvec; i += 32) cp_async16(reinterpret_cast<uint4*>(u_s) + i, usrc + i);
       if (dlam == 1)
         for (int e = lane; e < nc; e += 32) cp_async4(lam_s + e, p.lam_log + sh * C + e);
+      else if (lane < nc)  // per-key snapshots stay in global memory: warm L2 for the replay
+        bulk_prefetch_l2(p.lam_log + (sh * C + lane) * dlam, static_cast<uint32_t>(dlam * 4));
       cp_async_arrive(&bars[NCHUNK]);
     }
     if (lane == 0) {
