@@ -309,6 +309,19 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
   // c^k_i = k.w_i, c^q_i = q.w_i (warp-shuffle sums); needs only q, k and the log
   auto replay_coefficients = [&]() {
     if (MODE == MODE_DENSE) return;
+    // per-key decay: the warp's first entry's snapshot row (warmed in L2) is loaded before
+    // the wait for the log copy, so the two latencies overlap
+    constexpr int NID = (D + 31) / 32;
+    float lpre[NID];
+#pragma unroll
+    for (int i = 0; i < NID; ++i) lpre[i] = 0.0f;
+    if (dlam > 1 && warp < n) {
+#pragma unroll
+      for (int i = 0; i < NID; ++i) {
+        const int d = lane + 32 * i;
+        if (d < D) lpre[i] = __ldg(p.lam_log + (sh * C + warp) * dlam + d);
+      }
+    }
     // wait for the log copy even when L = 0 (a merge copies all C entries), and pad
     // the merge tables only after it
     if (!mbar_wait(&bars[NCHUNK], 0u)) timeout = true;
@@ -335,7 +348,8 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
           const float kv = (klb == 2)
                                ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(uni)[e * D + d])
                                : reinterpret_cast<const float*>(uni)[e * D + d];
-          const float wd = (dlam == 1) ? kv : expf(ellp_s[d] - __ldg(lam_e + d)) * kv;
+          const float lam_d = (e == warp) ? lpre[i] : __ldg(lam_e + d);
+          const float wd = (dlam == 1) ? kv : expf(ellp_s[d] - lam_d) * kv;
           ck = fmaf(k_s[d], wd, ck);
           cq = fmaf(q_s[d], wd, cq);
           if (is_merge) kd_s[d * cp + e] = (dlam == 1) ? fscal * kv : wd;
