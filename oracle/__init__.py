@@ -12,7 +12,8 @@ Contents:
     :func:`build`, loaded with ctypes.
   * ``verify_batch`` -- speculative-decoding verify: T positions per request
     through the dense step, one pool row per position (composition of the
-    pinned dense step with the row routing of the inference handbook).
+    pinned dense step with the row routing of the inference handbook); with
+    a fused conv, the widened conv window (``orc_verify_conv_window``).
   * ``prefill_batch`` -- the prompt of every request through the dense step,
     token by token, masked past each prompt length.
   * ``chunked.py``   -- numpy fp64 chunkwise forms (gated linear attention
@@ -118,6 +119,8 @@ def _declare(lib):
     lib.orc_kda_log_decay.restype = ctypes.c_double
     lib.orc_out_norm_gate.argtypes = [ctypes.c_int, dp, dp, dp, ctypes.c_double, dp]
     lib.orc_out_norm_gate.restype = None
+    lib.orc_verify_conv_window.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, dp, dp, dp, dp, dp]
+    lib.orc_verify_conv_window.restype = ctypes.c_int
     return lib
 
 
@@ -283,8 +286,24 @@ def step_batch(cfg: dict, mode: str, st: BatchState, slot, *, q=None, k=None, v=
     return o
 
 
-def verify_batch(cfg: dict, pool, state_indices, num_accepted, *, q, k, v, lam, beta, lib=None,
-                 out_gate=None, **kda):
+def verify_conv_window(win, num_accepted, x, w, bias=None, lib=None):
+    """One request's widened conv window through a verify round (inference handbook,
+    "推测解码：验证后如何恢复状态"): ``win`` [nch, T+2] (the last T+2 pre-conv inputs,
+    column 0 oldest) is read at offset num_accepted - 1 and updated in place; ``x``
+    [T, nch] are the round's pre-conv inputs. Returns the SiLU(conv) outputs [T, nch]."""
+    lib = lib or load()
+    win, x, w, bias = map(_f64, (win, x, w, bias))
+    T, nch = x.shape
+    assert win.shape == (nch, T + 2)
+    y = np.empty_like(x)
+    rc = lib.orc_verify_conv_window(nch, T, int(num_accepted), _ptr(win), _ptr(x), _ptr(w), _ptr(bias), _ptr(y))
+    if rc != 0:
+        raise ValueError(f"oracle verify_conv_window: {ERRORS.get(rc, rc)}")
+    return y
+
+
+def verify_batch(cfg: dict, pool, state_indices, num_accepted, *, q=None, k=None, v=None, lam, beta,
+                 lib=None, out_gate=None, mixed=None, conv_w=None, conv_b=None, conv_window=None, **kda):
     """Speculative-decoding verify, written from the inference handbook's passage
     "推测解码：验证后如何恢复状态": a request feeds T positions (the last sampled token,
     then the drafts) through the recurrence; the initial state is the pool row of column
@@ -297,12 +316,23 @@ def verify_batch(cfg: dict, pool, state_indices, num_accepted, *, q, k, v, lam, 
     (flags L2NORM / PLAIN / GATE_RAW, q_scale, l2_eps). Each position is one dense step of
     :func:`step_batch`; the KDA gate / epilogue inputs (``out_gate`` [B,T,H,dv], and
     ``a_log``, ``dt_bias``, ``out_norm_w``, ``lower_bound``) pass through to it.
+    With ``mixed`` [B, T, nch] (channels [q heads | k heads | v heads]), q, k and v are the
+    outputs of :func:`verify_conv_window` on the request's window ``conv_window[row]``
+    ([num_slots, nch, T+2], updated in place), row = the request's column-0 index.
     Returns o [B, T, H, dv]."""
     idx = np.asarray(state_indices, dtype=np.int64)
     na = np.asarray(num_accepted, dtype=np.int64)
     B, T = idx.shape
     H, dk, dv, dlam = cfg["num_heads"], cfg["dk"], cfg["dv"], cfg.get("dlam", 1)
     live = [b for b in range(B) if idx[b, 0] >= 0]
+    if mixed is not None:
+        q, k, v = np.zeros((B, T, H, dk)), np.zeros((B, T, H, dk)), np.zeros((B, T, H, dv))
+        for b in live:
+            y = verify_conv_window(conv_window[idx[b, 0]], na[b], np.ascontiguousarray(mixed[b]),
+                                   conv_w, conv_b, lib=lib)
+            q[b] = y[:, : H * dk].reshape(T, H, dk)
+            k[b] = y[:, H * dk: 2 * H * dk].reshape(T, H, dk)
+            v[b] = y[:, 2 * H * dk:].reshape(T, H, dv)
     run = BatchState(B, H, dk, dv, dlam)
     for b in live:
         run.S[b] = pool[idx[b, na[b] - 1]]

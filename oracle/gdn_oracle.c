@@ -142,6 +142,52 @@ void orc_conv1d_silu(int nch, const double *x, double *cs, const double *w,
   }
 }
 
+/* ---------------------------------------------------------------------------
+ * Widened conv window of a speculative-decoding verify round, one request
+ * ([HB] "推测解码：验证后如何恢复状态": the conv cache is widened to
+ * conv_kernel - 1 + num_spec inputs, the round's candidates are appended at its
+ * end, and the next round reads it at offset num_accepted - 1).
+ * With T = 1 + num_spec positions the window holds W = (CONV_K - 1) + (T - 1)
+ * PRE-conv inputs per channel, column 0 oldest. A round that enters with
+ * na = num_accepted (1 <= na <= T) takes the CONV_K - 1 inputs before its first
+ * position from columns na-1 .. na+1, convolves its T inputs with them
+ * (orc_conv1d_silu, one token at a time), and leaves in the window the last W
+ * inputs of that sequence: columns na and na+1, then its own T inputs.
+ *   win  [nch][W]  updated in place
+ *   x    [T][nch]  pre-conv inputs of the round
+ *   w    [nch][4], bias [nch] or NULL
+ *   y    [T][nch]  SiLU(conv) outputs
+ * Returns ORC_OK, or ORC_ERR_ARG when na is outside [1, T].
+ * ------------------------------------------------------------------------- */
+int orc_verify_conv_window(int nch, int T, int na, double *win, const double *x,
+                           const double *w, const double *bias, double *y) {
+  if (T < 1 || na < 1 || na > T) return ORC_ERR_ARG;
+  const int W = (CONV_K - 1) + (T - 1);
+  const int off = na - 1;
+  double *cs = (double *)malloc(sizeof(double) * (size_t)nch * 3);
+  double *seq = (double *)malloc(sizeof(double) * (size_t)nch * (size_t)(T + CONV_K - 1));
+  if (!cs || !seq) {
+    free(cs);
+    free(seq);
+    return ORC_ERR_ARG;
+  }
+  /* the inputs the round sees, oldest first: the three before it, then its own */
+  for (int c = 0; c < nch; ++c) {
+    for (int j = 0; j < CONV_K - 1; ++j) {
+      cs[c * 3 + j] = win[(size_t)c * W + off + j];
+      seq[(size_t)c * (T + CONV_K - 1) + j] = win[(size_t)c * W + off + j];
+    }
+    for (int t = 0; t < T; ++t) seq[(size_t)c * (T + CONV_K - 1) + CONV_K - 1 + t] = x[(size_t)t * nch + c];
+  }
+  for (int t = 0; t < T; ++t) orc_conv1d_silu(nch, x + (size_t)t * nch, cs, w, bias, y + (size_t)t * nch);
+  /* keep the last W of the T + 3 inputs */
+  for (int c = 0; c < nch; ++c)
+    for (int i = 0; i < W; ++i) win[(size_t)c * W + i] = seq[(size_t)c * (T + CONV_K - 1) + (T + CONV_K - 1 - W) + i];
+  free(cs);
+  free(seq);
+  return ORC_OK;
+}
+
 /* L2 normalisation ([EVO] appendix 附2): y = scale * x / sqrt(sum x^2 + eps).
  * Returns 1/sqrt(sum x^2 + eps), the factor that maps x to its unit vector. */
 double orc_l2norm(int n, const double *x, double eps, double scale, double *y) {

@@ -455,11 +455,79 @@ def pin_prefill_batch(lib, seed=15):
             assert np.array_equal(pool[row], init[row])
 
 
+def _silu(z):
+    return z / (1 + np.exp(-z))
+
+
+def pin_verify_conv_window(lib, nch=5, T=4, rounds=7, seed=16):
+    """Widened conv window of speculative-decoding verify (inference handbook, "推测解码：验证后
+    如何恢复状态") against brute force over the accepted history: every round's conv outputs
+    are SiLU(w . the last four inputs) of (accepted history, the round's inputs up to t), and
+    the window afterwards holds the last T+2 of (history, round). Rounds accept 1..T positions
+    (all T once); the first round enters a plain three-column cache with num_accepted = 1."""
+    r = _rng(seed)
+    w, bias = r.standard_normal((nch, 4)), r.standard_normal(nch)
+    hist = [r.standard_normal(nch) for _ in range(3)]
+    win = np.zeros((nch, T + 2))
+    win[:, :3] = np.stack(hist, axis=1)
+    na = 1
+    for rd in range(rounds):
+        x = r.standard_normal((T, nch))
+        y = oracle.verify_conv_window(win, na, x.copy(), w, bias, lib=lib)
+        for t in range(T):
+            taps = (hist[-3:] + [x[u] for u in range(t + 1)])[-4:]
+            z = sum(taps[j] * w[:, j] for j in range(4)) + bias
+            assert np.allclose(y[t], _silu(z), atol=1e-14, rtol=0), (rd, t)
+        assert np.array_equal(win, np.stack(hist[-2:] + [x[u] for u in range(T)], axis=1)), rd
+        na = T if rd == 2 else int(r.integers(1, T + 1))
+        hist += [x[u] for u in range(na)]
+    for bad in (0, T + 1):
+        try:
+            oracle.verify_conv_window(win, bad, np.zeros((T, nch)), w, lib=lib)
+        except ValueError:
+            continue
+        raise AssertionError(f"num_accepted {bad} accepted")
+
+
+def pin_verify_conv_glue(lib, seed=17):
+    """verify_batch with mixed_qkv == verify_batch on the q, k, v that brute-force conv outputs
+    give, split [q heads | k heads | v heads]; the window row is the request's column-0 index,
+    a padding request's window is untouched."""
+    r = _rng(seed)
+    B, T, H, d, S = 3, 3, 2, 4, 9
+    nch = 3 * H * d
+    idx = np.array([[4, 0, 7], [-1, -1, -1], [2, 8, 5]], dtype=np.int32)
+    na = np.array([2, 1, 3], dtype=np.int32)
+    pool = r.standard_normal((S, H, d, d)) * 0.3
+    win = r.standard_normal((S, nch, T + 2))
+    win0, pool0 = win.copy(), pool.copy()
+    mixed = r.standard_normal((B, T, nch))
+    w = r.standard_normal((nch, 4))
+    lam = np.log(1 / (1 + np.exp(-(r.standard_normal((B, T, H, 1)) + 3))))
+    beta = 1 / (1 + np.exp(-r.standard_normal((B, T, H))))
+    cfg = _batch_cfg(B, H, d, d, S, 1, 0, oracle.L2NORM, q_scale=0.5)
+    o = oracle.verify_batch(cfg, pool, idx, na, lam=lam, beta=beta, lib=lib, mixed=mixed, conv_w=w,
+                            conv_window=win)
+    qkv = np.zeros((B, T, nch))
+    for b in (0, 2):
+        seq = list(win0[idx[b, 0]][:, na[b] - 1: na[b] + 2].T) + list(mixed[b])
+        for t in range(T):
+            qkv[b, t] = _silu(sum(seq[t + j] * w[:, j] for j in range(4)))
+    q = qkv[..., : H * d].reshape(B, T, H, d)
+    k = qkv[..., H * d: 2 * H * d].reshape(B, T, H, d)
+    v = qkv[..., 2 * H * d:].reshape(B, T, H, d)
+    o_ref = oracle.verify_batch(cfg, pool0, idx, na, q=q, k=k, v=v, lam=lam, beta=beta, lib=lib)
+    assert np.max(np.abs(o - o_ref)) <= 1e-12 and np.max(np.abs(pool - pool0)) <= 1e-12
+    for row in range(S):
+        if row not in (4, 2):
+            assert np.array_equal(win[row], win0[row])
+
+
 PINS = [pin_teaching_dense, pin_teaching_deltalog, pin_gla_chunked, pin_delta_wy,
         lambda lib: pin_delta_wy(lib, per_key=True), lambda lib: pin_delta_wy(lib, T=50, dk=8, dv=12, C=16),
         pin_transition_form, pin_invariants, pin_conv, pin_l2norm, pin_deltalog_equals_dense,
         pin_batch_glue, pin_prenorm_log, pin_verify_routing, pin_kda_gate, pin_out_norm_gate,
-        pin_kda_batch_glue, pin_prefill_batch]
+        pin_kda_batch_glue, pin_prefill_batch, pin_verify_conv_window, pin_verify_conv_glue]
 
 
 # ----------------------------------------------------------------------------
@@ -538,6 +606,15 @@ def test_verify_routing(oracle_lib):
 
 def test_prefill_batch(oracle_lib):
     pin_prefill_batch(oracle_lib)
+
+
+def test_verify_conv_window(oracle_lib):
+    pin_verify_conv_window(oracle_lib)
+    pin_verify_conv_window(oracle_lib, T=1, seed=18)
+
+
+def test_verify_conv_glue(oracle_lib):
+    pin_verify_conv_glue(oracle_lib)
 
 
 def test_kda_gate(oracle_lib):
@@ -624,6 +701,15 @@ MUTANTS = [
     ("output gate sign flipped",
      "y[j] = o[j] * inv * (w ? w[j] : 1.0) * orc_sigmoid(g[j]);",
      "y[j] = o[j] * inv * (w ? w[j] : 1.0) * orc_sigmoid(-g[j]);"),
+    ("verify conv window read from column 0",
+     "const int off = na - 1;",
+     "const int off = 0;"),
+    ("verify conv window keeps the oldest inputs",
+     "+ (T + CONV_K - 1 - W) + i];",
+     "+ i];"),
+    ("verify conv window not rewritten",
+     "for (int i = 0; i < W; ++i) win[",
+     "for (int i = 0; i < W && 0; ++i) win["),
     ("epilogue not applied in the batch step",
      "      if (fl & ORC_OUT_NORM_GATE)\n        orc_out_norm_gate(",
      "      if (0)\n        orc_out_norm_gate("),
