@@ -242,11 +242,22 @@ int gdn_decode_step(const gdn_dims *dims, const gdn_inputs *in, float *base_pool
  *   in->q, in->k, in->v [B][T][H][d] (bf16 or fp32), in->log_decay [B][T][H][dlam],
  *   in->beta [B][T][H] (or NULL: beta = 1); in->slot is not used.
  *   o [B][T][H][dv] fp32: the readout of every position.
+ * With GDN_FUSE_CONV, q, k and v come from the width-4 conv + SiLU of
+ * in->mixed_qkv [B][T][channels] (channel order and conv_w / conv_b as for the decode
+ * calls) through the widened conv window of the same passage:
+ *   in->conv_pool [num_slots][channels][T + 2] (bf16 with GDN_QKV_BF16, else fp32):
+ *       per channel the last T + 2 pre-conv inputs, column 0 oldest; the request's
+ *       window is row state_indices[b][0]. The three inputs before position 0 are read
+ *       from columns num_accepted[b] - 1 .. num_accepted[b] + 1, and the row is rewritten
+ *       with columns num_accepted[b] and num_accepted[b] + 1 followed by the T inputs of
+ *       this call (bit-exact copies). A plain three-column conv state enters as columns
+ *       0..2 with num_accepted = 1. Consecutive verify calls on one window pool use the
+ *       same num_tokens.
  * A request with state_indices[b][0] < 0 is padding and is skipped. A row outside
  * [0, num_slots) skips the request with GDN_STATUS_BAD_SLOT; num_accepted outside
- * [1, T] skips it with GDN_STATUS_BAD_LEN. Requires 1 <= num_tokens <= 16; the
- * verify path is the dense recurrence, so GDN_FUSE_CONV and the DeltaLog flags are
- * rejected with GDN_ERR_UNSUPPORTED.
+ * [1, T] skips it with GDN_STATUS_BAD_LEN; a skipped request's rows, window and
+ * outputs are untouched. Requires 1 <= num_tokens <= 16; the verify path is the
+ * dense recurrence, so the DeltaLog flags are rejected with GDN_ERR_UNSUPPORTED.
  */
 int gdn_decode_verify(const gdn_dims *dims, int32_t num_tokens, const gdn_inputs *in,
                       const int32_t *state_indices, const int32_t *num_accepted,

@@ -235,16 +235,25 @@ int gdn_decode_verify(const gdn_dims* dims, int32_t num_tokens, const gdn_inputs
   if (rc != GDN_OK) return rc;
   if (num_tokens < 1 || num_tokens > kMaxVerifyTokens)
     return fail(GDN_ERR_UNSUPPORTED, "num_tokens %d outside [1, %d]", num_tokens, kMaxVerifyTokens);
-  if (dims->flags & (GDN_FUSE_CONV | GDN_KLOG_FP32 | GDN_KLOG_PRENORM | GDN_ULOG_BF16 | GDN_TEST_STARVE_WAIT))
-    return fail(GDN_ERR_UNSUPPORTED, "verify runs the dense recurrence: no fused conv, no log flags");
+  if (dims->flags & (GDN_KLOG_FP32 | GDN_KLOG_PRENORM | GDN_ULOG_BF16 | GDN_TEST_STARVE_WAIT))
+    return fail(GDN_ERR_UNSUPPORTED, "verify runs the dense recurrence: no log flags");
   if (static_cast<long long>(dims->batch) * num_tokens * dims->num_heads > 0x7fffffffLL)
     return fail(GDN_ERR_INVALID_ARG, "batch * num_tokens * num_heads too large");
   if (dims->batch == 0) return GDN_OK;
-  if (in == nullptr || in->log_decay == nullptr || in->q == nullptr || in->k == nullptr || in->v == nullptr)
-    return fail(GDN_ERR_INVALID_ARG, "q, k, v and log_decay are required");
+  if (in == nullptr || in->log_decay == nullptr)
+    return fail(GDN_ERR_INVALID_ARG, "inputs and log_decay are required");
   if ((rc = check_gate_inputs(dims, in)) != GDN_OK) return rc;
-  if (!aligned16(in->q) || !aligned16(in->k) || !aligned16(in->v))
-    return fail(GDN_ERR_UNSUPPORTED, "q, k and v must be 16-byte aligned");
+  if (dims->flags & GDN_FUSE_CONV) {
+    if (in->mixed_qkv == nullptr || in->conv_w == nullptr || in->conv_pool == nullptr)
+      return fail(GDN_ERR_INVALID_ARG, "GDN_FUSE_CONV needs mixed_qkv, conv_w and conv_pool");
+    if (!aligned16(in->mixed_qkv) || !aligned16(in->conv_w))
+      return fail(GDN_ERR_UNSUPPORTED, "mixed_qkv and conv_w must be 16-byte aligned");
+  } else {
+    if (in->q == nullptr || in->k == nullptr || in->v == nullptr)
+      return fail(GDN_ERR_INVALID_ARG, "q, k and v are required");
+    if (!aligned16(in->q) || !aligned16(in->k) || !aligned16(in->v))
+      return fail(GDN_ERR_UNSUPPORTED, "q, k and v must be 16-byte aligned");
+  }
   if (state_indices == nullptr || num_accepted == nullptr || state_pool == nullptr || o == nullptr)
     return fail(GDN_ERR_INVALID_ARG, "state_indices, num_accepted, state_pool and o are required");
   if (!aligned16(state_pool) || !aligned16(o))

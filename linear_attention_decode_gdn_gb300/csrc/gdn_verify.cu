@@ -19,6 +19,38 @@ constexpr int kMaxVerifyTokens = 16;
 
 namespace {
 
+// Widened conv window of one channel (inference handbook, "推测解码：验证后如何恢复状态":
+// the conv cache of a verify path holds conv_kernel - 1 + num_spec pre-conv inputs, the
+// round's inputs are appended at its end, and the next round starts reading at offset
+// num_accepted - 1).  With T positions the window row has T + 2 elements (dtype of the
+// inputs), column 0 oldest.  s[0..2] are the three inputs before the current position.
+__device__ __forceinline__ float conv_window_load(const void* pool, size_t i, bool bf16) {
+  return bf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(pool)[i]) : static_cast<const float*>(pool)[i];
+}
+
+__device__ __forceinline__ void conv_window_store(void* pool, size_t i, float x, bool bf16) {
+  // values that came in as bf16 convert back exactly
+  if (bf16)
+    static_cast<uint16_t*>(pool)[i] = static_cast<uint16_t>(__float_as_uint(x) >> 16);
+  else
+    static_cast<float*>(pool)[i] = x;
+}
+
+// SiLU(s0 w0 + s1 w1 + s2 w2 + x w3 (+ bias)) of channel c, then the window slides by x
+// (same product order as the one-step conv of the decode kernels)
+__device__ __forceinline__ float conv_window_step(const DecodeParams& p, int c, float (&s)[3], float x) {
+  const float4 w = __ldg(reinterpret_cast<const float4*>(p.conv_w) + c);
+  float acc = s[0] * w.x;
+  acc = fmaf(s[1], w.y, acc);
+  acc = fmaf(s[2], w.z, acc);
+  acc = fmaf(x, w.w, acc);
+  if (p.conv_b != nullptr) acc += __ldg(p.conv_b + c);
+  s[0] = s[1];
+  s[1] = s[2];
+  s[2] = x;
+  return siluf_(acc);
+}
+
 // Shared-memory layout (bytes): tile | mbarriers | scalars | two vector sets | partial sums.
 struct VerifyLayout {
   uint32_t tile, bars, scal, vec, red, total;
@@ -119,6 +151,34 @@ __global__ void __launch_bounds__(NT_DECODE) gdn_verify_kernel(const DecodeParam
   float4* tile4 = reinterpret_cast<float4*>(tile);
   bool timeout = false;
 
+  // fused conv: thread i of the q range owns the q and v channels of key index i, thread i
+  // of the k range the k channel; the window row is the request's column-0 row, read here
+  // only when that row and the acceptance count are valid (the copy-issuing warp skips the
+  // request otherwise, before anything is written)
+  const bool conv = (fl & GDN_FUSE_CONV) != 0u;
+  const bool cbf16 = (fl & GDN_QKV_BF16) != 0u;
+  const int HD = p.H * D;
+  const int cx = is_q ? h * D + ii : HD + h * D + ii;
+  const int cv = 2 * HD + h * D + ii;
+  const int CW = T + 2;
+  size_t wx = 0, wv = 0;
+  float sx[3] = {0.0f, 0.0f, 0.0f}, sv[3] = {0.0f, 0.0f, 0.0f};
+  if (conv && !ctrl && (is_q || is_k)) {
+    const int r0 = __ldg(p.state_indices + static_cast<size_t>(b) * T);
+    const int na = __ldg(p.num_accepted + b);
+    if (r0 >= 0 && r0 < p.num_slots && na >= 1 && na <= T) {
+      wx = (static_cast<size_t>(r0) * p.channels + cx) * CW + (na - 1);
+      wv = (static_cast<size_t>(r0) * p.channels + cv) * CW + (na - 1);
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        sx[j] = conv_window_load(p.conv_pool, wx + j, cbf16);
+        if (is_q) sv[j] = conv_window_load(p.conv_pool, wv + j, cbf16);
+      }
+      wx -= (na - 1);  // row starts, for the rewrite
+      wv -= (na - 1);
+    }
+  }
+
   for (int t = 0; t < T; ++t) {
     const int bt = b * T + t;  // inputs and outputs are [B][T][H][...]: position t of request b
     float* vec = reinterpret_cast<float*>(smem + L.vec) + (t & 1) * 5 * D;
@@ -142,7 +202,15 @@ __global__ void __launch_bounds__(NT_DECODE) gdn_verify_kernel(const DecodeParam
       }
       if ((fl & GDN_OUT_NORM_GATE) && is_q) og = __ldg(p.out_gate + (static_cast<size_t>(bt) * p.H + h) * D + ii);
       if (p.beta) beta = __ldg(p.beta + static_cast<size_t>(bt) * p.H + h);
-      load_token(p, bt, h, 0, tid, &x, &vj);
+      if (conv) {
+        if (is_q || is_k) {
+          const size_t xr = static_cast<size_t>(bt) * p.channels;
+          x = conv_window_step(p, cx, sx, load_elem(p.mixed, xr + cx, cbf16));
+          if (is_q) vj = conv_window_step(p, cv, sv, load_elem(p.mixed, xr + cv, cbf16));
+        }
+      } else {
+        load_token(p, bt, h, 0, tid, &x, &vj);
+      }
       if (fl & GDN_GATE_RAW) {
         lam = log_sigmoidf_(lam);
         if (p.beta) beta = sigmoidf_(beta);
@@ -167,6 +235,19 @@ __global__ void __launch_bounds__(NT_DECODE) gdn_verify_kernel(const DecodeParam
       if (ctrl || flags_s[0]) return;
     } else {
       consumer_sync();  // (A) the previous position's tile update is complete
+    }
+    if (conv && (is_q || is_k)) {
+      // the window keeps the last T + 2 inputs: the two after the offset, then the round's
+      if (t == 0) {
+        conv_window_store(p.conv_pool, wx, sx[0], cbf16);
+        conv_window_store(p.conv_pool, wx + 1, sx[1], cbf16);
+        if (is_q) {
+          conv_window_store(p.conv_pool, wv, sv[0], cbf16);
+          conv_window_store(p.conv_pool, wv + 1, sv[1], cbf16);
+        }
+      }
+      conv_window_store(p.conv_pool, wx + 2 + t, sx[2], cbf16);
+      if (is_q) conv_window_store(p.conv_pool, wv + 2 + t, sv[2], cbf16);
     }
 
     const float qss = scal_f[0] + scal_f[1] + scal_f[2] + scal_f[3];

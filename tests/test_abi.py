@@ -154,10 +154,17 @@ def test_verify_validation_rejects_before_launch(gdn):
     for T in (0, 17):
         _expect(gdn, lambda: gdn.decode_verify(d, T, ins, fake, fake, fake, fake, stream=0),
                 _abi.GDN_ERR_UNSUPPORTED)
-    for flag in (gdn.FUSE_CONV, gdn.KLOG_FP32, gdn.ULOG_BF16):
+    for flag in (gdn.KLOG_FP32, gdn.ULOG_BF16, gdn.KLOG_PRENORM):
         dd = gdn.make_dims(2, 2, 64, num_slots=8, flags=flag)
         _expect(gdn, lambda: gdn.decode_verify(dd, 4, ins, fake, fake, fake, fake, stream=0),
                 _abi.GDN_ERR_UNSUPPORTED)
+    # the fused conv needs mixed_qkv, conv_w and the window pool, 16-byte aligned
+    dc = gdn.make_dims(2, 2, 64, num_slots=8, flags=gdn.FUSE_CONV | gdn.QKV_BF16)
+    _expect(gdn, lambda: gdn.decode_verify(dc, 4, ins, fake, fake, fake, fake, stream=0),
+            _abi.GDN_ERR_INVALID_ARG)
+    cins = gdn.make_inputs(mixed_qkv=fake + 2, conv_w=fake, conv_pool=fake, log_decay=fake)
+    _expect(gdn, lambda: gdn.decode_verify(dc, 4, cins, fake, fake, fake, fake, stream=0),
+            _abi.GDN_ERR_UNSUPPORTED)
     _expect(gdn, lambda: gdn.decode_verify(d, 4, ins, None, fake, fake, fake, stream=0), _abi.GDN_ERR_INVALID_ARG)
     _expect(gdn, lambda: gdn.decode_verify(d, 4, gdn.make_inputs(q=fake, k=fake, v=fake), fake, fake, fake,
                                            fake, stream=0), _abi.GDN_ERR_INVALID_ARG)

@@ -227,3 +227,77 @@ def test_verify_status_and_skips():
                 assert np.array_equal(pg[row], pool0[row])
     for b in (0, 3):
         assert not torch.all(o[b] == 3.0)
+
+
+def _run_conv(D, T, bf16=True, bias=True, B=5, H=2, rounds=3, seed=40, pad=(2,)):
+    """Verify with the fused conv through the widened conv window: ``rounds`` calls in a row,
+    each entering with the previous round's acceptance counts (column 0 of every request
+    keeps its window row). Returns the output / state relative errors and whether every
+    window matches the oracle's bit for bit."""
+    r = np.random.default_rng(seed)
+    nch = 3 * H * D
+    S = B * T + 3
+    pool0 = (r.standard_normal((S, H, D, D)) * 0.1).astype(np.float32)
+    win0 = r.standard_normal((S, nch, T + 2)).astype(np.float32)
+    w = (r.standard_normal((nch, 4)) * 0.5).astype(np.float32)
+    cb = (r.standard_normal(nch) * 0.1).astype(np.float32) if bias else None
+    if bf16:
+        win_bits, win0 = wl.bf16_round(win0)
+        win_dev = dev_bf16(win_bits)
+    else:
+        win_dev = dev_f32(win0)
+    pool_dev, pool_ref, win_ref = dev_f32(pool0), pool0.astype(np.float64), win0.astype(np.float64)
+    flags = (gdn.QKV_BF16 if bf16 else 0) | gdn.FUSE_CONV
+    dims = gdn.make_dims(B, H, D, num_slots=S, flags=flags, q_scale=D ** -0.5)
+    cfg = dict(batch=B, num_heads=H, dk=D, dv=D, num_slots=S, dlam=1, log_capacity=0,
+               flags=oracle.L2NORM, q_scale=D ** -0.5, l2_eps=1e-6)
+    idx = _rows(B, T, S, seed, pad)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    err = ref = 0.0
+    na = np.ones(B, dtype=np.int32)
+    for rd in range(rounds):
+        mixed = r.standard_normal((B, T, nch)).astype(np.float32)
+        if bf16:
+            mbits, mixed = wl.bf16_round(mixed)
+            mixed_dev = dev_bf16(mbits.reshape(mixed.shape))
+        else:
+            mixed_dev = dev_f32(mixed)
+        a_raw = r.standard_normal((B, T, H, 1)).astype(np.float32) + np.float32(3)
+        lam = (-np.log1p(np.exp(-a_raw.astype(np.float64)))).astype(np.float32)
+        beta = (1 / (1 + np.exp(-r.standard_normal((B, T, H)).astype(np.float64)))).astype(np.float32)
+        o = torch.full((B, T, H, D), 7.0, dtype=torch.float32, device="cuda")
+        keep = dict(mixed_qkv=mixed_dev, conv_w=dev_f32(w), conv_b=None if cb is None else dev_f32(cb),
+                    conv_pool=win_dev, log_decay=dev_f32(lam), beta=dev_f32(beta))
+        gdn.decode_verify(dims, T, gdn.make_inputs(**keep), dev_i32(idx), dev_i32(na), pool_dev, o, status)
+        f = lambda a: np.ascontiguousarray(a, dtype=np.float64)  # noqa: E731
+        o_ref = oracle.verify_batch(cfg, pool_ref, idx, na, lam=f(lam), beta=f(beta), mixed=f(mixed),
+                                    conv_w=f(w), conv_b=None if cb is None else f(cb), conv_window=win_ref)
+        torch.cuda.synchronize()
+        live = idx[:, 0] >= 0
+        og = o.cpu().numpy().astype(np.float64)
+        err = max(err, float(np.max(np.abs(og[live] - o_ref[live]))))
+        ref = max(ref, float(np.max(np.abs(o_ref[live]))))
+        assert np.all(og[~live] == 7.0)
+        na = r.integers(1, T + 1, size=B).astype(np.int32)
+    assert int(status.item()) == 0
+    if bf16:
+        wg = (win_dev.cpu().view(torch.int16).numpy().astype(np.uint16).astype(np.uint32) << 16).view(np.float32)
+    else:
+        wg = win_dev.cpu().numpy()
+    win_ok = np.array_equal(wg.astype(np.float64), win_ref)
+    pg = pool_dev.cpu().numpy().astype(np.float64)
+    serr = float(np.max(np.abs(pg - pool_ref))) / float(np.max(np.abs(pool_ref)))
+    return err / ref, serr, win_ok
+
+
+@pytest.mark.parametrize("D,T", [(128, 4), (64, 3), (16, 1), (32, 16)])
+def test_verify_conv_window(D, T):
+    """Fused conv through the widened window (inference handbook, speculative-decoding
+    state recovery): outputs and states at the dense bar, windows bit-exact."""
+    e_o, e_s, win_ok = _run_conv(D, T, seed=40 + D + T)
+    assert e_o <= TOL and e_s <= TOL and win_ok, (e_o, e_s, win_ok)
+
+
+def test_verify_conv_window_fp32_no_bias():
+    e_o, e_s, win_ok = _run_conv(128, 4, bf16=False, bias=False, seed=77)
+    assert e_o <= TOL and e_s <= TOL and win_ok, (e_o, e_s, win_ok)
