@@ -348,23 +348,33 @@ def verify_batch(cfg: dict, pool, state_indices, num_accepted, *, q=None, k=None
     return o
 
 
-def prefill_batch(cfg: dict, pool, slot, seq_lens, *, q, k, v, lam, beta, lib=None):
+def prefill_batch(cfg: dict, pool, slot, seq_lens, *, q=None, k=None, v=None, lam, beta, lib=None,
+                  mixed=None, conv_w=None, conv_b=None, conv_pool=None):
     """The prompt through the recurrence, token by token: position t of request b is one dense
     step of :func:`step_batch` on its pool row when t < seq_lens[b] (a prefill seeds the state
     a decode continues from; evolution article, "Prefill中的Chunk微观并行", states the same
     result for the chunked form). ``pool`` [num_slots, H, dk, dv] float64 is updated in place;
-    q, k [B,T,H,dk], v [B,T,H,dv], lam [B,T,H,dlam], beta [B,T,H]. Returns o [B,T,H,dv]
-    (zero past each prompt)."""
+    q, k [B,T,H,dk], v [B,T,H,dv], lam [B,T,H,dlam], beta [B,T,H]. With ``mixed`` [B,T,nch]
+    the step runs the causal conv + SiLU on it instead (flag CONV), through the slot's conv
+    state ``conv_pool`` [num_slots, nch, 3] (updated in place: afterwards it holds the last
+    three inputs of the prompt). Returns o [B,T,H,dv] (zero past each prompt)."""
     slot = np.asarray(slot, dtype=np.int32)
-    B, T = q.shape[0], q.shape[1]
+    src = q if mixed is None else mixed
+    B, T = src.shape[0], src.shape[1]
     H, dk, dv, dlam = cfg["num_heads"], cfg["dk"], cfg["dv"], cfg.get("dlam", 1)
     lens = np.full(B, T) if seq_lens is None else np.asarray(seq_lens)
     st = BatchState(cfg["num_slots"], H, dk, dv, dlam)
     st.S = pool  # the step updates the caller's pool in place
     c = dict(cfg, batch=B, log_capacity=0)
+    if mixed is not None:
+        st.conv = conv_pool
+        c["flags"] = c.get("flags", 0) | CONV
     o = np.zeros((B, T, H, dv))
     for t in range(T):
         live = np.where((lens > t) & (slot >= 0), slot, -1).astype(np.int32)
-        o[:, t] = step_batch(c, "dense", st, live, q=q[:, t], k=k[:, t], v=v[:, t],
-                             lam=lam[:, t], beta=beta[:, t], lib=lib)
+        if mixed is None:
+            tok = dict(q=q[:, t], k=k[:, t], v=v[:, t])
+        else:
+            tok = dict(mixed=mixed[:, t], conv_w=conv_w, conv_b=conv_b)
+        o[:, t] = step_batch(c, "dense", st, live, lam=lam[:, t], beta=beta[:, t], lib=lib, **tok)
     return o

@@ -523,11 +523,49 @@ def pin_verify_conv_glue(lib, seed=17):
             assert np.array_equal(win[row], win0[row])
 
 
+def pin_prefill_conv_glue(lib, seed=19):
+    """prefill_batch with mixed_qkv == prefill_batch on the q, k, v that brute-force conv
+    outputs give (history: the slot's three-column conv state, then the prompt), masked past
+    each prompt length; afterwards each slot's conv state holds the last three inputs of
+    (old state, prompt) and a padding request's state is untouched."""
+    r = _rng(seed)
+    B, T, H, d, S = 4, 7, 2, 4, 6
+    nch = 3 * H * d
+    slot = np.array([3, -1, 0, 5], dtype=np.int32)
+    lens = np.array([7, 7, 2, 0])
+    pool = r.standard_normal((S, H, d, d)) * 0.3
+    cs = r.standard_normal((S, nch, 3))
+    pool0, cs0 = pool.copy(), cs.copy()
+    mixed = r.standard_normal((B, T, nch))
+    w, cb = r.standard_normal((nch, 4)), r.standard_normal(nch)
+    lam = np.log(1 / (1 + np.exp(-(r.standard_normal((B, T, H, 1)) + 3))))
+    beta = 1 / (1 + np.exp(-r.standard_normal((B, T, H))))
+    cfg = _batch_cfg(B, H, d, d, S, 1, 0, oracle.L2NORM, q_scale=0.5)
+    o = oracle.prefill_batch(cfg, pool, slot, lens, lam=lam, beta=beta, lib=lib, mixed=mixed,
+                             conv_w=w, conv_b=cb, conv_pool=cs)
+    qkv = np.zeros((B, T, nch))
+    for b in range(B):
+        if slot[b] < 0:
+            continue
+        seq = list(cs0[slot[b]].T) + list(mixed[b, : lens[b]])
+        for t in range(lens[b]):
+            qkv[b, t] = _silu(sum(seq[t + j] * w[:, j] for j in range(4)) + cb)
+        assert np.array_equal(cs[slot[b]], np.stack(seq[-3:], axis=1)), b
+    q = qkv[..., : H * d].reshape(B, T, H, d)
+    k = qkv[..., H * d: 2 * H * d].reshape(B, T, H, d)
+    v = qkv[..., 2 * H * d:].reshape(B, T, H, d)
+    o_ref = oracle.prefill_batch(cfg, pool0, slot, lens, q=q, k=k, v=v, lam=lam, beta=beta, lib=lib)
+    assert np.max(np.abs(o - o_ref)) <= 1e-12 and np.max(np.abs(pool - pool0)) <= 1e-12
+    for row in (1, 2, 4):
+        assert np.array_equal(cs[row], cs0[row])
+
+
 PINS = [pin_teaching_dense, pin_teaching_deltalog, pin_gla_chunked, pin_delta_wy,
         lambda lib: pin_delta_wy(lib, per_key=True), lambda lib: pin_delta_wy(lib, T=50, dk=8, dv=12, C=16),
         pin_transition_form, pin_invariants, pin_conv, pin_l2norm, pin_deltalog_equals_dense,
         pin_batch_glue, pin_prenorm_log, pin_verify_routing, pin_kda_gate, pin_out_norm_gate,
-        pin_kda_batch_glue, pin_prefill_batch, pin_verify_conv_window, pin_verify_conv_glue]
+        pin_kda_batch_glue, pin_prefill_batch, pin_verify_conv_window, pin_verify_conv_glue,
+        pin_prefill_conv_glue]
 
 
 # ----------------------------------------------------------------------------
@@ -615,6 +653,10 @@ def test_verify_conv_window(oracle_lib):
 
 def test_verify_conv_glue(oracle_lib):
     pin_verify_conv_glue(oracle_lib)
+
+
+def test_prefill_conv_glue(oracle_lib):
+    pin_prefill_conv_glue(oracle_lib)
 
 
 def test_kda_gate(oracle_lib):
