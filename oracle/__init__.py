@@ -349,7 +349,7 @@ def verify_batch(cfg: dict, pool, state_indices, num_accepted, *, q=None, k=None
 
 
 def prefill_batch(cfg: dict, pool, slot, seq_lens, *, q=None, k=None, v=None, lam, beta, lib=None,
-                  mixed=None, conv_w=None, conv_b=None, conv_pool=None):
+                  mixed=None, conv_w=None, conv_b=None, conv_pool=None, out_gate=None, **kda):
     """The prompt through the recurrence, token by token: position t of request b is one dense
     step of :func:`step_batch` on its pool row when t < seq_lens[b] (a prefill seeds the state
     a decode continues from; evolution article, "Prefill中的Chunk微观并行", states the same
@@ -357,7 +357,9 @@ def prefill_batch(cfg: dict, pool, slot, seq_lens, *, q=None, k=None, v=None, la
     q, k [B,T,H,dk], v [B,T,H,dv], lam [B,T,H,dlam], beta [B,T,H]. With ``mixed`` [B,T,nch]
     the step runs the causal conv + SiLU on it instead (flag CONV), through the slot's conv
     state ``conv_pool`` [num_slots, nch, 3] (updated in place: afterwards it holds the last
-    three inputs of the prompt). Returns o [B,T,H,dv] (zero past each prompt)."""
+    three inputs of the prompt). The KDA gate / epilogue inputs (``out_gate`` [B,T,H,dv], and
+    ``a_log``, ``dt_bias``, ``out_norm_w``, ``lower_bound``) pass through to each step.
+    Returns o [B,T,H,dv] (zero past each prompt)."""
     slot = np.asarray(slot, dtype=np.int32)
     src = q if mixed is None else mixed
     B, T = src.shape[0], src.shape[1]
@@ -376,5 +378,6 @@ def prefill_batch(cfg: dict, pool, slot, seq_lens, *, q=None, k=None, v=None, la
             tok = dict(q=q[:, t], k=k[:, t], v=v[:, t])
         else:
             tok = dict(mixed=mixed[:, t], conv_w=conv_w, conv_b=conv_b)
-        o[:, t] = step_batch(c, "dense", st, live, lam=lam[:, t], beta=beta[:, t], lib=lib, **tok)
+        o[:, t] = step_batch(c, "dense", st, live, lam=lam[:, t], beta=beta[:, t], lib=lib,
+                             out_gate=None if out_gate is None else out_gate[:, t], **tok, **kda)
     return o

@@ -560,12 +560,46 @@ def pin_prefill_conv_glue(lib, seed=19):
         assert np.array_equal(cs[row], cs0[row])
 
 
+def pin_prefill_kda_glue(lib, seed=20):
+    """prefill_batch with the KDA gate and output epilogue == prefill_batch on the decays the
+    pinned kda_log_decay gives and beta = sigmoid(logit), each live row then passed through
+    the pinned out_norm_gate; per-key decay, ragged prompts."""
+    r = _rng(seed)
+    B, T, H, d, S = 3, 5, 2, 4, 4
+    slot = np.array([2, 0, 3], dtype=np.int32)
+    lens = np.array([5, 3, 1])
+    pool = r.standard_normal((S, H, d, d)) * 0.3
+    pool0 = pool.copy()
+    q, k, v = (r.standard_normal((B, T, H, d)) for _ in range(3))
+    f = r.standard_normal((B, T, H, d)) - 3
+    logit, g = r.standard_normal((B, T, H)), r.standard_normal((B, T, H, d))
+    a_log, dt_bias = np.log(r.uniform(1, 16, H)), -4 + 0.5 * r.standard_normal((H, d))
+    w = 1 + 0.1 * r.standard_normal(d)
+    kda = dict(a_log=a_log, dt_bias=dt_bias, out_norm_w=w, lower_bound=-5.0)
+    cfg = _batch_cfg(B, H, d, d, S, d, 0, oracle.L2NORM | oracle.GATE_KDA | oracle.OUT_NORM_GATE)
+    o = oracle.prefill_batch(cfg, pool, slot, lens, q=q, k=k, v=v, lam=f, beta=logit, lib=lib,
+                             out_gate=g, **kda)
+    lam = np.zeros_like(f)
+    for b, t, h, c in np.ndindex(f.shape):
+        lam[b, t, h, c] = oracle.kda_log_decay(f[b, t, h, c], a_log[h], dt_bias[h, c], -5.0, lib=lib)
+    cfg_plain = _batch_cfg(B, H, d, d, S, d, 0, oracle.L2NORM)
+    o_plain = oracle.prefill_batch(cfg_plain, pool0, slot, lens, q=q, k=k, v=v, lam=lam,
+                                   beta=1 / (1 + np.exp(-logit)), lib=lib)
+    assert np.max(np.abs(pool - pool0)) <= 1e-12
+    for b in range(B):
+        for t in range(T):
+            for h in range(H):
+                want = (oracle.out_norm_gate(o_plain[b, t, h], g[b, t, h], w, lib=lib) if t < lens[b]
+                        else np.zeros(d))
+                assert np.max(np.abs(o[b, t, h] - want)) <= 1e-12, (b, t, h)
+
+
 PINS = [pin_teaching_dense, pin_teaching_deltalog, pin_gla_chunked, pin_delta_wy,
         lambda lib: pin_delta_wy(lib, per_key=True), lambda lib: pin_delta_wy(lib, T=50, dk=8, dv=12, C=16),
         pin_transition_form, pin_invariants, pin_conv, pin_l2norm, pin_deltalog_equals_dense,
         pin_batch_glue, pin_prenorm_log, pin_verify_routing, pin_kda_gate, pin_out_norm_gate,
         pin_kda_batch_glue, pin_prefill_batch, pin_verify_conv_window, pin_verify_conv_glue,
-        pin_prefill_conv_glue]
+        pin_prefill_conv_glue, pin_prefill_kda_glue]
 
 
 # ----------------------------------------------------------------------------
@@ -657,6 +691,10 @@ def test_verify_conv_glue(oracle_lib):
 
 def test_prefill_conv_glue(oracle_lib):
     pin_prefill_conv_glue(oracle_lib)
+
+
+def test_prefill_kda_glue(oracle_lib):
+    pin_prefill_kda_glue(oracle_lib)
 
 
 def test_kda_gate(oracle_lib):
