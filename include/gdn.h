@@ -278,9 +278,15 @@ int gdn_decode_verify(const gdn_dims *dims, int32_t num_tokens, const gdn_inputs
  *       outside [0, T] skips the request with GDN_STATUS_BAD_LEN.
  *   state_pool [num_slots][H][dk][dv] fp32, read and overwritten.
  *   o [B][T][H][dv] fp32: the readout of every position.
- * Flags: GDN_QKV_BF16, GDN_NO_QK_L2NORM, GDN_GATE_RAW, GDN_PLAIN_UPDATE and decay_per_key;
- * GDN_FUSE_CONV, the log flags and the KDA gate / epilogue flags are rejected with
- * GDN_ERR_UNSUPPORTED. Requires num_tokens >= 0.
+ * Flags: GDN_QKV_BF16, GDN_NO_QK_L2NORM, GDN_GATE_RAW, GDN_PLAIN_UPDATE, decay_per_key,
+ * and as for the decode calls:
+ *   GDN_FUSE_CONV: q, k, v are the width-4 conv + SiLU of in->mixed_qkv [B][T][channels]
+ *       (conv_w, conv_b as for decode); the inputs before position 0 come from the slot's
+ *       conv state in->conv_pool [num_slots][channels][3], which afterwards holds the last
+ *       three inputs of (old state, prompt) -- the state a fused-conv decode continues
+ *       from (unchanged for an empty prompt);
+ *   GDN_GATE_KDA and GDN_OUT_NORM_GATE (in->out_gate [B][T][H][dv]).
+ * The DeltaLog flags are rejected with GDN_ERR_UNSUPPORTED. Requires num_tokens >= 0.
  */
 int gdn_prefill(const gdn_dims *dims, int32_t num_tokens, const gdn_inputs *in,
                 const int32_t *seq_lens, float *state_pool, float *o, int32_t *status, void *stream);

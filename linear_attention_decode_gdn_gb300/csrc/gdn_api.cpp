@@ -273,15 +273,12 @@ int gdn_prefill(const gdn_dims* dims, int32_t num_tokens, const gdn_inputs* in, 
   int rc = check_dims(dims, false);
   if (rc != GDN_OK) return rc;
   if (num_tokens < 0) return fail(GDN_ERR_INVALID_ARG, "num_tokens < 0");
-  if (dims->flags & (GDN_FUSE_CONV | GDN_KLOG_FP32 | GDN_KLOG_PRENORM | GDN_ULOG_BF16 | GDN_GATE_KDA |
-                     GDN_OUT_NORM_GATE | GDN_TEST_STARVE_WAIT))
-    return fail(GDN_ERR_UNSUPPORTED, "prefill: no fused conv, log or KDA epilogue flags");
+  if (dims->flags & (GDN_KLOG_FP32 | GDN_KLOG_PRENORM | GDN_ULOG_BF16 | GDN_TEST_STARVE_WAIT))
+    return fail(GDN_ERR_UNSUPPORTED, "prefill: no DeltaLog flags");
   if (static_cast<long long>(dims->batch) * num_tokens * dims->num_heads > 0x7fffffffLL)
     return fail(GDN_ERR_INVALID_ARG, "batch * num_tokens * num_heads too large");
   if (dims->batch == 0 || num_tokens == 0) return GDN_OK;
-  if (in == nullptr || in->slot == nullptr || in->log_decay == nullptr || in->q == nullptr ||
-      in->k == nullptr || in->v == nullptr)
-    return fail(GDN_ERR_INVALID_ARG, "q, k, v, log_decay and slot are required");
+  if ((rc = check_inputs(dims, in)) != GDN_OK) return rc;
   if (state_pool == nullptr || o == nullptr) return fail(GDN_ERR_INVALID_ARG, "state_pool and o are required");
   if (!aligned16(state_pool)) return fail(GDN_ERR_UNSUPPORTED, "state_pool must be 16-byte aligned");
   gdn::DecodeParams p = make_params(dims, in);

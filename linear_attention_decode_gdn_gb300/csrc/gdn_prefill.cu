@@ -67,7 +67,36 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[PC], int lane) {
   return v[0];
 }
 
-template <int D>
+// Width-4 causal conv + SiLU of channel ch at prompt position pos (evolution article, "去掉分母
+// 引入卷积"): the four inputs pos-3 .. pos come from mixed_qkv [B][T][channels], or, before
+// the prompt, from the slot's conv state (columns 0..2 = positions -3..-1).  Same product
+// order as the decode kernels' one-step conv.
+__device__ __forceinline__ float prefill_conv(const DecodeParams& p, int b, int slot, int pos, int ch,
+                                              bool bf16) {
+  const float4 w = __ldg(reinterpret_cast<const float4*>(p.conv_w) + ch);
+  float x[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int pj = pos - 3 + j;
+    if (pj >= 0) {
+      x[j] = load_elem(p.mixed, (static_cast<size_t>(b) * p.T + pj) * p.channels + ch, bf16);
+    } else {
+      const size_t at = (static_cast<size_t>(slot) * p.channels + ch) * 3 + (pj + 3);
+      x[j] = bf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(p.conv_pool)[at])
+                  : static_cast<const float*>(p.conv_pool)[at];
+    }
+  }
+  float acc = x[0] * w.x;
+  acc = fmaf(x[1], w.y, acc);
+  acc = fmaf(x[2], w.z, acc);
+  acc = fmaf(x[3], w.w, acc);
+  if (p.conv_b != nullptr) acc += __ldg(p.conv_b + ch);
+  return siluf_(acc);
+}
+
+// EXT instances carry the fused conv, the KDA gate parametrisation and the output
+// epilogue; the others compile them out.
+template <int D, bool EXT>
 __global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int TCOL = D / 16;  // product tiles: 16 x 16 thread grid
@@ -81,7 +110,11 @@ __global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
   const bool bf16 = (fl & GDN_QKV_BF16) != 0u;
   const bool plain = (fl & GDN_PLAIN_UPDATE) != 0u;
   const bool l2 = (fl & GDN_NO_QK_L2NORM) == 0u;
+  const bool conv = EXT && (fl & GDN_FUSE_CONV) != 0u;
+  const bool kda_gate = EXT && (fl & GDN_GATE_KDA) != 0u;
+  const bool epilogue = EXT && (fl & GDN_OUT_NORM_GATE) != 0u;
   const int T = p.T;
+  const int HD = p.H * D;
 
   griddep_launch_dependents();
   griddep_wait();
@@ -126,6 +159,26 @@ __global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
     {
       constexpr int TPW = PC / NW;  // tokens per warp
       float qv[TPW][NI], kv[TPW][NI], vv[TPW][NI], lv[TPW][NI], bv[TPW];
+      if (conv) {
+#pragma unroll
+        for (int u = 0; u < TPW; ++u) {
+          const int tt = warp + NW * u;
+          const bool live = tt < n;
+          const size_t tokrow = (static_cast<size_t>(b) * T + t0 + tt) * p.H + h;
+#pragma unroll
+          for (int i = 0; i < NI; ++i) {
+            const int c = lane + 32 * i;
+            qv[u][i] = kv[u][i] = vv[u][i] = lv[u][i] = 0.0f;
+            if (live && c < D) {
+              qv[u][i] = prefill_conv(p, b, slot, t0 + tt, h * D + c, bf16);
+              kv[u][i] = prefill_conv(p, b, slot, t0 + tt, HD + h * D + c, bf16);
+              vv[u][i] = prefill_conv(p, b, slot, t0 + tt, 2 * HD + h * D + c, bf16);
+            }
+            if (live && c < dlam) lv[u][i] = __ldg(p.lam + tokrow * dlam + c);
+          }
+          bv[u] = live ? (p.beta ? __ldg(p.beta + tokrow) : 1.0f) : 0.0f;
+        }
+      } else {
       // raw loads first (the dtype branch outside the loops), conversions after them
       uint32_t qr[TPW][NI], kr[TPW][NI], vr[TPW][NI];
 #pragma unroll
@@ -162,6 +215,7 @@ __global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
           kv[u][i] = bf16 ? __uint_as_float(kr[u][i] << 16) : __uint_as_float(kr[u][i]);
           vv[u][i] = bf16 ? __uint_as_float(vr[u][i] << 16) : __uint_as_float(vr[u][i]);
         }
+      }
 #pragma unroll
       for (int u = 0; u < TPW; ++u) {
         const int tt = warp + NW * u;
@@ -186,13 +240,18 @@ __global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
           }
           if (c < dlam) {
             float lam = lv[u][i];
-            if (live && (fl & GDN_GATE_RAW)) lam = log_sigmoidf_(lam);
+            if (live && (fl & GDN_GATE_RAW)) {
+              lam = log_sigmoidf_(lam);
+            } else if (live && kda_gate) {
+              const float ga = __ldg(p.a_log + h), gdt = __ldg(p.dt_bias + static_cast<size_t>(h) * dlam + c);
+              lam = p.lower_bound * sigmoidf_(expf(ga) * (lam + gdt));
+            }
             gam[tt * dlam + c] = lam;
           }
         }
         if (lane == 0) {
           float be = bv[u];
-          if (live && p.beta && (fl & GDN_GATE_RAW)) be = sigmoidf_(be);
+          if (live && p.beta && (fl & (GDN_GATE_RAW | GDN_GATE_KDA))) be = sigmoidf_(be);
           bet[tt] = be;
         }
       }
@@ -308,7 +367,11 @@ __global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
         float y[4] = {Y[t * D + j], 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int s = 0; s <= t; ++s) y[s & 3] = fmaf(P[t * PC + s], bc[s], y[s & 3]);
-        if (t < n) p.o[((static_cast<size_t>(b) * T + t0 + t) * p.H + h) * D + j] = (y[0] + y[1]) + (y[2] + y[3]);
+        const float ot = (y[0] + y[1]) + (y[2] + y[3]);
+        if (epilogue)
+          Y[t * D + j] = ot;  // normalised and gated below, once the whole row is known
+        else if (t < n)
+          p.o[((static_cast<size_t>(b) * T + t0 + t) * p.H + h) * D + j] = ot;
       }
     }
     // Khat = e^{gamma_C - gamma_s} k_s (rows past n hold zero keys)
@@ -318,6 +381,21 @@ __global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
       Kt[i] = Kn[i] * expf(gam[(PC - 1) * dlam + gc] - gam[tt * dlam + gc]);
     }
     __syncthreads();
+
+    // ---- KDA output epilogue: o <- o / sqrt(mean(o^2) + eps) * w * sigmoid(g) per row ---
+    if (epilogue) {
+      for (int t = warp; t < n; t += NW) {
+        float ss = 0.0f;
+        for (int j = lane; j < D; j += 32) ss = fmaf(Y[t * D + j], Y[t * D + j], ss);
+        ss = warp_sum(ss);
+        const float inv = 1.0f / sqrtf(ss / static_cast<float>(D) + p.out_eps);
+        const size_t orow = ((static_cast<size_t>(b) * T + t0 + t) * p.H + h) * D;
+        for (int j = lane; j < D; j += 32) {
+          const float w = p.out_norm_w ? __ldg(p.out_norm_w + j) : 1.0f;
+          p.o[orow + j] = Y[t * D + j] * inv * w * sigmoidf_(__ldg(p.out_gate + orow + j));
+        }
+      }
+    }
 
     // ---- S <- D(gamma_C) S + Khat^T B ---------------------------------------------------
     {
@@ -353,12 +431,41 @@ __global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
   __syncthreads();
   for (int i = tid; i < D * D / 4; i += NT)
     reinterpret_cast<float4*>(Sg)[i] = reinterpret_cast<const float4*>(S)[i];
+  // the slot's conv state keeps the last three inputs of (old state, prompt), bit-exact;
+  // every read of the old state lies before the barrier above
+  if (conv && n_tok > 0) {
+    for (int idx = tid; idx < 3 * D; idx += NT) {
+      const int g = idx / D, c = idx - g * D;
+      const int ch = g * HD + h * D + c;
+      const size_t srow = (static_cast<size_t>(slot) * p.channels + ch) * 3;
+      uint32_t nb[3];
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        const int pj = n_tok - 3 + j;
+        if (pj >= 0) {
+          const size_t at = (static_cast<size_t>(b) * T + pj) * p.channels + ch;
+          nb[j] = bf16 ? static_cast<uint32_t>(__ldg(static_cast<const uint16_t*>(p.mixed) + at))
+                       : __float_as_uint(__ldg(static_cast<const float*>(p.mixed) + at));
+        } else {
+          nb[j] = bf16 ? static_cast<uint32_t>(static_cast<const uint16_t*>(p.conv_pool)[srow + pj + 3])
+                       : __float_as_uint(static_cast<const float*>(p.conv_pool)[srow + pj + 3]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        if (bf16)
+          static_cast<uint16_t*>(p.conv_pool)[srow + j] = static_cast<uint16_t>(nb[j]);
+        else
+          static_cast<float*>(p.conv_pool)[srow + j] = __uint_as_float(nb[j]);
+      }
+    }
+  }
 }
 
 constexpr int kMaxDevices = 64;
 
-template <int D>
-cudaError_t launch_prefill_d(const DecodeParams& p, cudaStream_t stream) {
+template <int D, bool EXT>
+cudaError_t launch_prefill_de(const DecodeParams& p, cudaStream_t stream) {
   static std::atomic<uint32_t> configured[kMaxDevices];
   const PrefillLayout L = prefill_layout(D, p.dlam);
   int dev = 0;
@@ -366,7 +473,7 @@ cudaError_t launch_prefill_d(const DecodeParams& p, cudaStream_t stream) {
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (configured[dev].load(std::memory_order_relaxed) < L.total) {
-    err = cudaFuncSetAttribute(gdn_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err = cudaFuncSetAttribute(gdn_prefill_kernel<D, EXT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(L.total));
     if (err != cudaSuccess) return err;
     configured[dev].store(L.total, std::memory_order_relaxed);
@@ -381,9 +488,15 @@ cudaError_t launch_prefill_d(const DecodeParams& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, gdn_prefill_kernel<D>, p);
+  err = cudaLaunchKernelEx(&cfg, gdn_prefill_kernel<D, EXT>, p);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_prefill_d(const DecodeParams& p, cudaStream_t stream) {
+  if (p.flags & (GDN_FUSE_CONV | GDN_GATE_KDA | GDN_OUT_NORM_GATE)) return launch_prefill_de<D, true>(p, stream);
+  return launch_prefill_de<D, false>(p, stream);
 }
 
 }  // namespace

@@ -221,3 +221,141 @@ def test_back_to_back_launches_match_oracle():
     S_ref = st.S
     assert float(np.max(np.abs(pd.state.cpu().numpy() - S_ref))) / float(np.max(np.abs(S_ref))) <= TOL
     assert float(np.max(np.abs(pl.state.cpu().numpy() - S_ref))) / float(np.max(np.abs(S_ref))) <= 5e-3
+
+
+def _run_ext(D, per_key, T, lens, conv=False, kda=False, bias=True, H=2, seed=50, slot=None,
+             bf16=True):
+    """Prefill with the fused conv (q, k, v from mixed_qkv through the slot's conv state)
+    and / or the KDA gate and output epilogue. Returns the output and state relative
+    errors, whether the conv states match the oracle's bit for bit, and the pools."""
+    B = len(lens)
+    slot = np.arange(B, dtype=np.int32)[::-1].copy() if slot is None else np.asarray(slot, np.int32)
+    S = int(max(slot.max(), 0)) + 2
+    dlam = D if per_key else 1
+    nch = 3 * H * D
+    r = np.random.default_rng(seed)
+    pool0 = (0.1 * r.standard_normal((S, H, D, D))).astype(np.float32)
+    flags = (gdn.QKV_BF16 if bf16 else 0) | (gdn.FUSE_CONV if conv else 0)
+    oflags = oracle.L2NORM
+    dev, ref = {}, {}
+    if conv:
+        mixed = r.standard_normal((B, T, nch)).astype(np.float32)
+        cs0 = r.standard_normal((S, nch, 3)).astype(np.float32)
+        if bf16:
+            mbits, mixed = wl.bf16_round(mixed)
+            cbits, cs0 = wl.bf16_round(cs0)
+            dev.update(mixed_qkv=dev_bf16(mbits), conv_pool=dev_bf16(cbits))
+        else:
+            dev.update(mixed_qkv=dev_f32(mixed), conv_pool=dev_f32(cs0))
+        w = (0.5 * r.standard_normal((nch, 4))).astype(np.float32)
+        cb = (0.1 * r.standard_normal(nch)).astype(np.float32) if bias else None
+        dev.update(conv_w=dev_f32(w), conv_b=None if cb is None else dev_f32(cb))
+        cs_ref = cs0.astype(np.float64)
+        ref.update(mixed=mixed.astype(np.float64), conv_w=w.astype(np.float64),
+                   conv_b=None if cb is None else cb.astype(np.float64), conv_pool=cs_ref)
+    else:
+        x = {n: r.standard_normal((B, T, H, D)).astype(np.float32) for n in ("q", "k", "v")}
+        for n in x:
+            bits, x[n] = wl.bf16_round(x[n])
+            dev[n] = dev_bf16(bits)
+            ref[n] = x[n].astype(np.float64)
+    if kda:
+        flags |= gdn.GATE_KDA | gdn.OUT_NORM_GATE
+        oflags |= oracle.GATE_KDA | oracle.OUT_NORM_GATE
+        wk = wl.Workload("prefill_kda", B, H, D, D, 1, (1,), True, False, per_key, seed + 3, kda_full=True)
+        kp = wl.kda_gate_params(wk)
+        f = (r.standard_normal((B, T, H, dlam)) - 3).astype(np.float32)
+        logit = r.standard_normal((B, T, H)).astype(np.float32)
+        g = r.standard_normal((B, T, H, D)).astype(np.float32)
+        dev.update(log_decay=dev_f32(f), beta=dev_f32(logit), out_gate=dev_f32(g),
+                   **{n: dev_f32(kp[n]) for n in ("a_log", "dt_bias", "out_norm_w")})
+        ref.update(lam=f.astype(np.float64), beta=logit.astype(np.float64), out_gate=g.astype(np.float64),
+                   a_log=kp["a_log"].astype(np.float64), dt_bias=kp["dt_bias"].astype(np.float64),
+                   out_norm_w=kp["out_norm_w"].astype(np.float64), lower_bound=kp["lower_bound"])
+    else:
+        a_raw = r.standard_normal((B, T, H, dlam)) + 3
+        lam = (-np.log1p(np.exp(-a_raw))).astype(np.float32)
+        beta = (1 / (1 + np.exp(-r.standard_normal((B, T, H))))).astype(np.float32)
+        dev.update(log_decay=dev_f32(lam), beta=dev_f32(beta))
+        ref.update(lam=lam.astype(np.float64), beta=beta.astype(np.float64))
+    dims = gdn.make_dims(B, H, D, num_slots=S, decay_per_key=per_key, flags=flags, q_scale=D ** -0.5)
+    cfg = dict(batch=B, num_heads=H, dk=D, dv=D, num_slots=S, dlam=dlam, log_capacity=0, flags=oflags,
+               q_scale=D ** -0.5, l2_eps=1e-6)
+    pool, pool_ref = dev_f32(pool0), pool0.astype(np.float64)
+    o = torch.full((B, T, H, D), 5.0, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gdn.prefill(dims, T, gdn.make_inputs(slot=dev_i32(slot), **dev), pool, o, seq_lens=dev_i32(lens), status=status)
+    o_ref = oracle.prefill_batch(cfg, pool_ref, slot, lens, **ref)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    og = o.cpu().numpy().astype(np.float64)
+    err = ref_max = 0.0
+    for b in range(B):
+        n = lens[b] if slot[b] >= 0 else 0
+        err = max(err, float(np.max(np.abs(og[b, :n] - o_ref[b, :n]), initial=0.0)))
+        ref_max = max(ref_max, float(np.max(np.abs(o_ref[b, :n]), initial=0.0)))
+        assert np.all(og[b, n:] == 5.0)
+    pg = pool.cpu().numpy().astype(np.float64)
+    serr = float(np.max(np.abs(pg - pool_ref))) / float(np.max(np.abs(pool_ref)))
+    conv_ok = True
+    if conv:
+        cp = dev["conv_pool"].cpu()
+        cg = ((cp.view(torch.int16).numpy().astype(np.uint16).astype(np.uint32) << 16).view(np.float32)
+              if bf16 else cp.numpy())
+        conv_ok = np.array_equal(cg.astype(np.float64), cs_ref)
+    return err / ref_max, serr, conv_ok, (dims, pool, dev, cfg, pool_ref, ref)
+
+
+@pytest.mark.parametrize("D,per_key", [(128, False), (64, True), (16, False)])
+def test_prefill_fused_conv(D, per_key):
+    """q, k, v from the width-4 conv of mixed_qkv; prompts of 0, 1, 2, 33 and 70 positions
+    (the conv reaches into the slot's conv state for the first three), a padding request;
+    conv states afterwards bit-exact."""
+    e_o, e_s, ok, _ = _run_ext(D, per_key, 70, np.array([0, 1, 2, 33, 70, 40]), conv=True,
+                               slot=[4, 0, 2, -1, 3, 1], seed=50 + D)
+    assert e_o <= TOL and e_s <= TOL and ok, (e_o, e_s, ok)
+
+
+def test_prefill_fused_conv_fp32_no_bias():
+    e_o, e_s, ok, _ = _run_ext(128, False, 40, np.array([40, 3, 17]), conv=True, bias=False, bf16=False, seed=61)
+    assert e_o <= TOL and e_s <= TOL and ok, (e_o, e_s, ok)
+
+
+def test_prefill_kda_gate_and_epilogue():
+    """The KDA gate parametrisation and output epilogue, per-key and per-head decay."""
+    for per_key in (True, False):
+        e_o, e_s, _, _ = _run_ext(128, per_key, 70, np.array([70, 33, 1, 0]), kda=True, seed=62 + int(per_key))
+        assert e_o <= TOL and e_s <= TOL, (per_key, e_o, e_s)
+
+
+def test_prefill_conv_then_fused_conv_decode():
+    """The small hybrid-layer form end to end: a fused-conv prefill leaves the state and the
+    conv state a fused-conv dense decode continues from (matches the oracle's pass over the
+    prompt and four generated tokens)."""
+    e_o, e_s, ok, (dims, pool, dev, cfg, pool_ref, ref) = _run_ext(
+        128, False, 50, np.array([50, 37, 2, 50]), conv=True, slot=[0, 1, 2, 3], seed=70)
+    assert e_o <= TOL and e_s <= TOL and ok, (e_o, e_s, ok)
+    B, H, D = 4, 2, 128
+    nch = 3 * H * D
+    st = oracle.BatchState(cfg["num_slots"], H, D, D)
+    st.S, st.conv = pool_ref, ref["conv_pool"]
+    cfg_d = dict(cfg, batch=B, flags=cfg["flags"] | oracle.CONV)
+    slot = np.arange(B, dtype=np.int32)
+    r = np.random.default_rng(71)
+    o = torch.zeros((B, H, D), device="cuda")
+    err = ref_max = 0.0
+    for t in range(4):
+        bits, mixed = wl.bf16_round(r.standard_normal((B, nch)).astype(np.float32))
+        lam = (-np.log1p(np.exp(-(r.standard_normal((B, H, 1)) + 3)))).astype(np.float32)
+        beta = (1 / (1 + np.exp(-r.standard_normal((B, H))))).astype(np.float32)
+        ins = gdn.make_inputs(mixed_qkv=dev_bf16(bits), conv_w=dev["conv_w"], conv_b=dev["conv_b"],
+                              conv_pool=dev["conv_pool"], log_decay=dev_f32(lam), beta=dev_f32(beta),
+                              slot=dev_i32(slot))
+        gdn.decode_dense(dims, ins, pool, o)
+        o_ref = oracle.step_batch(cfg_d, "dense", st, slot, mixed=mixed.astype(np.float64),
+                                  conv_w=ref["conv_w"], conv_b=ref["conv_b"], lam=lam.astype(np.float64),
+                                  beta=beta.astype(np.float64))
+        torch.cuda.synchronize()
+        err = max(err, float(np.max(np.abs(o.cpu().numpy() - o_ref))))
+        ref_max = max(ref_max, float(np.max(np.abs(o_ref))))
+    assert err / ref_max <= TOL, err / ref_max
