@@ -22,8 +22,12 @@ namespace {
 constexpr int PC = 32;  // tokens per chunk (one warp's width: the pair reductions map s to lanes)
 
 struct PrefillLayout {
-  uint32_t S, Kn, Qn, V, Kt, Y, A, P, gam, bet, total;
+  uint32_t S, Kn, Qn, V, Kt, Y, A, P, gam, bet, KQt, total;
 };
+
+// [Ktil; Qtil] stored transposed for the first product at head size 128: row c holds the
+// 2*PC entries of key channel c, padded to a 16-byte multiple
+constexpr int KQS = 2 * PC + 4;
 
 __host__ __device__ inline PrefillLayout prefill_layout(int D, int dlam) {
   PrefillLayout L{};
@@ -48,6 +52,9 @@ __host__ __device__ inline PrefillLayout prefill_layout(int D, int dlam) {
   off += static_cast<uint32_t>(PC * dlam * 4);
   L.bet = off;  // [PC]
   off += static_cast<uint32_t>(PC * 4);
+  off = (off + 15u) & ~15u;
+  L.KQt = off;  // [D][KQS] (head size 128 only)
+  off += (D == 128) ? static_cast<uint32_t>(D * KQS * 4) : 0u;
   L.total = off;
   return L;
 }
@@ -142,6 +149,7 @@ __global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
   float* P = reinterpret_cast<float*>(smem + L.P);
   float* gam = reinterpret_cast<float*>(smem + L.gam);
   float* bet = reinterpret_cast<float*>(smem + L.bet);
+  float* KQt = reinterpret_cast<float*>(smem + L.KQt);
 
   float* Sg = p.state + (static_cast<size_t>(slot) * p.H + h) * static_cast<size_t>(D * D);
   for (int i = tid; i < D * D / 4; i += NT)
@@ -298,18 +306,75 @@ __global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
     __syncthreads();
 
     // ---- Ktil = e^{gamma} k, Qtil = e^{gamma} q ----------------------------------------
-    for (int i = tid; i < PC * D; i += NT) {
-      const int tt = i / D, c = i - tt * D;
-      const float e = expf(gam[tt * dlam + (dlam > 1 ? c : 0)]);
-      Kt[i] = Kn[i] * e;
-      Qn[i] *= e;
+    if constexpr (D == 128) {
+      // transposed: KQt[c][t] = Ktil_t[c], KQt[c][PC + t] = Qtil_t[c]
+      for (int i = tid; i < PC * D; i += NT) {
+        const int tt = i / D, c = i - tt * D;
+        const float e = expf(gam[tt * dlam + (dlam > 1 ? c : 0)]);
+        KQt[c * KQS + tt] = Kn[i] * e;
+        KQt[c * KQS + PC + tt] = Qn[i] * e;
+      }
+    } else {
+      for (int i = tid; i < PC * D; i += NT) {
+        const int tt = i / D, c = i - tt * D;
+        const float e = expf(gam[tt * dlam + (dlam > 1 ? c : 0)]);
+        Kt[i] = Kn[i] * e;
+        Qn[i] *= e;
+      }
     }
     __syncthreads();
 
     // ---- [Ktil; Qtil] S0: R = diag(beta)(V - Ktil S0), Y = Qtil S0 ---------------------
-    // 64 rows (16 groups of 4) x D columns (16 groups of D/16); the Ktil rows are skipped
-    // under the plain update
-    if (!plain || rg >= 8) {
+    // the Ktil rows are skipped under the plain update
+    if constexpr (D == 128) {
+      // warp w: rows 16*(w/2) .. +16 of the 64, columns 64*(w%2) .. +64; lane: 4 rows and
+      // two runs of 4 columns, 32 apart.  Per channel a warp loads one float4 of KQt (4
+      // distinct, broadcast) and two of S (8 distinct, contiguous): 3 shared-memory
+      // wavefronts per 32 FMAs per lane
+      const int wb = warp >> 1, rgl = lane >> 3;
+      const int row0 = wb * 16 + rgl * 4;
+      const int col0 = (warp & 1) * 64 + (lane & 7) * 4;
+      if (!plain || wb >= 2) {
+        float acc[4][8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+#pragma unroll 4
+        for (int c = 0; c < D; ++c) {
+          const float4 a = *reinterpret_cast<const float4*>(KQt + c * KQS + row0);
+          const float4 b0 = *reinterpret_cast<const float4*>(S + c * D + col0);
+          const float4 b1 = *reinterpret_cast<const float4*>(S + c * D + col0 + 32);
+          const float av[4] = {a.x, a.y, a.z, a.w};
+          const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = row0 + i;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int col = col0 + 32 * hf;
+            const float* ac = acc[i] + 4 * hf;
+            if (row < PC) {
+              float4 x = *reinterpret_cast<const float4*>(V + row * D + col);
+              const float be = bet[row];
+              x.x = be * (x.x - ac[0]);
+              x.y = be * (x.y - ac[1]);
+              x.z = be * (x.z - ac[2]);
+              x.w = be * (x.w - ac[3]);
+              *reinterpret_cast<float4*>(V + row * D + col) = x;
+            } else {
+              *reinterpret_cast<float4*>(Y + (row - PC) * D + col) = make_float4(ac[0], ac[1], ac[2], ac[3]);
+            }
+          }
+        }
+      }
+    } else if (!plain || rg >= 8) {
+      // 64 rows (16 groups of 4) x D columns (16 groups of D/16)
       const float* Ain = (rg < 8) ? Kt : Qn;
       const int r0 = (rg & 7) * 4;
       float acc[4][TCOL];
@@ -398,7 +463,43 @@ __global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
     }
 
     // ---- S <- D(gamma_C) S + Khat^T B ---------------------------------------------------
-    {
+    if constexpr (D == 128) {
+      // lane: rows 8*rg .. +8, columns 4*cg .. +4 and 64 + 4*cg .. +4 (contiguous float4 runs
+      // across the 16 lanes of a row group, for the operand loads and the state update)
+      float acc[8][8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+#pragma unroll 4
+      for (int s = 0; s < PC; ++s) {
+        const float4 a0 = *reinterpret_cast<const float4*>(Kt + s * D + rg * 8);
+        const float4 a1 = *reinterpret_cast<const float4*>(Kt + s * D + rg * 8 + 4);
+        const float4 b0 = *reinterpret_cast<const float4*>(V + s * D + cg * 4);
+        const float4 b1 = *reinterpret_cast<const float4*>(V + s * D + 64 + cg * 4);
+        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = rg * 8 + i;
+        const float dC = expf(gam[(PC - 1) * dlam + (dlam > 1 ? r : 0)]);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          float* sp = S + r * D + 64 * hf + cg * 4;
+          float4 x = *reinterpret_cast<const float4*>(sp);
+          x.x = fmaf(dC, x.x, acc[i][4 * hf + 0]);
+          x.y = fmaf(dC, x.y, acc[i][4 * hf + 1]);
+          x.z = fmaf(dC, x.z, acc[i][4 * hf + 2]);
+          x.w = fmaf(dC, x.w, acc[i][4 * hf + 3]);
+          *reinterpret_cast<float4*>(sp) = x;
+        }
+      }
+    } else {
       float acc[TCOL][TCOL];
 #pragma unroll
       for (int i = 0; i < TCOL; ++i)
