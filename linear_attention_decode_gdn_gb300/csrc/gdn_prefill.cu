@@ -267,17 +267,77 @@ __global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
     __syncthreads();
 
     // ---- cumulative log-decays inside the chunk --------------------------------------
+    // Per-key decay: the pair factor e^{gamma_t - gamma_s} is split at a reference token
+    // (evolution article, appendix 1 "chunk内 A和M 的计算": 16-token sub-blocks; rows of
+    // sub-block a and columns before it use a's first token, both exponents <= 0; the
+    // diagonal sub-blocks use their own first token, the column exponent then spans at most
+    // 15 tokens).  Here ref(t) = 0 for t < 16, else 16, and a column s < 16 carries both
+    // references.  The split needs every factor's exponent <= 80 (no fp32 overflow); the
+    // pages bound it through lower_bound = -5, which this interface does not assume, so
+    // it is checked per chunk and the exact per-term form is used where it fails.
+    bool split_ok = true;
     for (int c = tid; c < dlam; c += NT) {
       float acc = 0.0f;
       for (int tt = 0; tt < PC; ++tt) {
         acc += gam[tt * dlam + c];
         gam[tt * dlam + c] = acc;
       }
+      if (dlam > 1) {
+        const float g0 = gam[c], g16 = gam[16 * dlam + c];
+        for (int tt = 0; tt < PC; ++tt) {
+          const float g = gam[tt * dlam + c];
+          const float e_row = g - (tt < 16 ? g0 : g16);
+          const float e_col = fmaxf(g16 - g, tt < 16 ? g0 - g : -INFINITY);
+          if (!(fmaxf(e_row, e_col) <= 80.0f)) split_ok = false;  // also catches NaN
+        }
+      }
     }
-    __syncthreads();
+    const bool split = (dlam > 1) && !__syncthreads_or(!split_ok);
+
+    // column factors of the split: Km16[s][c] = k_s[c] e^{gamma_16 - gamma_s} (all s, in
+    // the Khat buffer) and Km0[s][c] = k_s[c] e^{gamma_0 - gamma_s} (s < 16, in Y); both
+    // buffers are free until the products below
+    float* Km16 = Kt;
+    float* Km0 = Y;
+    if (split) {
+      for (int i = tid; i < (PC + 16) * D; i += NT) {
+        const int r = i / D, c = i - r * D;
+        if (r < PC)
+          Km16[r * D + c] = Kn[r * D + c] * expf(gam[16 * dlam + c] - gam[r * dlam + c]);
+        else
+          Km0[(r - PC) * D + c] = Kn[(r - PC) * D + c] * expf(gam[c] - gam[(r - PC) * dlam + c]);
+      }
+      __syncthreads();
+    }
 
     // ---- A (strictly lower, times beta_t) and P (lower with the diagonal) --------------
     // warp w takes rows t = w, w + 8, ...; lane = key channel; the pair sums end in lane s
+    if (split) {
+      for (int t = warp; t < PC; t += NW) {
+        float ak[PC], aq[PC];
+#pragma unroll
+        for (int s2 = 0; s2 < PC; ++s2) ak[s2] = aq[s2] = 0.0f;
+        const float* kml = (t < 16) ? Km0 : Km16;  // columns s < 16
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+          const int c = lane + 32 * i;
+          if (c < D) {
+            const float f = expf(gam[t * dlam + c] - gam[(t < 16 ? 0 : 16) * dlam + c]);
+            const float kt = Kn[t * D + c] * f, qt = Qn[t * D + c] * f;
+#pragma unroll
+            for (int s2 = 0; s2 < PC; ++s2) {
+              const float w = (s2 < 16) ? kml[s2 * D + c] : Km16[s2 * D + c];
+              ak[s2] = fmaf(kt, w, ak[s2]);
+              aq[s2] = fmaf(qt, w, aq[s2]);
+            }
+          }
+        }
+        const float a_ts = transpose_reduce(ak, lane);
+        const float p_ts = transpose_reduce(aq, lane);
+        A[t * PC + lane] = (lane < t) ? bet[t] * a_ts : 0.0f;
+        P[t * PC + lane] = (lane <= t) ? p_ts : 0.0f;
+      }
+    } else
     for (int t = warp; t < PC; t += NW) {
       float ak[PC], aq[PC];
 #pragma unroll

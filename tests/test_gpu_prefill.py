@@ -359,3 +359,39 @@ def test_prefill_conv_then_fused_conv_decode():
         err = max(err, float(np.max(np.abs(o.cpu().numpy() - o_ref))))
         ref_max = max(ref_max, float(np.max(np.abs(o_ref))))
     assert err / ref_max <= TOL, err / ref_max
+
+
+@pytest.mark.parametrize("lam_mean", [-6.0, -4.5])
+def test_prefill_strong_per_key_decay(lam_mean):
+    """Per-key decay strong enough that a 16-token sub-block spans more than e^80 (mean -6:
+    the exact per-term pair factors) or close to it (mean -4.5: the reference-point split),
+    and a prompt whose chunks alternate between mild and strong decay (both paths in one
+    call); outputs and states at the dense bar."""
+    B, T, H, D = 3, 96, 2, 128
+    lens = np.array([96, 70, 33])
+    dev, ref = _inputs(B, T, H, D, D, True, 90)
+    r = np.random.default_rng(91)
+    lam = (lam_mean + 0.5 * r.standard_normal((B, T, H, D))).astype(np.float32)
+    lam = np.minimum(lam, np.float32(0))
+    mixed = lam.copy()
+    mixed[:, 32:64] = (-0.05 * r.random((B, 32, H, D))).astype(np.float32)  # chunk 1 mild
+    for lm in (lam, mixed):
+        dev["log_decay"] = dev_f32(lm)
+        ref["lam"] = lm.astype(np.float64)
+        slot = np.arange(B, dtype=np.int32)
+        pool0 = (0.1 * r.standard_normal((B, H, D, D))).astype(np.float32)
+        pool, pool_ref = dev_f32(pool0), pool0.astype(np.float64)
+        dims = gdn.make_dims(B, H, D, num_slots=B, decay_per_key=True, flags=gdn.QKV_BF16, q_scale=D ** -0.5)
+        cfg = dict(batch=B, num_heads=H, dk=D, dv=D, num_slots=B, dlam=D, log_capacity=0,
+                   flags=oracle.L2NORM, q_scale=D ** -0.5, l2_eps=1e-6)
+        o = torch.zeros((B, T, H, D), device="cuda")
+        gdn.prefill(dims, T, gdn.make_inputs(slot=dev_i32(slot), **dev), pool, o, seq_lens=dev_i32(lens))
+        o_ref = oracle.prefill_batch(cfg, pool_ref, slot, lens, **ref)
+        torch.cuda.synchronize()
+        og = o.cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(og))
+        err = max(float(np.max(np.abs(og[b, :lens[b]] - o_ref[b, :lens[b]]))) for b in range(B))
+        scale = max(float(np.max(np.abs(o_ref[b, :lens[b]]))) for b in range(B))
+        pg = pool.cpu().numpy().astype(np.float64)
+        serr = float(np.max(np.abs(pg - pool_ref))) / float(np.max(np.abs(pool_ref)))
+        assert err / scale <= TOL and serr <= TOL, (lam_mean, err / scale, serr)
