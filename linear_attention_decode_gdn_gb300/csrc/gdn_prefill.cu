@@ -227,7 +227,6 @@ __global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
 #pragma unroll
       for (int u = 0; u < TPW; ++u) {
         const int tt = warp + NW * u;
-        const bool live = tt < n;
         float sq = 0.0f, sk = 0.0f;
 #pragma unroll
         for (int i = 0; i < NI; ++i) {
@@ -246,25 +245,26 @@ __global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
             Kn[tt * D + c] = kv[u][i] * kinv;
             V[tt * D + c] = vv[u][i];
           }
-          if (c < dlam) {
-            float lam = lv[u][i];
-            if (live && (fl & GDN_GATE_RAW)) {
-              lam = log_sigmoidf_(lam);
-            } else if (live && kda_gate) {
-              const float ga = __ldg(p.a_log + h), gdt = __ldg(p.dt_bias + static_cast<size_t>(h) * dlam + c);
-              lam = p.lower_bound * sigmoidf_(expf(ga) * (lam + gdt));
-            }
-            gam[tt * dlam + c] = lam;
-          }
+          if (c < dlam) gam[tt * dlam + c] = lv[u][i];  // gate inputs; transformed below
         }
-        if (lane == 0) {
-          float be = bv[u];
-          if (live && p.beta && (fl & (GDN_GATE_RAW | GDN_GATE_KDA))) be = sigmoidf_(be);
-          bet[tt] = be;
-        }
+        if (lane == 0) bet[tt] = bv[u];
       }
     }
     __syncthreads();
+
+    // ---- gate parametrisations, once per element (kept out of the unrolled token code) --
+    if (fl & (GDN_GATE_RAW | GDN_GATE_KDA)) {
+      const float ga = kda_gate ? expf(__ldg(p.a_log + h)) : 0.0f;
+      for (int idx = tid; idx < n * dlam; idx += NT) {  // live tokens only
+        const int c = idx - (idx / dlam) * dlam;
+        const float x = gam[idx];
+        gam[idx] = kda_gate ? p.lower_bound * sigmoidf_(ga * (x + __ldg(p.dt_bias + static_cast<size_t>(h) * dlam + c)))
+                            : log_sigmoidf_(x);
+      }
+      if (p.beta)
+        for (int tt = tid; tt < n; tt += NT) bet[tt] = sigmoidf_(bet[tt]);
+      __syncthreads();
+    }
 
     // ---- cumulative log-decays inside the chunk --------------------------------------
     // Per-key decay: the pair factor e^{gamma_t - gamma_s} is split at a reference token
@@ -277,17 +277,19 @@ __global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
     // it is checked per chunk and the exact per-term form is used where it fails.
     bool split_ok = true;
     for (int c = tid; c < dlam; c += NT) {
-      float acc = 0.0f;
-      for (int tt = 0; tt < PC; ++tt) {
-        acc += gam[tt * dlam + c];
-        gam[tt * dlam + c] = acc;
-      }
+      // all 32 loads first, then the running sum in registers (no load-store chain)
+      float g[PC];
+#pragma unroll
+      for (int tt = 0; tt < PC; ++tt) g[tt] = gam[tt * dlam + c];
+#pragma unroll
+      for (int tt = 1; tt < PC; ++tt) g[tt] += g[tt - 1];
+#pragma unroll
+      for (int tt = 0; tt < PC; ++tt) gam[tt * dlam + c] = g[tt];
       if (dlam > 1) {
-        const float g0 = gam[c], g16 = gam[16 * dlam + c];
+#pragma unroll
         for (int tt = 0; tt < PC; ++tt) {
-          const float g = gam[tt * dlam + c];
-          const float e_row = g - (tt < 16 ? g0 : g16);
-          const float e_col = fmaxf(g16 - g, tt < 16 ? g0 - g : -INFINITY);
+          const float e_row = g[tt] - (tt < 16 ? g[0] : g[16]);
+          const float e_col = fmaxf(g[16] - g[tt], tt < 16 ? g[0] - g[tt] : -INFINITY);
           if (!(fmaxf(e_row, e_col) <= 80.0f)) split_ok = false;  // also catches NaN
         }
       }
@@ -318,7 +320,7 @@ __global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
 #pragma unroll
         for (int s2 = 0; s2 < PC; ++s2) ak[s2] = aq[s2] = 0.0f;
         const float* kml = (t < 16) ? Km0 : Km16;  // columns s < 16
-#pragma unroll
+#pragma unroll 1
         for (int i = 0; i < NI; ++i) {
           const int c = lane + 32 * i;
           if (c < D) {
@@ -342,18 +344,33 @@ __global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
       float ak[PC], aq[PC];
 #pragma unroll
       for (int s = 0; s < PC; ++s) ak[s] = aq[s] = 0.0f;
+      if (dlam > 1) {  // exact per-term decay factors
+#pragma unroll 1
+        for (int i = 0; i < NI; ++i) {
+          const int c = lane + 32 * i;
+          if (c < D) {
+            const float kt = Kn[t * D + c], qt = Qn[t * D + c];
+            const float gt = gam[t * dlam + c];
 #pragma unroll
-      for (int i = 0; i < NI; ++i) {
-        const int c = lane + 32 * i;
-        if (c < D) {
-          const float kt = Kn[t * D + c], qt = Qn[t * D + c];
-          const float gt = (dlam > 1) ? gam[t * dlam + c] : 0.0f;
+            for (int s = 0; s < PC; ++s) {
+              const float w = expf(gt - gam[s * dlam + c]) * Kn[s * D + c];
+              ak[s] = fmaf(kt, w, ak[s]);
+              aq[s] = fmaf(qt, w, aq[s]);
+            }
+          }
+        }
+      } else {  // per-head decay: plain dot products, the ratio is applied below
+#pragma unroll 1
+        for (int i = 0; i < NI; ++i) {
+          const int c = lane + 32 * i;
+          if (c < D) {
+            const float kt = Kn[t * D + c], qt = Qn[t * D + c];
 #pragma unroll
-          for (int s = 0; s < PC; ++s) {
-            const float ks = Kn[s * D + c];
-            const float w = (dlam > 1) ? expf(gt - gam[s * dlam + c]) * ks : ks;
-            ak[s] = fmaf(kt, w, ak[s]);
-            aq[s] = fmaf(qt, w, aq[s]);
+            for (int s = 0; s < PC; ++s) {
+              const float ks = Kn[s * D + c];
+              ak[s] = fmaf(kt, ks, ak[s]);
+              aq[s] = fmaf(qt, ks, aq[s]);
+            }
           }
         }
       }
