@@ -102,9 +102,10 @@ __device__ __forceinline__ float prefill_conv(const DecodeParams& p, int b, int 
 }
 
 // EXT instances carry the fused conv, the KDA gate parametrisation and the output
-// epilogue; the others compile them out.
+// epilogue; the others compile them out.  At head size 128 shared memory admits one CTA
+// per SM, so the register budget is the whole 255; smaller heads keep two CTAs per SM.
 template <int D, bool EXT>
-__global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(NT, D == 128 ? 1 : 2) gdn_prefill_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int TCOL = D / 16;  // product tiles: 16 x 16 thread grid
   constexpr int NI = (D + 31) / 32;
@@ -417,7 +418,7 @@ __global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
         for (int i = 0; i < 4; ++i)
 #pragma unroll
           for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
-#pragma unroll 4
+#pragma unroll 16
         for (int c = 0; c < D; ++c) {
           const float4 a = *reinterpret_cast<const float4*>(KQt + c * KQS + row0);
           const float4 b0 = *reinterpret_cast<const float4*>(S + c * D + col0);
@@ -503,6 +504,10 @@ __global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
         }
         bc[t] = (x[0] + x[1]) + (x[2] + x[3]);
       }
+      if constexpr (D == 128) {
+#pragma unroll
+        for (int t = 0; t < PC; ++t) V[t * D + j] = bc[t];  // B; the readout follows below
+      } else {
 #pragma unroll
       for (int t = 0; t < PC; ++t) {
         V[t * D + j] = bc[t];  // B for the state update
@@ -515,6 +520,7 @@ __global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
         else if (t < n)
           p.o[((static_cast<size_t>(b) * T + t0 + t) * p.H + h) * D + j] = ot;
       }
+      }
     }
     // Khat = e^{gamma_C - gamma_s} k_s (rows past n hold zero keys)
     for (int i = tid; i < PC * D; i += NT) {
@@ -523,6 +529,43 @@ __global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
       Kt[i] = Kn[i] * expf(gam[(PC - 1) * dlam + gc] - gam[tt * dlam + gc]);
     }
     __syncthreads();
+
+    if constexpr (D == 128) {
+      // readout O = Y + P B over every thread (warp: 4 rows, lane: 4 columns)
+      const int r0 = warp * 4, c0 = lane * 4;
+      float acc[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 y = *reinterpret_cast<const float4*>(Y + (r0 + i) * D + c0);
+        acc[i][0] = y.x;
+        acc[i][1] = y.y;
+        acc[i][2] = y.z;
+        acc[i][3] = y.w;
+      }
+#pragma unroll 4
+      for (int s2 = 0; s2 < PC; ++s2) {
+        const float4 bv = *reinterpret_cast<const float4*>(V + s2 * D + c0);
+        const float bb[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float pv = P[(r0 + i) * PC + s2];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) acc[i][jj] = fmaf(pv, bb[jj], acc[i][jj]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int t = r0 + i;
+        if (epilogue) {
+          *reinterpret_cast<float4*>(Y + t * D + c0) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        } else if (t < n) {
+          float* orow = p.o + ((static_cast<size_t>(b) * T + t0 + t) * p.H + h) * D + c0;
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) orow[jj] = acc[i][jj];
+        }
+      }
+      if (epilogue) __syncthreads();  // the epilogue reads whole rows of Y
+    }
 
     // ---- KDA output epilogue: o <- o / sqrt(mean(o^2) + eps) * w * sigmoid(g) per row ---
     if (epilogue) {
@@ -548,7 +591,7 @@ __global__ void __launch_bounds__(NT) gdn_prefill_kernel(const DecodeParams p) {
       for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
-#pragma unroll 4
+#pragma unroll
       for (int s = 0; s < PC; ++s) {
         const float4 a0 = *reinterpret_cast<const float4*>(Kt + s * D + rg * 8);
         const float4 a1 = *reinterpret_cast<const float4*>(Kt + s * D + rg * 8 + 4);
