@@ -164,27 +164,35 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- traffic model
 
-def head_bytes(mode: str, n: int, w, klb=2, conv=False, ulb=4) -> int:
-    """Algorithmic DRAM bytes one decode launch moves per (request, head), following the
-    traffic model of the DeltaLog notes (Sec. 2.5, Eqs. (8)-(11)): common inputs and
-    outputs, the state read (and write for dense / merge), the log entries replayed
-    and written, and the decay metadata."""
+def head_bytes_rw(mode: str, n: int, w, klb=2, conv=False, ulb=4):
+    """Algorithmic DRAM (read, write) bytes one decode launch moves per (request, head),
+    following the traffic model of the DeltaLog notes (Sec. 2.5, Eqs. (8)-(11)): inputs and
+    output, the state read (and write for dense / merge), the n log entries replayed, the
+    entry an append writes, and the decay metadata."""
     D = w.dk
     e = 2 if w.qkv_bf16 else 4
     dlam = w.dlam
-    common = 3 * D * e + 4 * dlam + (0 if w.raw_value else 4) + 4 * D  # q,k,v + lambda + beta + o
+    rd = 3 * D * e + 4 * dlam + (0 if w.raw_value else 4)   # q, k, v, lambda, beta
     if w.kda_full:
-        common += 4 * D                                 # output-gate logits
+        rd += 4 * D                                         # output-gate logits
+    wr = 4 * D                                              # o
     if conv:
-        common += 3 * D * 3 * e * 2 + 3 * D * 16       # conv cache read + write, weights
+        rd += 3 * D * 3 * e + 3 * D * 16                    # conv cache, weights
+        wr += 3 * D * 3 * e                                 # conv cache shifted
     state = 4 * D * D
-    entry = D * klb + ulb * D + 4 * dlam                # one log position
+    entry = D * klb + ulb * D + 4 * dlam                    # one log position
     if mode == "dense":
-        return common + 2 * state
-    meta = 4 * dlam + 4                                 # ell and L read
+        return rd + state, wr + state
+    meta = 4 * dlam + 4                                     # ell and L read
     if mode == "append":
-        return common + state + n * entry + meta + entry + 4 * dlam + 4
-    return common + 2 * state + n * entry + meta + 4 * dlam + 4  # merge: base r+w, log read
+        return rd + state + n * entry + meta, wr + entry + 4 * dlam + 4
+    return rd + state + n * entry + meta, wr + state + 4 * dlam + 4  # merge: base r+w
+
+
+def head_bytes(mode: str, n: int, w, klb=2, conv=False, ulb=4) -> int:
+    """Algorithmic DRAM bytes (read + write) of one decode launch per (request, head)."""
+    r, wr = head_bytes_rw(mode, n, w, klb, conv, ulb)
+    return r + wr
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -364,6 +372,23 @@ def run_gpu(args, rank, local_rank, world):
                        "algorithmic_bytes_per_decode_step": nbytes / M,
                        "algorithmic_gbs": gbs, "frac_of_peak": gbs / peak}
     modes["speedup_deltalog_vs_dense"] = value / (du / dt)
+    # algorithmic read / write bytes per launch by phase (the DeltaLog notes' Fig. 8 split)
+    # and per decode step, with the write and total reductions of the log against dense
+    phases = {"dense": head_bytes_rw("dense", 0, w, klb, w.conv, ulb)}
+    if M > 1:
+        phases["append_L0"] = head_bytes_rw("append", 0, w, klb, w.conv, ulb)
+        phases[f"append_L{M - 2}"] = head_bytes_rw("append", M - 2, w, klb, w.conv, ulb)
+    phases[f"merge_L{M - 1}"] = head_bytes_rw("merge", M - 1, w, klb, w.conv, ulb)
+    cyc = [head_bytes_rw("append", n, w, klb, w.conv, ulb) for n in range(M - 1)] + \
+        [head_bytes_rw("merge", M - 1, w, klb, w.conv, ulb)]
+    step_r, step_w = sum(c[0] for c in cyc) * heads / M, sum(c[1] for c in cyc) * heads / M
+    dense_r, dense_w = phases["dense"][0] * heads, phases["dense"][1] * heads
+    modes["traffic"] = {
+        "per_launch": {k: {"read": v[0] * heads, "write": v[1] * heads} for k, v in phases.items()},
+        "per_decode_step": {f"deltalog_M{M}": {"read": step_r, "write": step_w},
+                            "dense": {"read": dense_r, "write": dense_w}},
+        "write_reduction": dense_w / step_w, "total_reduction": (dense_r + dense_w) / (step_r + step_w),
+        "source": "algorithmic model (measured DRAM counters in profiles/)"}
 
     # dominant kernel of the timed DeltaLog cycle: largest share of device time
     dom = max(per["deltalog"][1], key=lambda k: kernels[k]["total_ms"])
