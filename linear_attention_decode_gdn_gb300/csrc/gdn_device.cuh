@@ -41,23 +41,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-// Raises the transaction count of the current phase without arriving.
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-// Orders this thread's generic-proxy shared-memory accesses before later
-// asynchronous-proxy (TMA) accesses to the same buffers.
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // Named barrier 1 over the 256 compute threads (the copy-issuing warp never joins it).
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
@@ -84,18 +67,9 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   return pol;
 }
 
-// One TMA bulk copy global -> shared (no tensor map: a contiguous byte range).
-// dst, src 16-byte aligned; bytes a multiple of 16. Completion is signalled on
-// `bar` through the transaction count.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
-                                          uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
-
+// One TMA bulk copy global -> shared (no tensor map: a contiguous byte range) with an
+// L2 cache policy. dst, src 16-byte aligned; bytes a multiple of 16. Completion is
+// signalled on `bar` through the transaction count.
 __device__ __forceinline__ void bulk_load_hint(void* dst, const void* src, uint32_t bytes,
                                                uint64_t* bar, uint64_t policy) {
   asm volatile(
