@@ -471,3 +471,56 @@ def test_step_entry_with_requests_at_different_phases():
     assert len(set(lens[:, 0].tolist())) > 1  # phases really differ
     assert ls.status(v) == 0
     assert v.rel_err <= LOG_TOL, v.rel_err
+
+
+def test_cuda_graph_capture_of_a_cycle():
+    """One DeltaLog cycle (M calls of gdn_decode_step, launched with programmatic stream
+    serialisation) captured into a CUDA graph and replayed for three cycles, new inputs
+    copied into the captured buffers between replays; outputs and the base match the fp64
+    oracle's dense recurrence (the base equals the state after each merge)."""
+    B, H, D, M, cycles = 16, 8, 128, 4, 3
+    w = _custom("graph", B, H, D, M * cycles, seed=31)
+    dims = gdn.make_dims(B, H, D, num_slots=B, flags=gdn.QKV_BF16, log_capacity=M - 1)
+    pools = gdn.Pools.allocate(dims, deltalog=True)
+    log = pools.log()
+    slot = torch.arange(B, dtype=torch.int32, device="cuda")
+    bufs = [{n: torch.zeros((B, H, D), dtype=torch.bfloat16, device="cuda") for n in ("q", "k", "v")}
+            for _ in range(M)]
+    for b in bufs:
+        b.update(log_decay=torch.zeros((B, H, 1), device="cuda"), beta=torch.zeros((B, H), device="cuda"))
+    ins = [gdn.make_inputs(slot=slot, **b) for b in bufs]
+    o = torch.zeros((M, B, H, D), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        # one eager call configures the kernel attributes outside the capture; then reset
+        gdn.decode_step(dims, ins[0], pools.state, log, o[0], status, stream=stream)
+        gdn.slot_reset(dims, slot, B, log, None, pools.state, status, stream=stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for t in range(M):
+            gdn.decode_step(dims, ins[t], pools.state, log, o[t], status, stream=stream)
+    cfg = dict(batch=B, num_heads=H, dk=D, dv=D, num_slots=B, dlam=1, log_capacity=0,
+               flags=oracle.L2NORM, q_scale=1.0, l2_eps=1e-6)
+    ost = oracle.BatchState(B, H, D, D)
+    sl = np.arange(B, dtype=np.int32)
+    err = ref = 0.0
+    for c in range(cycles):
+        xs = [wl.step_inputs(w, c * M + t) for t in range(M)]
+        for b, x in zip(bufs, xs):
+            for n in ("q", "k", "v"):
+                b[n].copy_(torch.from_numpy(x[n + "_bits"].view(np.int16)).view(torch.bfloat16))
+            b["log_decay"].copy_(torch.from_numpy(x["lam"]))
+            b["beta"].copy_(torch.from_numpy(x["beta"]))
+        graph.replay()
+        torch.cuda.synchronize()
+        for t, x in enumerate(xs):
+            o_ref = oracle.step_batch(cfg, "dense", ost, sl, **{n: x[n].astype(np.float64) for n in ("q", "k", "v")},
+                                      lam=x["lam"].astype(np.float64), beta=x["beta"].astype(np.float64))
+            err = max(err, float(np.max(np.abs(o[t].cpu().numpy() - o_ref))))
+            ref = max(ref, float(np.max(np.abs(o_ref))))
+        base_err = float(np.max(np.abs(pools.state.cpu().numpy() - ost.S))) / float(np.max(np.abs(ost.S)))
+        assert base_err <= LOG_TOL, (c, base_err)
+    assert int(status.item()) == 0
+    assert err / ref <= LOG_TOL, err / ref
