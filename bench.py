@@ -459,14 +459,23 @@ def run_verify(args, w, flags, dev, stream, gdn, peak):
     acceptance count. Unit: positions x heads per second."""
     import torch
     B, H, D, T = w.batch, w.num_heads, w.dk, args.verify
-    if w.conv:
-        return {"unavailable": "the verify path runs the dense recurrence without the fused conv"}
     vflags = flags & ~(gdn.KLOG_PRENORM | gdn.ULOG_BF16 | gdn.GATE_KDA | gdn.OUT_NORM_GATE)
     rng = np.random.default_rng(w.seed + 77)
+    S = B * T
+    conv = {}
+    if w.conv:  # q, k, v from the conv of mixed_qkv through the widened window [S][channels][T+2]
+        conv["conv_w"] = torch.from_numpy(wl_conv_weights(w)).to(dev)
+        conv["conv_pool"] = torch.zeros((S, w.channels, T + 2), dtype=torch.bfloat16 if w.qkv_bf16
+                                        else torch.float32, device=dev)
     ring = []
     for t in range(RING):
-        x = {}
-        for n in ("q", "k", "v"):
+        x = dict(conv)
+        if w.conv:
+            a = rng.standard_normal((B, T, w.channels), dtype=np.float32)
+            bits, _ = wl_bf16(a)
+            x["mixed_qkv"] = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16) if w.qkv_bf16 \
+                else torch.from_numpy(a).to(dev)
+        for n in (() if w.conv else ("q", "k", "v")):
             a = rng.standard_normal((B, T, H, D), dtype=np.float32) * np.float32(1.0 if n == "v" else w.qk_mult)
             bits, _ = wl_bf16(a)
             x[n] = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16) if w.qkv_bf16 \
@@ -478,7 +487,6 @@ def run_verify(args, w, flags, dev, stream, gdn, peak):
             x["beta"] = torch.from_numpy((1 / (1 + np.exp(-b_raw))).astype(np.float32)).to(dev)
         acc = torch.from_numpy(rng.integers(1, T + 1, size=B).astype(np.int32)).to(dev)
         ring.append((gdn.make_inputs(**x), acc, x))
-    S = B * T
     dims = gdn.make_dims(B, H, D, num_slots=S, decay_per_key=w.decay_per_key, flags=vflags)
     pool = torch.zeros((S, H, D, D), dtype=torch.float32, device=dev)
     idx = torch.arange(S, dtype=torch.int32, device=dev).view(B, T)
@@ -505,6 +513,8 @@ def run_verify(args, w, flags, dev, stream, gdn, peak):
     el, units = reduce_timing(t0.elapsed_time(t1) / 1e3, B * H * T * calls, device=dev)
     e = 2 if w.qkv_bf16 else 4
     per_head = 4 * D * D * (1 + T) + T * (3 * D * e + 4 * w.dlam + (0 if w.raw_value else 4) + 4 * D) + 8
+    if w.conv:  # the window: three inputs read, T + 2 written, per channel; the weights
+        per_head += 3 * D * ((3 + T + 2) * e + 16)
     gbs = B * H * per_head * calls / el / 1e9
     return {"value": units / el, "unit": "positions x heads / s", "positions_per_request": T,
             "us_per_call": el / calls * 1e6, "calls": calls, "launches": calls + max(3, args.warmup),
@@ -585,6 +595,11 @@ def run_prefill(args, w, flags, dev, stream, gdn):
 def wl_bf16(a):
     from linear_attention_decode_gdn_gb300 import workloads as wl
     return wl.bf16_round(a)
+
+
+def wl_conv_weights(w):
+    from linear_attention_decode_gdn_gb300 import workloads as wl
+    return wl.conv_weights(w)
 
 
 class _Cudart:
