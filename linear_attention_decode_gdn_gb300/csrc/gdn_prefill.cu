@@ -28,6 +28,8 @@ struct PrefillLayout {
 // [Ktil; Qtil] stored transposed for the first product at head size 128: row c holds the
 // 2*PC entries of key channel c, padded to a 16-byte multiple
 constexpr int KQS = 2 * PC + 4;
+// A is stored column-major with padded columns for the right-looking substitution
+constexpr int ATS = PC + 4;
 
 __host__ __device__ inline PrefillLayout prefill_layout(int D, int dlam) {
   PrefillLayout L{};
@@ -44,8 +46,8 @@ __host__ __device__ inline PrefillLayout prefill_layout(int D, int dlam) {
   off += static_cast<uint32_t>(PC * D * 4);
   L.Y = off;    // Qtil S0
   off += static_cast<uint32_t>(PC * D * 4);
-  L.A = off;    // [PC][PC]
-  off += static_cast<uint32_t>(PC * PC * 4);
+  L.A = off;    // column-major: A[s * ATS + t] (row t, column s), columns padded to ATS
+  off += static_cast<uint32_t>(PC * ATS * 4);
   L.P = off;
   off += static_cast<uint32_t>(PC * PC * 4);
   L.gam = off;  // cumulative log-decays [PC][dlam]
@@ -337,7 +339,7 @@ __global__ void __launch_bounds__(NT, D == 128 ? 1 : 2) gdn_prefill_kernel(const
         }
         const float a_ts = transpose_reduce(ak, lane);
         const float p_ts = transpose_reduce(aq, lane);
-        A[t * PC + lane] = (lane < t) ? bet[t] * a_ts : 0.0f;
+        A[lane * ATS + t] = (lane < t) ? bet[t] * a_ts : 0.0f;
         P[t * PC + lane] = (lane <= t) ? p_ts : 0.0f;
       }
     } else
@@ -378,7 +380,7 @@ __global__ void __launch_bounds__(NT, D == 128 ? 1 : 2) gdn_prefill_kernel(const
       const float a_ts = transpose_reduce(ak, lane);
       const float p_ts = transpose_reduce(aq, lane);
       const float r = (dlam == 1) ? expf(gam[t] - gam[lane]) : 1.0f;  // per-head decay ratio
-      A[t * PC + lane] = (lane < t) ? bet[t] * (a_ts * r) : 0.0f;
+      A[lane * ATS + t] = (lane < t) ? bet[t] * (a_ts * r) : 0.0f;
       P[t * PC + lane] = (lane <= t) ? p_ts * r : 0.0f;
     }
     __syncthreads();
@@ -493,16 +495,18 @@ __global__ void __launch_bounds__(NT, D == 128 ? 1 : 2) gdn_prefill_kernel(const
     // ---- (I + A) B = R by forward substitution, then the readout; column-parallel -------
     if (tid < D) {
       const int j = tid;
+      // right-looking: once row s is final it is folded into every later row at once, so
+      // each step has up to 31 independent FMAs and the chain from row to row is one FMA
       float bc[PC];
-      // four partial sums per row shorten the dependent FMA chains
 #pragma unroll
-      for (int t = 0; t < PC; ++t) {
-        float x[4] = {V[t * D + j], 0.0f, 0.0f, 0.0f};
-        if (!plain) {
+      for (int t = 0; t < PC; ++t) bc[t] = V[t * D + j];
+      if (!plain) {
 #pragma unroll
-          for (int s = 0; s < t; ++s) x[s & 3] = fmaf(-A[t * PC + s], bc[s], x[s & 3]);
+        for (int s = 0; s < PC - 1; ++s) {
+          const float bs = bc[s];
+#pragma unroll
+          for (int t = s + 1; t < PC; ++t) bc[t] = fmaf(-A[s * ATS + t], bs, bc[t]);
         }
-        bc[t] = (x[0] + x[1]) + (x[2] + x[3]);
       }
       if constexpr (D == 128) {
 #pragma unroll
