@@ -244,9 +244,14 @@ __global__ void __launch_bounds__(NT, D == 128 ? 1 : 2) gdn_prefill_kernel(const
         for (int i = 0; i < NI; ++i) {
           const int c = lane + 32 * i;
           if (c < D) {
-            Qn[tt * D + c] = qv[u][i] * qsc;
-            Kn[tt * D + c] = kv[u][i] * kinv;
+            const float qn = qv[u][i] * qsc, kn = kv[u][i] * kinv;
+            Qn[tt * D + c] = qn;
+            Kn[tt * D + c] = kn;
             V[tt * D + c] = vv[u][i];
+            if (D == 128 && dlam == 1) {  // channel-major copies: pair sums, then Ktil / Qtil
+              KQt[c * KQS + tt] = kn;
+              KQt[c * KQS + PC + tt] = qn;
+            }
           }
           if (c < dlam) gam[tt * dlam + c] = lv[u][i];  // gate inputs; transformed below
         }
@@ -342,6 +347,35 @@ __global__ void __launch_bounds__(NT, D == 128 ? 1 : 2) gdn_prefill_kernel(const
         A[lane * ATS + t] = (lane < t) ? bet[t] * a_ts : 0.0f;
         P[t * PC + lane] = (lane <= t) ? p_ts : 0.0f;
       }
+    } else if (D == 128 && dlam == 1) {
+      // per-head decay on the channel-major copies: warp w takes rows 4w .. 4w+3, lane s the
+      // column; per channel one broadcast float4 of k_t, one of q_t and k_s of the lane, and
+      // no reduction across lanes
+      const int tr = warp * 4;
+      float aa[4] = {0.0f, 0.0f, 0.0f, 0.0f}, ap[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 8
+      for (int c = 0; c < D; ++c) {
+        const float4 kt = *reinterpret_cast<const float4*>(KQt + c * KQS + tr);
+        const float4 qt = *reinterpret_cast<const float4*>(KQt + c * KQS + PC + tr);
+        const float ks = KQt[c * KQS + lane];
+        aa[0] = fmaf(kt.x, ks, aa[0]);
+        aa[1] = fmaf(kt.y, ks, aa[1]);
+        aa[2] = fmaf(kt.z, ks, aa[2]);
+        aa[3] = fmaf(kt.w, ks, aa[3]);
+        ap[0] = fmaf(qt.x, ks, ap[0]);
+        ap[1] = fmaf(qt.y, ks, ap[1]);
+        ap[2] = fmaf(qt.z, ks, ap[2]);
+        ap[3] = fmaf(qt.w, ks, ap[3]);
+      }
+      float av[4];
+#pragma unroll
+      for (int r4 = 0; r4 < 4; ++r4) {
+        const int t = tr + r4;
+        const float r = expf(gam[t] - gam[lane]);  // per-head decay ratio
+        av[r4] = (lane < t) ? bet[t] * (aa[r4] * r) : 0.0f;
+        P[t * PC + lane] = (lane <= t) ? ap[r4] * r : 0.0f;
+      }
+      *reinterpret_cast<float4*>(A + lane * ATS + tr) = make_float4(av[0], av[1], av[2], av[3]);
     } else
     for (int t = warp; t < PC; t += NW) {
       float ak[PC], aq[PC];
@@ -387,12 +421,19 @@ __global__ void __launch_bounds__(NT, D == 128 ? 1 : 2) gdn_prefill_kernel(const
 
     // ---- Ktil = e^{gamma} k, Qtil = e^{gamma} q ----------------------------------------
     if constexpr (D == 128) {
-      // transposed: KQt[c][t] = Ktil_t[c], KQt[c][PC + t] = Qtil_t[c]
-      for (int i = tid; i < PC * D; i += NT) {
-        const int tt = i / D, c = i - tt * D;
-        const float e = expf(gam[tt * dlam + (dlam > 1 ? c : 0)]);
-        KQt[c * KQS + tt] = Kn[i] * e;
-        KQt[c * KQS + PC + tt] = Qn[i] * e;
+      // KQt[c][t] = Ktil_t[c], KQt[c][PC + t] = Qtil_t[c]
+      if (dlam == 1) {  // in place on the channel-major copies
+        for (int i = tid; i < 2 * PC * D; i += NT) {
+          const int c = i / (2 * PC), col = i - c * (2 * PC);
+          KQt[c * KQS + col] *= expf(gam[col & (PC - 1)]);
+        }
+      } else {          // transposed from the row-major tiles
+        for (int i = tid; i < PC * D; i += NT) {
+          const int tt = i / D, c = i - tt * D;
+          const float e = expf(gam[tt * dlam + c]);
+          KQt[c * KQS + tt] = Kn[i] * e;
+          KQt[c * KQS + PC + tt] = Qn[i] * e;
+        }
       }
     } else {
       for (int i = tid; i < PC * D; i += NT) {
