@@ -238,8 +238,10 @@ __global__ void __launch_bounds__(NT, D == 128 ? 1 : 2) gdn_prefill_kernel(const
         }
         sq = warp_sum(sq);
         sk = warp_sum(sk);
-        const float qsc = (l2 ? 1.0f / sqrtf(sq + p.l2_eps) : 1.0f) * p.q_scale;
-        const float kinv = l2 ? 1.0f / sqrtf(sk + p.l2_eps) : 1.0f;
+        // one reciprocal square root per vector (a few ulp; the decode kernels' exact
+        // sqrt-and-divide would cost most of this stage)
+        const float qsc = (l2 ? rsqrtf(sq + p.l2_eps) : 1.0f) * p.q_scale;
+        const float kinv = l2 ? rsqrtf(sk + p.l2_eps) : 1.0f;
 #pragma unroll
         for (int i = 0; i < NI; ++i) {
           const int c = lane + 32 * i;
