@@ -61,6 +61,23 @@ __host__ __device__ inline PrefillLayout prefill_layout(int D, int dlam) {
   return L;
 }
 
+// Two FP32 lanes in one 64-bit register (low half first) and the packed FMA of sm_100+
+// (fma.rn.f32x2): one instruction, two FMAs, each rounded as fmaf rounds.
+using f2 = unsigned long long;
+__device__ __forceinline__ f2 f2_splat(float x) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(f2 v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
+  f2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 // v[i] of every lane -> lane l holds the sum over lanes of v[l] (32 values, 31 shuffles).
 __device__ __forceinline__ float transpose_reduce(float (&v)[PC], int lane) {
 #pragma unroll
@@ -458,22 +475,24 @@ __global__ void __launch_bounds__(NT, D == 128 ? 1 : 2) gdn_prefill_kernel(const
       const int row0 = wb * 16 + rgl * 4;
       const int col0 = (warp & 1) * 64 + (lane & 7) * 4;
       if (!plain || wb >= 2) {
-        float acc[4][8];
+        f2 acc2[4][4];  // [row][column pair]: columns col0 + {0,1}, {2,3}, 32 + {0,1}, 32 + {2,3}
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-          for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+          for (int j = 0; j < 4; ++j) acc2[i][j] = 0ull;
 #pragma unroll 16
         for (int c = 0; c < D; ++c) {
           const float4 a = *reinterpret_cast<const float4*>(KQt + c * KQS + row0);
-          const float4 b0 = *reinterpret_cast<const float4*>(S + c * D + col0);
-          const float4 b1 = *reinterpret_cast<const float4*>(S + c * D + col0 + 32);
+          const ulonglong2 b0 = *reinterpret_cast<const ulonglong2*>(S + c * D + col0);
+          const ulonglong2 b1 = *reinterpret_cast<const ulonglong2*>(S + c * D + col0 + 32);
           const float av[4] = {a.x, a.y, a.z, a.w};
-          const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+          const f2 bv[4] = {b0.x, b0.y, b1.x, b1.y};
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
+          for (int i = 0; i < 4; ++i) {
+            const f2 a2 = f2_splat(av[i]);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+            for (int j = 0; j < 4; ++j) acc2[i][j] = f2_fma(a2, bv[j], acc2[i][j]);
+          }
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -481,7 +500,9 @@ __global__ void __launch_bounds__(NT, D == 128 ? 1 : 2) gdn_prefill_kernel(const
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
             const int col = col0 + 32 * hf;
-            const float* ac = acc[i] + 4 * hf;
+            float ac[4];
+            f2_unpack(acc2[i][2 * hf], ac[0], ac[1]);
+            f2_unpack(acc2[i][2 * hf + 1], ac[2], ac[3]);
             if (row < PC) {
               float4 x = *reinterpret_cast<const float4*>(V + row * D + col);
               const float be = bet[row];
@@ -633,23 +654,25 @@ __global__ void __launch_bounds__(NT, D == 128 ? 1 : 2) gdn_prefill_kernel(const
     if constexpr (D == 128) {
       // lane: rows 8*rg .. +8, columns 4*cg .. +4 and 64 + 4*cg .. +4 (contiguous float4 runs
       // across the 16 lanes of a row group, for the operand loads and the state update)
-      float acc[8][8];
+      f2 acc2[8][4];  // [row][column pair]: columns 4cg + {0,1}, {2,3}, 64 + 4cg + {0,1}, {2,3}
 #pragma unroll
       for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
-#pragma unroll
+        for (int j = 0; j < 4; ++j) acc2[i][j] = 0ull;
+#pragma unroll 8
       for (int s = 0; s < PC; ++s) {
         const float4 a0 = *reinterpret_cast<const float4*>(Kt + s * D + rg * 8);
         const float4 a1 = *reinterpret_cast<const float4*>(Kt + s * D + rg * 8 + 4);
-        const float4 b0 = *reinterpret_cast<const float4*>(V + s * D + cg * 4);
-        const float4 b1 = *reinterpret_cast<const float4*>(V + s * D + 64 + cg * 4);
+        const ulonglong2 b0 = *reinterpret_cast<const ulonglong2*>(V + s * D + cg * 4);
+        const ulonglong2 b1 = *reinterpret_cast<const ulonglong2*>(V + s * D + 64 + cg * 4);
         const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        const f2 bv[4] = {b0.x, b0.y, b1.x, b1.y};
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < 8; ++i) {
+          const f2 a2 = f2_splat(av[i]);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+          for (int j = 0; j < 4; ++j) acc2[i][j] = f2_fma(a2, bv[j], acc2[i][j]);
+        }
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -658,11 +681,14 @@ __global__ void __launch_bounds__(NT, D == 128 ? 1 : 2) gdn_prefill_kernel(const
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           float* sp = S + r * D + 64 * hf + cg * 4;
+          float ac[4];
+          f2_unpack(acc2[i][2 * hf], ac[0], ac[1]);
+          f2_unpack(acc2[i][2 * hf + 1], ac[2], ac[3]);
           float4 x = *reinterpret_cast<const float4*>(sp);
-          x.x = fmaf(dC, x.x, acc[i][4 * hf + 0]);
-          x.y = fmaf(dC, x.y, acc[i][4 * hf + 1]);
-          x.z = fmaf(dC, x.z, acc[i][4 * hf + 2]);
-          x.w = fmaf(dC, x.w, acc[i][4 * hf + 3]);
+          x.x = fmaf(dC, x.x, ac[0]);
+          x.y = fmaf(dC, x.y, ac[1]);
+          x.z = fmaf(dC, x.z, ac[2]);
+          x.w = fmaf(dC, x.w, ac[3]);
           *reinterpret_cast<float4*>(sp) = x;
         }
       }
