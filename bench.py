@@ -100,7 +100,7 @@ def kernel_source_hash() -> str:
 def profiled_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the
     current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    path = os.path.join(ROOT, "profiles", "decode_traffic_headline.txt")
     if not os.path.exists(path):
         return None
     src = kernel_source_hash()
