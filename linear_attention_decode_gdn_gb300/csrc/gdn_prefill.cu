@@ -22,7 +22,7 @@ namespace {
 constexpr int PC = 32;  // tokens per chunk (one warp's width: the pair reductions map s to lanes)
 
 struct PrefillLayout {
-  uint32_t S, Kn, Qn, V, Kt, Y, A, P, gam, bet, KQt, total;
+  uint32_t S, Kn, Qn, V, Kt, Y, A, P, gam, bet, eg, KQt, total;
 };
 
 // [Ktil; Qtil] stored transposed for the first product at head size 128: row c holds the
@@ -54,6 +54,8 @@ __host__ __device__ inline PrefillLayout prefill_layout(int D, int dlam) {
   off += static_cast<uint32_t>(PC * dlam * 4);
   L.bet = off;  // [PC]
   off += static_cast<uint32_t>(PC * 4);
+  L.eg = off;   // per-head decay: e^{gamma_t} [PC], then e^{gamma_C - gamma_t} [PC]
+  off += static_cast<uint32_t>(2 * PC * 4);
   off = (off + 15u) & ~15u;
   L.KQt = off;  // [D][KQS] (head size 128 only)
   off += (D == 128) ? static_cast<uint32_t>(D * KQS * 4) : 0u;
@@ -169,6 +171,8 @@ __global__ void __launch_bounds__(NT, D == 128 ? 1 : 2) gdn_prefill_kernel(const
   float* P = reinterpret_cast<float*>(smem + L.P);
   float* gam = reinterpret_cast<float*>(smem + L.gam);
   float* bet = reinterpret_cast<float*>(smem + L.bet);
+  float* eg = reinterpret_cast<float*>(smem + L.eg);
+  float* ek = eg + PC;
   float* KQt = reinterpret_cast<float*>(smem + L.KQt);
 
   float* Sg = p.state + (static_cast<size_t>(slot) * p.H + h) * static_cast<size_t>(D * D);
@@ -322,6 +326,12 @@ __global__ void __launch_bounds__(NT, D == 128 ? 1 : 2) gdn_prefill_kernel(const
       }
     }
     const bool split = (dlam > 1) && !__syncthreads_or(!split_ok);
+    // per-head decay: its 32 distinct factors e^{gamma_t} and e^{gamma_C - gamma_t}, once (read
+    // after the barrier that ends the pair sums)
+    if (dlam == 1 && warp == 0) {
+      eg[lane] = expf(gam[lane]);
+      ek[lane] = expf(gam[PC - 1] - gam[lane]);
+    }
 
     // column factors of the split: Km16[s][c] = k_s[c] e^{gamma_16 - gamma_s} (all s, in
     // the Khat buffer) and Km0[s][c] = k_s[c] e^{gamma_0 - gamma_s} (s < 16, in Y); both
@@ -444,7 +454,7 @@ __global__ void __launch_bounds__(NT, D == 128 ? 1 : 2) gdn_prefill_kernel(const
       if (dlam == 1) {  // in place on the channel-major copies
         for (int i = tid; i < 2 * PC * D; i += NT) {
           const int c = i / (2 * PC), col = i - c * (2 * PC);
-          KQt[c * KQS + col] *= expf(gam[col & (PC - 1)]);
+          KQt[c * KQS + col] *= eg[col & (PC - 1)];
         }
       } else {          // transposed from the row-major tiles
         for (int i = tid; i < PC * D; i += NT) {
@@ -457,7 +467,7 @@ __global__ void __launch_bounds__(NT, D == 128 ? 1 : 2) gdn_prefill_kernel(const
     } else {
       for (int i = tid; i < PC * D; i += NT) {
         const int tt = i / D, c = i - tt * D;
-        const float e = expf(gam[tt * dlam + (dlam > 1 ? c : 0)]);
+        const float e = (dlam > 1) ? expf(gam[tt * dlam + c]) : eg[tt];
         Kt[i] = Kn[i] * e;
         Qn[i] *= e;
       }
@@ -594,7 +604,7 @@ __global__ void __launch_bounds__(NT, D == 128 ? 1 : 2) gdn_prefill_kernel(const
     for (int i = tid; i < PC * D; i += NT) {
       const int tt = i / D, c = i - tt * D;
       const int gc = (dlam > 1) ? c : 0;
-      Kt[i] = Kn[i] * expf(gam[(PC - 1) * dlam + gc] - gam[tt * dlam + gc]);
+      Kt[i] = Kn[i] * ((dlam > 1) ? expf(gam[(PC - 1) * dlam + gc] - gam[tt * dlam + gc]) : ek[tt]);
     }
     __syncthreads();
 
@@ -677,7 +687,7 @@ __global__ void __launch_bounds__(NT, D == 128 ? 1 : 2) gdn_prefill_kernel(const
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int r = rg * 8 + i;
-        const float dC = expf(gam[(PC - 1) * dlam + (dlam > 1 ? r : 0)]);
+        const float dC = (dlam > 1) ? expf(gam[(PC - 1) * dlam + r]) : eg[PC - 1];
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           float* sp = S + r * D + 64 * hf + cg * 4;
@@ -713,7 +723,7 @@ __global__ void __launch_bounds__(NT, D == 128 ? 1 : 2) gdn_prefill_kernel(const
 #pragma unroll
       for (int i = 0; i < TCOL; ++i) {
         const int r = rg * TCOL + i;
-        const float dC = expf(gam[(PC - 1) * dlam + (dlam > 1 ? r : 0)]);
+        const float dC = (dlam > 1) ? expf(gam[(PC - 1) * dlam + r]) : eg[PC - 1];
 #pragma unroll
         for (int j = 0; j < TCOL; ++j) {
           const int col = cg * TCOL + j;
