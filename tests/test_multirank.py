@@ -50,3 +50,23 @@ def test_reduce_timing_single_process_is_identity():
     sys.path.insert(0, ROOT)
     import bench
     assert bench.reduce_timing(1.5, 7.0) == (1.5, 7.0)
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    """Under torchrun the reference arm (the CPU oracle) runs and prints on rank 0 alone; the
+    other ranks exit 0 without work or output (no process group is needed for it)."""
+    import json
+    import subprocess
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "1"]
+    outs = {}
+    for rank in (1, 0):
+        env = dict(os.environ, WORLD_SIZE="2", RANK=str(rank), LOCAL_RANK=str(rank))
+        r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+        assert r.returncode == 0, r.stderr[-2000:]
+        outs[rank] = r.stdout
+    assert outs[1].strip() == ""
+    lines = [ln for ln in outs[0].splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
