@@ -172,3 +172,37 @@ def test_verify_validation_rejects_before_launch(gdn):
             _abi.GDN_ERR_UNSUPPORTED)
     # an empty batch is a no-op
     gdn.decode_verify(gdn.make_dims(0, 2, 64, num_slots=8), 4, ins, fake, fake, fake, fake, stream=0)
+
+
+def test_prefill_validation_rejects_before_launch(gdn):
+    from linear_attention_decode_gdn_gb300 import _abi
+    fake = 1 << 20  # never dereferenced: every call below fails validation first
+    ok = gdn.make_inputs(q=fake, k=fake, v=fake, log_decay=fake, slot=fake)
+    d = gdn.make_dims(2, 2, 64, num_slots=8)
+    _expect(gdn, lambda: gdn.prefill(d, -1, ok, fake, fake, stream=0), _abi.GDN_ERR_INVALID_ARG)
+    for flag in (gdn.KLOG_FP32, gdn.ULOG_BF16, gdn.KLOG_PRENORM):
+        dd = gdn.make_dims(2, 2, 64, num_slots=8, flags=flag)
+        _expect(gdn, lambda: gdn.prefill(dd, 8, ok, fake, fake, stream=0), _abi.GDN_ERR_UNSUPPORTED)
+    # required inputs: slot, log_decay, and q/k/v or (with the fused conv) mixed_qkv, conv_w, conv_pool
+    _expect(gdn, lambda: gdn.prefill(d, 8, gdn.make_inputs(q=fake, k=fake, v=fake, log_decay=fake), fake, fake,
+                                     stream=0), _abi.GDN_ERR_INVALID_ARG)
+    _expect(gdn, lambda: gdn.prefill(d, 8, gdn.make_inputs(q=fake, k=fake, log_decay=fake, slot=fake), fake, fake,
+                                     stream=0), _abi.GDN_ERR_INVALID_ARG)
+    dc = gdn.make_dims(2, 2, 64, num_slots=8, flags=gdn.FUSE_CONV | gdn.QKV_BF16)
+    _expect(gdn, lambda: gdn.prefill(dc, 8, ok, fake, fake, stream=0), _abi.GDN_ERR_INVALID_ARG)
+    mis = gdn.make_inputs(mixed_qkv=fake + 2, conv_w=fake, conv_pool=fake, log_decay=fake, slot=fake)
+    _expect(gdn, lambda: gdn.prefill(dc, 8, mis, fake, fake, stream=0), _abi.GDN_ERR_UNSUPPORTED)
+    # the KDA gate needs A_log and dt_bias; the output epilogue needs the gate logits
+    dk = gdn.make_dims(2, 2, 64, num_slots=8, flags=gdn.GATE_KDA)
+    _expect(gdn, lambda: gdn.prefill(dk, 8, ok, fake, fake, stream=0), _abi.GDN_ERR_INVALID_ARG)
+    de = gdn.make_dims(2, 2, 64, num_slots=8, flags=gdn.OUT_NORM_GATE)
+    _expect(gdn, lambda: gdn.prefill(de, 8, ok, fake, fake, stream=0), _abi.GDN_ERR_INVALID_ARG)
+    # pools: present and 16-byte aligned
+    _expect(gdn, lambda: gdn.prefill(d, 8, ok, None, fake, stream=0), _abi.GDN_ERR_INVALID_ARG)
+    _expect(gdn, lambda: gdn.prefill(d, 8, ok, fake + 4, fake, stream=0), _abi.GDN_ERR_UNSUPPORTED)
+    # head sizes other than 16/32/64/128 are not built
+    _expect(gdn, lambda: gdn.prefill(gdn.make_dims(2, 2, 96, num_slots=8), 8, ok, fake, fake, stream=0),
+            _abi.GDN_ERR_UNSUPPORTED)
+    # an empty batch or an empty prompt is a no-op
+    gdn.prefill(gdn.make_dims(0, 2, 64, num_slots=8), 8, ok, fake, fake, stream=0)
+    gdn.prefill(d, 0, ok, fake, fake, stream=0)
