@@ -351,6 +351,7 @@ __global__ void __launch_bounds__(NT, D == 128 ? 1 : 2) gdn_prefill_kernel(const
 
     // ---- A (strictly lower, times beta_t) and P (lower with the diagonal) --------------
     // warp w takes rows t = w, w + 8, ...; lane = key channel; the pair sums end in lane s
+    // (a per-head decay at head size 128 uses the channel-major copies instead, below)
     if (split) {
       for (int t = warp; t < PC; t += NW) {
         float ak[PC], aq[PC];
@@ -566,7 +567,8 @@ __global__ void __launch_bounds__(NT, D == 128 ? 1 : 2) gdn_prefill_kernel(const
     }
     __syncthreads();
 
-    // ---- (I + A) B = R by forward substitution, then the readout; column-parallel -------
+    // ---- (I + A) B = R by forward substitution (column-parallel), then the readout -------
+    // (a register-tiled product over every thread at head size 128, after the barrier)
     if (tid < D) {
       const int j = tid;
       // right-looking: once row s is final it is folded into every later row at once, so
