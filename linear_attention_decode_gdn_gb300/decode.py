@@ -137,7 +137,9 @@ class Pools:
     length: object | None
 
     @classmethod
-    def allocate(cls, dims: Dims, device="cuda", conv=False, deltalog=False):
+    def allocate(cls, dims: Dims, device="cuda", conv=False, deltalog=False, verify_tokens=None):
+        """conv: the conv cache [slots][channels][3] (decode, prefill); with verify_tokens = T
+        instead the widened window [slots][channels][T + 2] of gdn_decode_verify."""
         import torch
         S, H, dk, dv = dims.num_slots, dims.num_heads, dims.dk, dims.dv
         dlam = dk if dims.decay_per_key else 1
@@ -147,7 +149,8 @@ class Pools:
         if conv:
             ch = 2 * H * dk + H * dv
             cdt = torch.bfloat16 if dims.flags & _abi.QKV_BF16 else torch.float32
-            conv_pool = torch.zeros((S, ch, 3), dtype=cdt, device=device)
+            width = 3 if verify_tokens is None else int(verify_tokens) + 2
+            conv_pool = torch.zeros((S, ch, width), dtype=cdt, device=device)
         k_log = u_log = lam_log = ell = length = None
         if deltalog:
             kdt = torch.float32 if dims.flags & _abi.KLOG_FP32 else torch.bfloat16

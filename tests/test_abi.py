@@ -206,3 +206,21 @@ def test_prefill_validation_rejects_before_launch(gdn):
     # an empty batch or an empty prompt is a no-op
     gdn.prefill(gdn.make_dims(0, 2, 64, num_slots=8), 8, ok, fake, fake, stream=0)
     gdn.prefill(d, 0, ok, fake, fake, stream=0)
+
+
+def test_pools_shapes(gdn):
+    """Pools.allocate sizes every pool as include/gdn.h documents it (device-independent)."""
+    import torch
+    d = gdn.make_dims(3, 2, 16, num_slots=5, flags=gdn.QKV_BF16, log_capacity=3, decay_per_key=True)
+    p = gdn.Pools.allocate(d, device="cpu", conv=True, deltalog=True)
+    assert tuple(p.state.shape) == (5, 2, 16, 16) and p.state.dtype == torch.float32
+    assert tuple(p.conv.shape) == (5, 3 * 2 * 16, 3) and p.conv.dtype == torch.bfloat16
+    assert tuple(p.k_log.shape) == (5, 2, 3, 16) and p.k_log.dtype == torch.bfloat16
+    assert tuple(p.u_log.shape) == (5, 2, 3, 16) and p.u_log.dtype == torch.float32
+    assert tuple(p.lam_log.shape) == (5, 2, 3, 16) and tuple(p.ell.shape) == (5, 2, 16)
+    assert tuple(p.length.shape) == (5, 2) and p.length.dtype == torch.int32
+    v = gdn.Pools.allocate(gdn.make_dims(3, 2, 16, num_slots=5), device="cpu", conv=True, verify_tokens=4)
+    assert tuple(v.conv.shape) == (5, 96, 6) and v.conv.dtype == torch.float32
+    r = gdn.Pools.allocate(gdn.make_dims(3, 2, 16, num_slots=5, flags=gdn.ULOG_BF16 | gdn.KLOG_FP32,
+                                         log_capacity=2), device="cpu", deltalog=True)
+    assert r.u_log.dtype == torch.bfloat16 and r.k_log.dtype == torch.float32
