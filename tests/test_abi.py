@@ -224,3 +224,25 @@ def test_pools_shapes(gdn):
     r = gdn.Pools.allocate(gdn.make_dims(3, 2, 16, num_slots=5, flags=gdn.ULOG_BF16 | gdn.KLOG_FP32,
                                          log_capacity=2), device="cpu", deltalog=True)
     assert r.u_log.dtype == torch.bfloat16 and r.k_log.dtype == torch.float32
+
+
+def test_binding_constants_match_the_header():
+    """Every return code, status bit and flag #defined in include/gdn.h has the same value in
+    the Python binding (the binding copies them; this catches drift)."""
+    from linear_attention_decode_gdn_gb300 import _abi
+    text = open(HEADER).read()
+    defs = {}
+    for name, expr in re.findall(r"^#define (GDN_\w+) ([^/\n]+)", text, flags=re.M):
+        expr = expr.strip()
+        m = re.fullmatch(r"\(1u << (\d+)\)", expr)
+        if m:
+            defs[name] = 1 << int(m.group(1))
+        elif re.fullmatch(r"(0x[0-9a-fA-F]+|\d+)u?", expr):
+            defs[name] = int(expr.rstrip("u"), 0)
+    assert len(defs) >= 20, sorted(defs)
+    for name, value in defs.items():
+        if name in ("GDN_H", "GDN_API_VERSION"):
+            continue
+        py = name[len("GDN_"):]
+        assert hasattr(_abi, py) or hasattr(_abi, name), name
+        assert getattr(_abi, py, getattr(_abi, name, None)) == value, (name, value)
