@@ -14,9 +14,14 @@ already resident in HBM (a 16-step ring of pre-generated inputs). The state
 
 Also reported: the dense mode on the same inputs, per-kernel CUDA-event
 durations with the algorithmic bytes each launch moves (roofline against the
-measured HBM copy bandwidth), an end-to-end figure through the public API with
-pinned host buffers, the SM clocks sampled during the timed region, and the
-fp64 CPU oracle timed on the host cores (a baseline, not the target).
+measured HBM copy bandwidth, and the fraction of the nominal ~8 TB/s beside it),
+the read / write traffic by phase and its reduction against dense (algorithmic
+model, and ncu-measured when a capture of the current kernel sources is
+committed), an end-to-end figure through the public API with pinned host
+buffers, the SM clocks sampled during the timed region, dense-vs-M sweeps over
+the suite's decode workloads, the chunked prefill and the speculative-decoding
+verify on the same shape, and the fp64 CPU oracle timed on the host cores (a
+baseline, not the target).
 
 ``--impl reference`` times the fp64 CPU oracle alone on the same metric.
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
@@ -43,6 +48,8 @@ METRIC = "GDN decode head-steps/s and achieved HBM GB/s (% of GB300 peak), dense
 UNIT = "head-steps/s"
 RING = 16
 FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 126 * 2**20   # GB300 L2 (~126 MiB)
+SPEC_HBM_GBS = 8000.0   # nominal HBM3e bandwidth of a GB300 (~8 TB/s), reported beside the measured peak
 KERNEL_SOURCES = ("gdn_decode.cu", "gdn_device.cuh", "gdn_internal.h")
 
 
@@ -95,22 +102,6 @@ def kernel_source_hash() -> str:
             code = re.sub(r"//[^\n]*", "", f.read())
         h.update(" ".join(code.split()).encode())
     return h.hexdigest()[:16]
-
-
-def profiled_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "decode_traffic_headline.txt")
-    if not os.path.exists(path):
-        return None
-    src = kernel_source_hash()
-    for line in open(path):
-        if line.startswith("#") or not line.strip():
-            continue
-        f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
-        if f.get("kernel") == kernel and f.get("workload") == workload and f.get("src") == src:
-            return float(f["dram_bytes_per_launch"])
-    return None
 
 
 class ClockSampler:
@@ -197,6 +188,247 @@ def head_bytes(mode: str, n: int, w, klb=2, conv=False, ulb=4) -> int:
 
 # ----------------------------------------------------------------------------- GPU arm
 
+def decode_flags(gdn, w, klog_prenorm=False) -> int:
+    flags = (gdn.QKV_BF16 if w.qkv_bf16 else 0) | (gdn.FUSE_CONV if w.conv else 0)
+    if klog_prenorm:
+        flags |= gdn.KLOG_PRENORM
+    if w.raw_value:  # the RWKV6 instantiation: b = v (beta NULL), raw q/k, bf16 value log
+        flags |= gdn.PLAIN_UPDATE | gdn.NO_QK_L2NORM | gdn.ULOG_BF16
+    if w.kda_full:   # the KDA gate parametrisation and output epilogue
+        flags |= gdn.GATE_KDA | gdn.OUT_NORM_GATE
+    return flags
+
+
+class DecodeRunner:
+    """One workload's decode launches through the C ABI: a ring of pre-generated decode
+    steps resident in HBM, the dense state pool and one DeltaLog pool set per merge
+    interval (allocated on first use), and timed sequences of launches."""
+
+    def __init__(self, gdn, lib, w, dev, stream, rank, ring=RING, klog_prenorm=False, keep_host=False):
+        import torch
+        from linear_attention_decode_gdn_gb300 import workloads as wl
+        self.gdn, self.lib, self.w, self.dev, self.stream = gdn, lib, w, dev, stream
+        self.sptr = ctypes.c_void_p(stream.cuda_stream)
+        self.flags = decode_flags(gdn, w, klog_prenorm)
+        self.kda_dev = {}
+        if w.kda_full:
+            kp = wl.kda_gate_params(w)
+            self.kda_dev = {n: torch.from_numpy(kp[n]).to(dev) for n in ("a_log", "dt_bias", "out_norm_w")}
+        self.ring, self.host_ring = [], []
+        for t in range(ring):
+            x = wl.step_inputs(w, t + 1000 * rank)
+            d = {}
+            if w.conv:
+                d["mixed_qkv"] = torch.from_numpy(x["mixed_bits"].view(np.int16)).view(torch.bfloat16)
+            else:
+                for n_ in ("q", "k", "v"):
+                    d[n_] = (torch.from_numpy(x[n_ + "_bits"].view(np.int16)).view(torch.bfloat16)
+                             if w.qkv_bf16 else torch.from_numpy(x[n_]))
+            if w.kda_full:
+                d["log_decay"] = torch.from_numpy(x["f"])
+                d["beta"] = torch.from_numpy(x["b_raw"])
+                d["out_gate"] = torch.from_numpy(x["out_gate"])
+            else:
+                d["log_decay"] = torch.from_numpy(x["lam"])
+                if not w.raw_value:
+                    d["beta"] = torch.from_numpy(x["beta"])
+            if keep_host:
+                self.host_ring.append({k: v.pin_memory() for k, v in d.items()})
+            self.ring.append({k: v.to(dev) for k, v in d.items()})
+        self.slot = torch.arange(w.batch, dtype=torch.int32, device=dev)
+        self.conv_w = torch.from_numpy(wl.conv_weights(w)).to(dev) if w.conv else None
+        self.o = torch.zeros((w.batch, w.num_heads, w.dv), dtype=torch.float32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.sets = {}
+        self.launches = 0
+
+    def _set(self, M):
+        """(dims, pools, per-ring-step inputs, log) of merge interval M (0: dense)."""
+        if M not in self.sets:
+            gdn, w = self.gdn, self.w
+            dims = gdn.make_dims(w.batch, w.num_heads, w.dk, num_slots=w.batch,
+                                 decay_per_key=w.decay_per_key, log_capacity=max(M - 1, 0), flags=self.flags)
+            pools = gdn.Pools.allocate(dims, device=self.dev, conv=w.conv, deltalog=M > 0)
+            ins = []
+            for r in range(len(self.ring)):
+                d = dict(self.ring[r], **self.kda_dev)
+                if w.conv:
+                    d.update(conv_w=self.conv_w, conv_pool=pools.conv)
+                ins.append(gdn.make_inputs(slot=self.slot, **d))
+            self.sets[M] = (dims, pools, ins, pools.log() if M > 0 else None)
+        return self.sets[M]
+
+    def launch(self, kind, r, M):
+        P = ctypes.byref
+        if kind == "dense":
+            dims, pools, ins, _ = self._set(0)
+            rc = self.lib.gdn_decode_dense(P(dims), P(ins[r]), pools.state.data_ptr(), self.o.data_ptr(),
+                                           self.status.data_ptr(), self.sptr)
+        else:
+            dims, pools, ins, log = self._set(M)
+            fn = self.lib.gdn_decode_append if kind == "append" else self.lib.gdn_decode_merge
+            rc = fn(P(dims), P(ins[r]), pools.state.data_ptr(), P(log), self.o.data_ptr(),
+                    self.status.data_ptr(), self.sptr)
+        if rc:
+            self.gdn._abi.check(rc, kind)
+        self.launches += 1
+
+    @staticmethod
+    def cycle_kinds(mode, M):
+        if mode == "dense":
+            return ["dense"] * M
+        return ["append"] * (M - 1) + ["merge"]
+
+    def timed(self, mode, M, steps, warmup, per_kernel=False):
+        """Times `steps` cycles of M decode steps after `warmup` cycles. Back to back
+        (per_kernel False) or with an event pair around every launch."""
+        import torch
+        kinds = self.cycle_kinds(mode, M)
+        r, n = 0, len(self.ring)
+        self._set(0 if mode == "dense" else M)  # allocate outside the timed region
+        for _ in range(warmup):
+            for k in kinds:
+                self.launch(k, r % n, M)
+                r += 1
+        torch.cuda.synchronize(self.dev)
+        barrier()
+        torch.cuda.synchronize(self.dev)
+        evs = []
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(self.stream)
+        for _ in range(steps):
+            for k in kinds:
+                if per_kernel:
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(self.stream)
+                    self.launch(k, r % n, M)
+                    b.record(self.stream)
+                    evs.append((k, a, b))
+                else:
+                    self.launch(k, r % n, M)
+                r += 1
+        t1.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        barrier()
+        elapsed = t0.elapsed_time(t1) / 1e3
+        per = {}
+        for k, a, b in evs:
+            per.setdefault(k, []).append(a.elapsed_time(b) / 1e3)
+        if int(self.status.item()) != 0:
+            raise RuntimeError(f"device status {int(self.status.item())} in the {self.w.name} run")
+        return elapsed, per
+
+    def free(self):
+        import torch
+        self.sets.clear()
+        self.ring.clear()
+        torch.cuda.empty_cache()
+
+
+def layout_bytes(flags, gdn):
+    """Bytes per element of the key log and the value log under `flags`."""
+    klb = 4 if flags & gdn.KLOG_FP32 else 2
+    ulb = 2 if flags & gdn.ULOG_BF16 else 4
+    return klb, ulb
+
+
+def cycle_bytes_per_head(w, M, klb, ulb):
+    """Algorithmic bytes of one cycle of M decode steps per (request, head): dense M steps
+    for M = 1 (the dense kernel), else M - 1 appends entering with L = 0 .. M-2 and the
+    merge entering with L = M - 1."""
+    if M == 1:
+        return head_bytes("dense", 0, w, klb, w.conv, ulb)
+    return (sum(head_bytes("append", n, w, klb, w.conv, ulb) for n in range(M - 1))
+            + head_bytes("merge", M - 1, w, klb, w.conv, ulb))
+
+
+def fractions(gbs, peak):
+    return {"frac_of_peak": gbs / peak, "frac_of_spec": gbs / SPEC_HBM_GBS}
+
+
+# Decode-step sweeps reported beside the headline value (dense vs the merge interval on the
+# suite's decode workloads); M = 1 is the dense kernel.
+SWEEPS = (("headline", (1, 2, 4, 8, 16)), ("high_concurrency", (1, 2, 4, 8, 16)), ("kda", (1, 8)),
+          ("small_conv", (1, 8)), ("kda_full", (1, 8)), ("rwkv6", (1, 4)))
+SWEEP_DECODE_STEPS = 256   # timed decode steps per sweep point (whole cycles)
+SWEEP_RING = 8
+
+
+def run_sweeps(gdn, lib, dev, stream, rank, world, peak):
+    """Every (workload, M) point of SWEEPS: head-steps/s, us per decode step and algorithmic
+    GB/s of launches back to back over SWEEP_DECODE_STEPS decode steps after 3 warm-up cycles."""
+    from linear_attention_decode_gdn_gb300 import workloads as wl
+    out, launches = {}, 0
+    for name, Ms in SWEEPS:
+        w = wl.WORKLOADS[name]
+        run = DecodeRunner(gdn, lib, w, dev, stream, rank, ring=SWEEP_RING)
+        klb, ulb = layout_bytes(run.flags, gdn)
+        heads = w.batch * w.num_heads
+        leg = {"batch": w.batch, "num_heads": w.num_heads, "dk": w.dk, "dv": w.dv,
+               # a state that fits in L2 is partly re-read from L2: its algorithmic GB/s is no
+               # HBM figure and may exceed the copy peak
+               "state_fits_in_l2": w.state_bytes < L2_BYTES}
+        for M in Ms:
+            cycles = max(1, SWEEP_DECODE_STEPS // M)
+            mode = "dense" if M == 1 else "deltalog"
+            el, _ = run.timed(mode, M, cycles, 3)
+            el, units = reduce_timing(el, heads * M * cycles, device=dev)
+            nbytes = heads * cycle_bytes_per_head(w, M, klb, ulb) * cycles * world
+            gbs = nbytes / el / 1e9
+            leg["dense" if M == 1 else f"M{M}"] = {
+                "head_steps_per_s": units / el, "us_per_decode_step": el / (cycles * M) * 1e6,
+                "algorithmic_bytes_per_decode_step": nbytes / (cycles * M * world),
+                "algorithmic_gbs": gbs, **fractions(gbs, peak)}
+            run.sets.clear()
+        best = max((k for k in leg if k.startswith("M")), key=lambda k: leg[k]["head_steps_per_s"])
+        leg["speedup_best_M_vs_dense"] = {"M": int(best[1:]),
+                                          "speedup": leg[best]["head_steps_per_s"] / leg["dense"]["head_steps_per_s"]}
+        launches += run.launches
+        run.free()
+        out[name] = leg
+    return out, launches
+
+
+def measured_traffic(workload: str, M: int, path=None):
+    """Per-launch DRAM bytes from the committed ncu capture of one whole decode cycle
+    (appends entering with L = 0 .. M-2, the merge, one dense launch), when it was taken on
+    the current kernel sources: {(kernel, L): (read, write)}; else None."""
+    path = path or os.path.join(ROOT, "profiles", "decode_traffic_headline.txt")
+    if not os.path.exists(path):
+        return None
+    src = kernel_source_hash()
+    got = {}
+    for line in open(path):
+        if line.startswith("#") or not line.strip():
+            continue
+        f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+        if f.get("workload") != workload or f.get("src") != src or int(f.get("M", -1)) != M:
+            continue
+        got[(f["kernel"], int(f.get("L", 0)))] = (float(f["read"]), float(f["write"]))
+    need = [("append", n) for n in range(M - 1)] + [("merge", M - 1), ("dense", 0)]
+    return got if all(k in got for k in need) else None
+
+
+def measured_summary(meas, M):
+    """The DeltaLog notes' Fig. 8 view of a measured cycle: read / write per launch for the
+    first and last append, the merge and dense; per decode step the cycle's bytes / M
+    against one dense launch; the write and total reductions."""
+    mr = sum(meas[("append", n)][0] for n in range(M - 1)) + meas[("merge", M - 1)][0]
+    mw = sum(meas[("append", n)][1] for n in range(M - 1)) + meas[("merge", M - 1)][1]
+    d_r, d_w = meas[("dense", 0)]
+    sel = [("append", 0), ("append", M - 2), ("merge", M - 1), ("dense", 0)]
+    return {
+        "per_launch": {(f"{k}_L{n}" if k != "dense" else k): {"read": meas[(k, n)][0], "write": meas[(k, n)][1]}
+                       for k, n in sel},
+        "per_decode_step": {f"deltalog_M{M}": {"read": mr / M, "write": mw / M},
+                            "dense": {"read": d_r, "write": d_w}},
+        "write_reduction": d_w / (mw / M), "total_reduction": (d_r + d_w) / ((mr + mw) / M),
+        "source": "ncu dram__bytes_read.sum / dram__bytes_write.sum of one whole cycle "
+                  "(profiles/decode_traffic_headline.txt, taken on the current kernel sources)"}
+
+
 def run_gpu(args, rank, local_rank, world):
     import torch
     import linear_attention_decode_gdn_gb300 as gdn
@@ -211,119 +443,11 @@ def run_gpu(args, rank, local_rank, world):
     w = wl.WORKLOADS[args.workload]
     M = args.merge_interval
     B, H, D = w.batch, w.num_heads, w.dk
-    flags = (gdn.QKV_BF16 if w.qkv_bf16 else 0) | (gdn.FUSE_CONV if w.conv else 0)
-    if args.klog_prenorm:
-        flags |= gdn.KLOG_PRENORM
-    if w.raw_value:  # the RWKV6 instantiation: b = v (beta NULL), raw q/k, bf16 value log
-        flags |= gdn.PLAIN_UPDATE | gdn.NO_QK_L2NORM | gdn.ULOG_BF16
-    kda_dev = {}
-    if w.kda_full:   # the KDA gate parametrisation and output epilogue
-        flags |= gdn.GATE_KDA | gdn.OUT_NORM_GATE
-        kp = wl.kda_gate_params(w)
-        kda_dev = {n: torch.from_numpy(kp[n]).to(dev) for n in ("a_log", "dt_bias", "out_norm_w")}
     lib = gdn._abi.load()
     stream = torch.cuda.current_stream(dev)
-    sptr = ctypes.c_void_p(stream.cuda_stream)
-
-    # ---- inputs: a ring of RING pre-generated decode steps, resident in HBM
-    ring = []
-    host_ring = []
-    for t in range(RING):
-        x = wl.step_inputs(w, t + 1000 * rank)
-        d = {}
-        if w.conv:
-            d["mixed_qkv"] = torch.from_numpy(x["mixed_bits"].view(np.int16)).view(torch.bfloat16)
-        else:
-            for n_ in ("q", "k", "v"):
-                d[n_] = (torch.from_numpy(x[n_ + "_bits"].view(np.int16)).view(torch.bfloat16)
-                         if w.qkv_bf16 else torch.from_numpy(x[n_]))
-        if w.kda_full:
-            d["log_decay"] = torch.from_numpy(x["f"])
-            d["beta"] = torch.from_numpy(x["b_raw"])
-            d["out_gate"] = torch.from_numpy(x["out_gate"])
-        else:
-            d["log_decay"] = torch.from_numpy(x["lam"])
-            if not w.raw_value:
-                d["beta"] = torch.from_numpy(x["beta"])
-        host_ring.append({k: v.pin_memory() for k, v in d.items()})
-        ring.append({k: v.to(dev) for k, v in d.items()})
-    slot = torch.arange(B, dtype=torch.int32, device=dev)
-    conv_w = None
-    if w.conv:
-        conv_w = torch.from_numpy(wl.conv_weights(w)).to(dev)
-
-    dims_dense = gdn.make_dims(B, H, D, num_slots=B, decay_per_key=w.decay_per_key, flags=flags)
-    dims_log = gdn.make_dims(B, H, D, num_slots=B, decay_per_key=w.decay_per_key,
-                             log_capacity=M - 1, flags=flags)
-    pools_d = gdn.Pools.allocate(dims_dense, device=dev, conv=w.conv)
-    pools_l = gdn.Pools.allocate(dims_log, device=dev, conv=w.conv, deltalog=M > 1)
-    if M == 1:
-        pools_l = gdn.Pools.allocate(dims_log, device=dev, conv=w.conv, deltalog=True)
-    o = torch.zeros((B, H, D), dtype=torch.float32, device=dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-
-    def inputs_for(r, pools):
-        d = dict(ring[r], **kda_dev)
-        if w.conv:
-            d.update(conv_w=conv_w, conv_pool=pools.conv)
-        return gdn.make_inputs(slot=slot, **d)
-
-    in_dense = [inputs_for(r, pools_d) for r in range(RING)]
-    in_log = [inputs_for(r, pools_l) for r in range(RING)]
-    log_l = pools_l.log()
-    P = ctypes.byref
-    fn = {"dense": lib.gdn_decode_dense, "append": lib.gdn_decode_append,
-          "merge": lib.gdn_decode_merge}
-
-    def launch(kind, r):
-        if kind == "dense":
-            rc = fn["dense"](P(dims_dense), P(in_dense[r]), pools_d.state.data_ptr(), o.data_ptr(),
-                             status.data_ptr(), sptr)
-        else:
-            rc = fn[kind](P(dims_log), P(in_log[r]), pools_l.state.data_ptr(), P(log_l),
-                          o.data_ptr(), status.data_ptr(), sptr)
-        if rc:
-            gdn._abi.check(rc, kind)
-
-    def cycle_kinds(mode):
-        if mode == "dense":
-            return ["dense"] * M
-        return ["append"] * (M - 1) + ["merge"]
-
-    def timed(mode, steps, warmup, per_kernel):
-        kinds = cycle_kinds(mode)
-        r = 0
-        for _ in range(warmup):
-            for k in kinds:
-                launch(k, r % RING)
-                r += 1
-        torch.cuda.synchronize(dev)
-        barrier()
-        torch.cuda.synchronize(dev)
-        evs = []
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for _ in range(steps):
-            for k in kinds:
-                if per_kernel:
-                    a = torch.cuda.Event(enable_timing=True)
-                    b = torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
-                    launch(k, r % RING)
-                    b.record(stream)
-                    evs.append((k, a, b))
-                else:
-                    launch(k, r % RING)
-                r += 1
-        t1.record(stream)
-        torch.cuda.synchronize(dev)
-        barrier()
-        elapsed = t0.elapsed_time(t1) / 1e3
-        per = {}
-        for k, a, b in evs:
-            per.setdefault(k, []).append(a.elapsed_time(b) / 1e3)
-        return elapsed, per
+    main = DecodeRunner(gdn, lib, w, dev, stream, rank, klog_prenorm=args.klog_prenorm,
+                        keep_host=not args.no_e2e)
+    flags = main.flags
 
     # ---- warm both modes, then the timed regions (clocks sampled meanwhile). The
     # throughput comes from launches back to back (nothing between them, so a launch can
@@ -331,17 +455,14 @@ def run_gpu(args, rank, local_rank, world):
     # region with an event pair around every launch (which serialises the launches).
     res, per = {}, {}
     with ClockSampler(local_rank) as clocks:
-        res["deltalog"] = timed("deltalog", args.steps, args.warmup, per_kernel=False)
-        res["dense"] = timed("dense", args.steps, args.warmup, per_kernel=False)
-        per["deltalog"] = timed("deltalog", args.steps, args.warmup, per_kernel=True)
-        per["dense"] = timed("dense", args.steps, args.warmup, per_kernel=True)
-    if int(status.item()) != 0:
-        raise RuntimeError(f"device status {int(status.item())} during the benchmark")
+        res["deltalog"] = main.timed("deltalog", M, args.steps, args.warmup)
+        res["dense"] = main.timed("dense", M, args.steps, args.warmup)
+        per["deltalog"] = main.timed("deltalog", M, args.steps, args.warmup, per_kernel=True)
+        per["dense"] = main.timed("dense", M, args.steps, args.warmup, per_kernel=True)
 
     peak, peak_kind = measured_peaks()
     heads = B * H
-    klb = 4 if flags & gdn.KLOG_FP32 else 2
-    ulb = 2 if flags & gdn.ULOG_BF16 else 4
+    klb, ulb = layout_bytes(flags, gdn)
     avg_n = (M - 2) / 2 if M > 1 else 0.0    # appends enter with L = 0 .. M-2
     bytes_per_launch = {
         "dense": heads * head_bytes("dense", 0, w, klb, w.conv, ulb),
@@ -356,12 +477,11 @@ def run_gpu(args, rank, local_rank, world):
             achieved = bytes_per_launch[k] / avg / 1e9
             kernels[k] = {"launches": len(durs), "avg_us": avg * 1e6, "total_ms": tot * 1e3,
                           "algorithmic_bytes_per_launch": bytes_per_launch[k],
-                          "achieved_gbs": achieved, "frac_of_peak": achieved / peak}
+                          "achieved_gbs": achieved, **fractions(achieved, peak)}
     lt, lu = reduce_timing(res["deltalog"][0], heads * M * args.steps, device=dev)
     dt, du = reduce_timing(res["dense"][0], heads * M * args.steps, device=dev)
     value = lu / lt
-    cycle_bytes = ((M - 1) * bytes_per_launch["append"] + bytes_per_launch["merge"]) if M > 1 \
-        else bytes_per_launch["merge"]
+    cycle_bytes = heads * cycle_bytes_per_head(w, M, klb, ulb)
     dense_bytes = M * bytes_per_launch["dense"]
     modes = {}
     for name, (el, units), nbytes in ((f"deltalog_M{M}", (lt, lu), cycle_bytes),
@@ -370,10 +490,11 @@ def run_gpu(args, rank, local_rank, world):
         modes[name] = {"head_steps_per_s": units / el,
                        "us_per_decode_step": el / (args.steps * M) * 1e6,
                        "algorithmic_bytes_per_decode_step": nbytes / M,
-                       "algorithmic_gbs": gbs, "frac_of_peak": gbs / peak}
+                       "algorithmic_gbs": gbs, **fractions(gbs, peak)}
     modes["speedup_deltalog_vs_dense"] = value / (du / dt)
-    # algorithmic read / write bytes per launch by phase (the DeltaLog notes' Fig. 8 split)
-    # and per decode step, with the write and total reductions of the log against dense
+    # read / write bytes per launch by phase (the DeltaLog notes' Fig. 8 split) and per
+    # decode step, with the write and total reductions of the log against dense: from the
+    # algorithmic model, and measured by ncu when a capture of the current sources exists
     phases = {"dense": head_bytes_rw("dense", 0, w, klb, w.conv, ulb)}
     if M > 1:
         phases["append_L0"] = head_bytes_rw("append", 0, w, klb, w.conv, ulb)
@@ -383,21 +504,30 @@ def run_gpu(args, rank, local_rank, world):
         [head_bytes_rw("merge", M - 1, w, klb, w.conv, ulb)]
     step_r, step_w = sum(c[0] for c in cyc) * heads / M, sum(c[1] for c in cyc) * heads / M
     dense_r, dense_w = phases["dense"][0] * heads, phases["dense"][1] * heads
-    modes["traffic"] = {
+    traffic = {"model": {
         "per_launch": {k: {"read": v[0] * heads, "write": v[1] * heads} for k, v in phases.items()},
         "per_decode_step": {f"deltalog_M{M}": {"read": step_r, "write": step_w},
                             "dense": {"read": dense_r, "write": dense_w}},
         "write_reduction": dense_w / step_w, "total_reduction": (dense_r + dense_w) / (step_r + step_w),
-        "source": "algorithmic model (measured DRAM counters in profiles/)"}
+        "source": "algorithmic model (DeltaLog notes Sec. 2.5, Eqs. (8)-(11))"}}
+    meas = measured_traffic(args.workload, M) if (M > 1 and not args.klog_prenorm) else None
+    traffic["measured"] = measured_summary(meas, M) if meas is not None else None
+    modes["traffic"] = traffic
 
     # dominant kernel of the timed DeltaLog cycle: largest share of device time
     dom = max(per["deltalog"][1], key=lambda k: kernels[k]["total_ms"])
     kd = kernels[dom]
-    traffic = profiled_traffic(dom, args.workload)
+    dom_traffic = None
+    if meas is not None:
+        if dom == "append":
+            dom_traffic = sum(sum(meas[("append", n)]) for n in range(M - 1)) / (M - 1)
+        else:
+            dom_traffic = sum(meas[("merge", M - 1)])
     roofline = {"bound": "hbm", "kernel": dom, "achieved": kd["achieved_gbs"], "peak": peak,
                 "peak_kind": f"{peak_kind} (hbm_gbs of MEASURED_PEAKS.json)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s", "unit": "GB/s", "frac": kd["achieved_gbs"] / peak,
-                "traffic": traffic,
+                "frac_of_spec": kd["achieved_gbs"] / SPEC_HBM_GBS, "spec_gbs": SPEC_HBM_GBS,
+                "traffic": dom_traffic,
                 "algorithmic_bytes_per_launch": kd["algorithmic_bytes_per_launch"],
                 "duration": "CUDA events around every launch of the second timed region "
                             "(serialised launches: no overlap with the previous grid)"}
@@ -405,13 +535,22 @@ def run_gpu(args, rank, local_rank, world):
     # ---- end to end through the public API: pinned host inputs in, o back to pinned host
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, M, dims_log, pools_l, host_ring, slot, conv_w, dev, stream, gdn, kda_dev)
+        dims_log, pools_l, _, _ = main._set(M)
+        e2e = run_e2e(args, w, M, dims_log, pools_l, main.host_ring, main.slot, main.conv_w, dev, stream, gdn,
+                      main.kda_dev)
+    launches_main = main.launches
+    main.free()
 
+    sweeps, sweep_launches, sweep_clocks = None, 0, None
+    if not args.no_sweeps:
+        with ClockSampler(local_rank) as sclocks:
+            sweeps, sweep_launches = run_sweeps(gdn, lib, dev, stream, rank, world, peak)
+        sweep_clocks = sclocks.summary()
     verify = run_verify(args, w, flags, dev, stream, gdn, peak) if args.verify else None
     prefill = run_prefill(args, w, flags, dev, stream, gdn) if args.prefill else None
 
-    launches = (args.steps * M * 4 + (e2e["launches"] if e2e else 0) + (verify["launches"] if verify else 0)
-                + (prefill.get("launches", 0) if prefill else 0))
+    launches = (launches_main + (e2e["launches"] if e2e else 0) + (verify["launches"] if verify else 0)
+                + (prefill.get("launches", 0) if prefill else 0) + sweep_launches)
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": lt / args.steps * 1e3, "higher_is_better": True,
@@ -430,6 +569,7 @@ def run_gpu(args, rank, local_rank, world):
         "kernels": kernels,
         "roofline": roofline,
         "e2e": e2e,
+        **({"sweeps": dict(sweeps, clocks=sweep_clocks)} if sweeps else {}),
         **({"verify": verify} if verify else {}),
         **({"prefill": prefill} if prefill else {}),
         "gpu_launches": launches,
@@ -518,7 +658,7 @@ def run_verify(args, w, flags, dev, stream, gdn, peak):
     gbs = B * H * per_head * calls / el / 1e9
     return {"value": units / el, "unit": "positions x heads / s", "positions_per_request": T,
             "us_per_call": el / calls * 1e6, "calls": calls, "launches": calls + max(3, args.warmup),
-            "algorithmic_bytes_per_call": B * H * per_head, "algorithmic_gbs": gbs, "frac_of_peak": gbs / peak,
+            "algorithmic_bytes_per_call": B * H * per_head, "algorithmic_gbs": gbs, **fractions(gbs, peak),
             "state_rows": "one read + T writes of the 64 KiB state per (request, head)"}
 
 
@@ -829,10 +969,12 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--prefill", type=int, default=0,
-                    help="also time the chunked prefill with this many positions per request")
-    ap.add_argument("--verify", type=int, default=0,
-                    help="also time the speculative-decoding verify path with this many positions")
+    ap.add_argument("--prefill", type=int, default=256,
+                    help="also time the chunked prefill with this many positions per request (0: off)")
+    ap.add_argument("--verify", type=int, default=4,
+                    help="also time the speculative-decoding verify path with this many positions (0: off)")
+    ap.add_argument("--no-sweeps", action="store_true",
+                    help="skip the dense-vs-M sweeps over the suite's decode workloads")
     args = ap.parse_args(argv)
 
     world, rank, local = dist_info()

@@ -289,8 +289,6 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
     qsc = (l2 ? 1.0f / sqrtf(qss + p.l2_eps) : 1.0f) * p.q_scale;
   };
 
-  if (fl & GDN_FUSE_CONV) conv_commit(p, b, h, slot, tid);
-
   const bool is_merge = (MODE == MODE_MERGE) || (MODE == MODE_STEP && n == C);
   const bool is_append = (MODE == MODE_APPEND) || (MODE == MODE_STEP && n < C);
   bool timeout = false;
@@ -429,6 +427,9 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
     if (tid == 0) atomic_status(p.status, GDN_STATUS_TIMEOUT);
     return;
   }
+  // the step goes ahead: only now does the conv cache row shift (a call that timed out
+  // above has written nothing, the cache included, so retrying it is safe)
+  if (fl & GDN_FUSE_CONV) conv_commit(p, b, h, slot, tid);
 
   // ---- phase 2: residual, write strength, readout, log commit ----------------------
   float oj = 0.0f;

@@ -236,19 +236,6 @@ __global__ void __launch_bounds__(NT_DECODE) gdn_verify_kernel(const DecodeParam
     } else {
       consumer_sync();  // (A) the previous position's tile update is complete
     }
-    if (conv && (is_q || is_k)) {
-      // the window keeps the last T + 2 inputs: the two after the offset, then the round's
-      if (t == 0) {
-        conv_window_store(p.conv_pool, wx, sx[0], cbf16);
-        conv_window_store(p.conv_pool, wx + 1, sx[1], cbf16);
-        if (is_q) {
-          conv_window_store(p.conv_pool, wv, sv[0], cbf16);
-          conv_window_store(p.conv_pool, wv + 1, sv[1], cbf16);
-        }
-      }
-      conv_window_store(p.conv_pool, wx + 2 + t, sx[2], cbf16);
-      if (is_q) conv_window_store(p.conv_pool, wv + 2 + t, sv[2], cbf16);
-    }
 
     const float qss = scal_f[0] + scal_f[1] + scal_f[2] + scal_f[3];
     const float kss = scal_f[4] + scal_f[5] + scal_f[6] + scal_f[7];
@@ -316,6 +303,21 @@ __global__ void __launch_bounds__(NT_DECODE) gdn_verify_kernel(const DecodeParam
     if (consumer_sync_or(timeout)) {  // (E)
       if (tid == 0) atomic_status(p.status, GDN_STATUS_TIMEOUT);
       return;
+    }
+    // the window keeps the last T + 2 inputs: the two after the offset, then the round's.
+    // Written only past the timeout check of the first position, so a call that gave up
+    // has left the window as it was (all reads of the window precede the loop).
+    if (conv && (is_q || is_k)) {
+      if (t == 0) {
+        conv_window_store(p.conv_pool, wx, sx[0], cbf16);
+        conv_window_store(p.conv_pool, wx + 1, sx[1], cbf16);
+        if (is_q) {
+          conv_window_store(p.conv_pool, wv, sv[0], cbf16);
+          conv_window_store(p.conv_pool, wv + 1, sv[1], cbf16);
+        }
+      }
+      conv_window_store(p.conv_pool, wx + 2 + t, sx[2], cbf16);
+      if (is_q) conv_window_store(p.conv_pool, wv + 2 + t, sv[2], cbf16);
     }
 
     // ---- phase 2: residual, write strength, readout of position t -------------------

@@ -72,6 +72,7 @@ class Variant:
     entry: str = "split"      # deltalog: 'split' = append/merge chosen on the host, 'step' = gdn_decode_step
     extra_flags: int = 0
     name: str = ""
+    drop_flags: int = 0       # flags of the workload this variant runs without
     max_err: float = 0.0
     max_ref: float = 0.0
     state_err: float = float("nan")
@@ -81,7 +82,8 @@ class Variant:
     def setup(self, w: wl.Workload, B, num_slots, q_scale, l2_eps, gate_raw):
         self.C = self.M - 1 if self.mode == "deltalog" else 0
         self.dims = gdn.make_dims(B, w.num_heads, w.dk, w.dv, num_slots, decay_per_key=w.decay_per_key,
-                                  log_capacity=self.C, flags=base_flags(w, gate_raw) | self.extra_flags,
+                                  log_capacity=self.C,
+                                  flags=(base_flags(w, gate_raw) | self.extra_flags) & ~self.drop_flags,
                                   q_scale=q_scale, l2_eps=l2_eps)
         self.pools = gdn.Pools.allocate(self.dims, conv=w.conv, deltalog=self.mode == "deltalog")
         self.o = torch.zeros((B, w.num_heads, w.dv), dtype=torch.float32, device="cuda")
@@ -123,6 +125,7 @@ class Lockstep:
         self.keep = keep_outputs
         self.variants = variants
         gpu_flags0 = base_flags(w, gate_raw) | (variants[0].extra_flags if variants else 0)
+        gpu_flags0 &= ~(variants[0].drop_flags if variants else 0)
         self.cfg = dict(batch=self.B, num_heads=w.num_heads, dk=w.dk, dv=w.dv, num_slots=self.num_slots,
                         dlam=w.dlam, log_capacity=0,
                         flags=oracle_flags(w, gpu_flags0) | extra_oracle_flags,

@@ -63,3 +63,40 @@ def test_headline_figures():
     per = {k: sum(bench.head_bytes_rw(m, n, w)) * heads / MiB
            for k, (m, n) in {"a0": ("append", 0), "a6": ("append", 6), "m7": ("merge", 7)}.items()}
     assert (round(per["a0"], 1), round(per["a6"], 1), round(per["m7"], 1)) == (264.1, 282.2, 538.2)
+
+
+def test_measured_traffic_parser_and_reductions(tmp_path):
+    """The bench reads per-launch ncu bytes of one whole cycle only when they were taken on
+    the current kernel sources, and forms the per-decode-step view from them: the cycle's
+    reads and writes over M against one dense launch."""
+    src = bench.kernel_source_hash()
+    M = 4
+    lines = ["# header", ""]
+    for n in range(M - 1):
+        lines.append(f"kernel=append L={n} M={M} workload=headline src={src} read={100 + n} write=2")
+    lines.append(f"kernel=merge L={M - 1} M={M} workload=headline src={src} read=110 write=90")
+    lines.append(f"kernel=dense L=0 M={M} workload=headline src={src} read=95 write=88")
+    p = tmp_path / "t.txt"
+    p.write_text("\n".join(lines) + "\n")
+    meas = bench.measured_traffic("headline", M, path=str(p))
+    assert meas[("append", 2)] == (102.0, 2.0) and meas[("dense", 0)] == (95.0, 88.0)
+    s = bench.measured_summary(meas, M)
+    cyc_r, cyc_w = 100 + 101 + 102 + 110, 2 * 3 + 90
+    assert s["per_decode_step"]["deltalog_M4"] == {"read": cyc_r / M, "write": cyc_w / M}
+    assert s["write_reduction"] == pytest.approx(88 / (cyc_w / M))
+    assert s["total_reduction"] == pytest.approx((95 + 88) / ((cyc_r + cyc_w) / M))
+    assert set(s["per_launch"]) == {"append_L0", "append_L2", "merge_L3", "dense"}
+    # another source hash, another workload, a missing phase: no measured figures
+    p.write_text("\n".join(lines).replace(src, "0" * 16) + "\n")
+    assert bench.measured_traffic("headline", M, path=str(p)) is None
+    p.write_text("\n".join(lines[:-1]) + "\n")
+    assert bench.measured_traffic("headline", M, path=str(p)) is None
+    assert bench.measured_traffic("kda", M, path=str(p)) is None
+
+
+def test_cycle_bytes_per_head_is_the_sum_of_its_launches():
+    w = wl.WORKLOADS["headline"]
+    assert bench.cycle_bytes_per_head(w, 1, 2, 4) == bench.head_bytes("dense", 0, w)
+    for M in (2, 4, 8, 16):
+        cyc = sum(bench.head_bytes("append", n, w) for n in range(M - 1)) + bench.head_bytes("merge", M - 1, w)
+        assert bench.cycle_bytes_per_head(w, M, 2, 4) == cyc
