@@ -76,6 +76,9 @@ cudaError_t launch_conv_l2norm(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_slot_reset(const ResetParams& p, cudaStream_t stream);
 cudaError_t launch_verify(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_prefill(const DecodeParams& p, cudaStream_t stream);
+// the tensor-core prefill (head size 128, per-head decay, no fused conv / KDA gate / epilogue)
+bool prefill_tc_supported(const DecodeParams& p);
+cudaError_t launch_prefill_tc(const DecodeParams& p, cudaStream_t stream);
 
 // Dynamic shared memory of a prefill CTA (bytes).
 size_t prefill_smem_bytes(int D, int dlam);

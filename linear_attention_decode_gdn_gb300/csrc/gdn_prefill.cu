@@ -810,6 +810,7 @@ cudaError_t launch_prefill_d(const DecodeParams& p, cudaStream_t stream) {
 size_t prefill_smem_bytes(int D, int dlam) { return prefill_layout(D, dlam).total; }
 
 cudaError_t launch_prefill(const DecodeParams& p, cudaStream_t stream) {
+  if (prefill_tc_supported(p)) return launch_prefill_tc(p, stream);
   switch (p.D) {
     case 16: return launch_prefill_d<16>(p, stream);
     case 32: return launch_prefill_d<32>(p, stream);

@@ -1,0 +1,581 @@
+// gdn_prefill_tc.cu -- chunked prefill on the tcgen05 tensor cores (head size 128, per-head decay).
+//
+// Evolution article, "Prefill中的Chunk微观并行" (the six-step order of "完整计算顺序"): inside a
+// chunk of C = 32 tokens with cumulative log-decays gamma_t,
+//   A_ts = beta_t e^{gamma_t - gamma_s} k_t.k_s  (s < t),   P_ts = e^{gamma_t - gamma_s} q_t.k_s  (s <= t)
+//   (I + A) B = diag(beta) (V - Ktil S0),  Ktil_t = e^{gamma_t} k_t
+//   O_t = e^{gamma_t} (q_t S0) + sum_{s <= t} P_ts B_s
+//   S_C = e^{gamma_C} S0 + Khat^T B,          Khat_s = e^{gamma_C - gamma_s} k_s
+// i.e. the decode step's recurrence token for token (decay first, residual on the decayed
+// state, outer-product write, post-update readout; S[dk][dv], o = S^T q).  The plain update
+// (b = beta v) has no A.
+//
+// The matrix products run on the fifth-generation tensor cores (kind::tf32) with three-term
+// TF32 splitting, x = hi + lo with hi = x truncated to TF32 (the tensor core truncates its
+// fp32 operands the same way) and X Y ~ Xhi Yhi + Xlo Yhi + Xhi Ylo, which keeps fp32
+// accuracy (error ~2^-20 relative per term):
+//   pair sums   [K; Q] K^T            (M = 64, N = 32, K = 128)
+//   state read  S^T [K; Q]^T          (M = 128, N = 64, K = 128; S from TMEM)
+//   state write S^T <- S^T + B^T Khat (M = 128, N = 128, K = 32)
+//   readout     O^T <- O^T + B^T P^T  (M = 128, N = 32, K = 32)
+// The fp32 state lives in tensor memory for the whole prompt, transposed (TMEM lane j = value
+// column, TMEM column c = key channel), with its TF32 remainder lo(S) beside it; shared memory
+// holds the operand tiles only.  The forward substitution stays on the CUDA cores
+// (column-parallel, one thread per value column).  One CTA of 8 warps per (request, head):
+// warps 0-3 own value columns j = tid for the substitution and the output; warps 4-7 rescale
+// the state in TMEM meanwhile; one elected lane of warp 0 issues the MMAs.  The next chunk's token stage runs
+// while the state-write and readout MMAs of the current chunk execute.
+#include <atomic>
+
+#include "gdn_tc.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int TD = 128;      // head size of this kernel
+constexpr int TC_C = 32;     // tokens per chunk
+constexpr int TC_NT = 256;   // threads per CTA
+constexpr int TC_ATS = TC_C + 4;
+
+// Operand tiles (K-major, no swizzle; element (r, k) at (r/8)*128 + (k/4)*LBO + (r%8)*16 + (k%4)*4,
+// so groups of 8 rows are adjacent and the k direction steps by LBO = rows/8 * 128 bytes).
+constexpr uint32_t X_LBO = (2 * TC_C / 8) * 128;   // [K; Q] rows: 64 x 128      (1024)
+constexpr uint32_t T128_LBO = (TD / 8) * 128;      // Khat^T, B^T:  128 x 32     (2048)
+constexpr uint32_t P_LBO = (TC_C / 8) * 128;       // P:            32 x 32      (512)
+constexpr uint32_t SBO = 128;
+
+// Staging rows of the raw token inputs, one chunk ahead: q, k, v rows of 128 elements (bf16 or
+// fp32) at a padded stride, then the 32 log-decays and the 32 write strengths.
+constexpr uint32_t ST_ROW = 128 * 4 + 16;
+
+// shared-memory layout (bytes)
+constexpr uint32_t OFF_XH = 0;                      // [K; Q] hi  64 x 128
+constexpr uint32_t OFF_XL = OFF_XH + 2 * TC_C * TD * 4;
+constexpr uint32_t OFF_KH = OFF_XL + 2 * TC_C * TD * 4;  // Khat^T hi 128 x 32
+constexpr uint32_t OFF_KL = OFF_KH + TD * TC_C * 4;
+constexpr uint32_t OFF_BH = OFF_KL + TD * TC_C * 4;      // B^T hi 128 x 32
+constexpr uint32_t OFF_BL = OFF_BH + TD * TC_C * 4;
+constexpr uint32_t OFF_PH = OFF_BL + TD * TC_C * 4;      // P hi 32 x 32
+constexpr uint32_t OFF_PL = OFF_PH + TC_C * TC_C * 4;
+constexpr uint32_t OFF_V = OFF_PL + TC_C * TC_C * 4;     // V row-major 32 x 128 fp32
+constexpr uint32_t OFF_A = OFF_V + TC_C * TD * 4;        // A column-major [s][TC_ATS]
+constexpr uint32_t OFF_RT = OFF_A + TC_C * TC_ATS * 4;   // e^{gamma_t - gamma_s} (s <= t), [s][t]
+constexpr uint32_t OFF_ST = OFF_RT + TC_C * TC_C * 4;    // staging: q, k, v rows, then gates
+constexpr uint32_t OFF_STG = OFF_ST + 3 * TC_C * ST_ROW;
+constexpr uint32_t OFF_G = OFF_STG + 2 * TC_C * 4;       // gamma, beta, e^gamma, e^{gamma_C - gamma},
+                                                         // key and query scale factors
+constexpr uint32_t OFF_BAR = OFF_G + 6 * TC_C * 4;       // mbarriers: ps, p1, p2, drain
+constexpr uint32_t OFF_TMEM = OFF_BAR + 4 * 8;
+constexpr uint32_t TC_SMEM = OFF_TMEM + 16;
+
+// TMEM columns
+constexpr uint32_t TM_S = 0;     // S^T fp32, 128 columns
+constexpr uint32_t TM_L = 128;   // lo(S^T)
+constexpr uint32_t TM_D1 = 256;  // [K S | Q S] -> [. | O], 64 columns, two buffers (chunk parity)
+constexpr uint32_t TM_PS = 320;  // pair sums (M = 64 layout), 32 columns
+constexpr uint32_t TM_D1B = 352;
+constexpr uint32_t TM_COLS = 512;
+
+constexpr uint32_t IDESC_PS = tc::idesc_tf32(64, 32);
+constexpr uint32_t IDESC_P1 = tc::idesc_tf32(128, 64);
+constexpr uint32_t IDESC_P2 = tc::idesc_tf32(128, 128);
+constexpr uint32_t IDESC_RO = tc::idesc_tf32(128, 32);
+
+__device__ __forceinline__ uint32_t kmaj_off(int r, int k, uint32_t lbo) {
+  return static_cast<uint32_t>((r >> 3) * SBO + (k >> 2) * lbo + (r & 7) * 16 + (k & 3) * 4);
+}
+
+// hi / lo of four values, stored as two float4 at byte offset `off` of the hi and lo tiles
+__device__ __forceinline__ void store_split4(unsigned char* smem, uint32_t hi_base, uint32_t lo_base, uint32_t off,
+                                             float a, float b, float c, float d) {
+  const float ha = tc::tf32_hi(a), hb = tc::tf32_hi(b), hc = tc::tf32_hi(c), hd = tc::tf32_hi(d);
+  *reinterpret_cast<float4*>(smem + hi_base + off) = make_float4(ha, hb, hc, hd);
+  *reinterpret_cast<float4*>(smem + lo_base + off) = make_float4(a - ha, b - hb, c - hc, d - hd);
+}
+
+__device__ __forceinline__ void store_split1(unsigned char* smem, uint32_t hi_base, uint32_t lo_base, uint32_t off,
+                                             float a) {
+  const float ha = tc::tf32_hi(a);
+  *reinterpret_cast<float*>(smem + hi_base + off) = ha;
+  *reinterpret_cast<float*>(smem + lo_base + off) = a - ha;
+}
+
+// four elements 4g .. 4g+3 of a staged row (bf16 or fp32), as float
+__device__ __forceinline__ float4 staged4(const unsigned char* row, int g, bool bf16) {
+  if (bf16) {
+    const uint2 u = *reinterpret_cast<const uint2*>(row + 8 * g);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xffff0000u));
+  }
+  return *reinterpret_cast<const float4*>(row + 16 * g);
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Bounded wait for phase `parity` of `bar`, the same answer in every lane of the warp (the
+// TMEM loads and stores that follow are warp-collective).
+__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+}
+
+__global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodeParams p) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x / p.H;
+  const int h = blockIdx.x - b * p.H;
+  const uint32_t fl = p.flags;
+  const bool bf16 = (fl & GDN_QKV_BF16) != 0u;
+  const bool plain = (fl & GDN_PLAIN_UPDATE) != 0u;
+  const bool l2 = (fl & GDN_NO_QK_L2NORM) == 0u;
+  // bf16 inputs are exact TF32 values: the products run on the raw q and k (one TF32 term
+  // for the pair sums, two for the state read) and the L2-norm scales are applied to the
+  // results; fp32 inputs are split into hi and lo after normalisation
+  const bool exact = bf16;
+  const int T = p.T;
+
+  griddep_launch_dependents();
+  griddep_wait();
+
+  const int slot = __ldg(p.slot + b);
+  if (slot < 0) return;  // padding request
+  if (slot >= p.num_slots) {
+    if (tid == 0) atomic_status(p.status, GDN_STATUS_BAD_SLOT);
+    return;
+  }
+  const int n_tok = p.seq_lens ? __ldg(p.seq_lens + b) : T;
+  if (n_tok < 0 || n_tok > T) {
+    if (tid == 0) atomic_status(p.status, GDN_STATUS_BAD_LEN);
+    return;
+  }
+  if (n_tok == 0) return;  // the state is left as it is
+
+  float* gam = reinterpret_cast<float*>(smem + OFF_G);
+  float* bet = gam + TC_C;
+  float* eg = gam + 2 * TC_C;
+  float* ek = gam + 3 * TC_C;
+  float* skf = gam + 4 * TC_C;  // per-token key scale applied to the products (1 when normalised in place)
+  float* sqf = gam + 5 * TC_C;  // per-token query scale
+  float* V = reinterpret_cast<float*>(smem + OFF_V);
+  float* A = reinterpret_cast<float*>(smem + OFF_A);
+  float* RT = reinterpret_cast<float*>(smem + OFF_RT);
+  const float* st_lam = reinterpret_cast<const float*>(smem + OFF_STG);
+  const float* st_beta = st_lam + TC_C;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
+  const uint32_t esz = bf16 ? 2u : 4u;
+
+  // ---- raw token rows and gates of the chunk at t0 into the staging rows (cp.async) ----------
+  auto prefetch = [&](int t0, int n) {
+    const int cpr = bf16 ? 16 : 32;  // 16-byte pieces per row
+    for (int idx = tid; idx < 3 * TC_C * cpr; idx += TC_NT) {
+      const int tensor = idx / (TC_C * cpr);
+      const int rem = idx - tensor * TC_C * cpr;
+      const int t = rem / cpr, part = rem - t * cpr;
+      if (t < n) {
+        const void* base = tensor == 0 ? p.q : (tensor == 1 ? p.k : p.v);
+        const unsigned char* src = static_cast<const unsigned char*>(base) +
+                                   (((static_cast<size_t>(b) * T + t0 + t) * p.H + h) * TD) * esz + 16 * part;
+        cp_async16(smem + OFF_ST + (tensor * TC_C + t) * ST_ROW + 16 * part, src);
+      }
+    }
+    if (tid < 2 * TC_C) {
+      const int t = tid & (TC_C - 1);
+      const float* g = tid < TC_C ? p.lam : p.beta;
+      if (t < n && g != nullptr)
+        cp_async4(smem + OFF_STG + 4 * tid, g + (static_cast<size_t>(b) * T + t0 + t) * p.H + h);
+    }
+    cp_async_commit();
+  };
+  prefetch(0, n_tok < TC_C ? n_tok : TC_C);
+
+  if (warp == 0) {
+    tc::tmem_alloc(tmem_slot, TM_COLS);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1u);
+    fence_mbar_init();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t lb = tc::lane_base(warp);
+  const int j = tid & (TD - 1);  // this thread's TMEM lane / value column
+
+  float* Sg = p.state + (static_cast<size_t>(slot) * p.H + h) * static_cast<size_t>(TD * TD);
+
+  // ---- the state into TMEM, transposed (lane j, column c), with its TF32 remainder ------------
+  {
+    const int c0 = 64 * (tid >> 7);  // warps 0-3 columns 0..63, warps 4-7 columns 64..127
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      float v[16], lo[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) v[k] = Sg[static_cast<size_t>(c0 + 16 * cc + k) * TD + j];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) lo[k] = v[k] - tc::tf32_hi(v[k]);
+      tc::st16(tmem + lb + TM_S + c0 + 16 * cc, v);
+      tc::st16(tmem + lb + TM_L + c0 + 16 * cc, lo);
+    }
+    tc::wait_st();
+  }
+
+  const uint32_t sbase = smem_addr(smem);
+  float kreg[8][4];  // warps 0-3: the normalised key rows of the chunk (for the Khat tile)
+
+  // ---- token stage (from the staging rows): [K; Q] tiles, V, gates, norm scales -------------
+  // warps 0-3: key rows t = 8 w + (lane & 7), channel groups g = (lane >> 3) + 4 i (4 channels
+  // each); warps 4-7: query rows the same way, then the value rows; warp 4 also the gates.
+  auto token_stage = [&](int n) {
+    cp_async_wait_all();
+    __syncthreads();  // every thread's copies have landed
+    const int wq = warp & 3;
+    const int t = 8 * wq + (lane & 7);
+    const int g0 = lane >> 3;
+    const bool live = t < n;
+    const bool isk = warp < 4;
+    const unsigned char* row = smem + OFF_ST + ((isk ? TC_C : 0) + t) * ST_ROW;
+    float4 x[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = live ? staged4(row, g0 + 4 * i, bf16) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (warp == 4) {  // gates of the chunk, lane = token
+      const bool lv = lane < n;
+      float lam = lv ? st_lam[lane] : 0.0f;
+      float be = lv ? (p.beta ? st_beta[lane] : 1.0f) : 0.0f;
+      if ((fl & GDN_GATE_RAW) && lv) {
+        lam = log_sigmoidf_(lam);
+        if (p.beta) be = sigmoidf_(be);
+      }
+      float g = lam;  // inclusive prefix sum over the chunk
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, g, off);
+        if (lane >= off) g += y;
+      }
+      const float gC = __shfl_sync(0xffffffffu, g, TC_C - 1);
+      gam[lane] = g;
+      bet[lane] = be;
+      eg[lane] = expf(g);
+      ek[lane] = expf(gC - g);
+    }
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss += x[i].x * x[i].x + x[i].y * x[i].y + x[i].z * x[i].z + x[i].w * x[i].w;
+    ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 16);
+    const float sc = (l2 ? rsqrtf(ss + p.l2_eps) : 1.0f) * (isk ? 1.0f : p.q_scale);
+    const int r = isk ? t : TC_C + t;
+    if ((lane >> 3) == 0) (isk ? skf : sqf)[t] = exact ? sc : 1.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int g = g0 + 4 * i;
+      const float a0 = x[i].x * sc, a1 = x[i].y * sc, a2 = x[i].z * sc, a3 = x[i].w * sc;
+      if (exact)  // the raw values: exact TF32, no remainder
+        *reinterpret_cast<float4*>(smem + OFF_XH + kmaj_off(r, 4 * g, X_LBO)) = x[i];
+      else
+        store_split4(smem, OFF_XH, OFF_XL, kmaj_off(r, 4 * g, X_LBO), a0, a1, a2, a3);
+      if (isk) {
+        kreg[i][0] = a0;
+        kreg[i][1] = a1;
+        kreg[i][2] = a2;
+        kreg[i][3] = a3;
+      }
+    }
+    if (!isk) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int tv = 8 * wq + u;
+        reinterpret_cast<float4*>(V + tv * TD)[lane] =
+            tv < n ? staged4(smem + OFF_ST + (2 * TC_C + tv) * ST_ROW, lane, bf16) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    __syncthreads();  // gates, scales, tiles visible; the staging rows are free again
+  };
+
+  int t0 = 0;
+  int n = n_tok < TC_C ? n_tok : TC_C;
+  token_stage(n);
+  if (TC_C < n_tok) prefetch(TC_C, n_tok - TC_C < TC_C ? n_tok - TC_C : TC_C);
+  int prev_t0 = 0, prev_n = 0;
+  bool bad = false;
+  uint32_t it = 0;
+
+  // readout of a finished chunk from its output buffer: O^T[j][t] for t < cn (warps 4-7)
+  auto store_output = [&](uint32_t d1, int ct0, int cn) {
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      float o[16];
+      tc::ld16(tmem + lb + d1 + TC_C + 16 * h2, o);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int t = 16 * h2 + k;
+        if (t < cn) p.o[((static_cast<size_t>(b) * T + ct0 + t) * p.H + h) * TD + j] = o[k];
+      }
+    }
+  };
+
+  while (true) {
+    const uint32_t d1 = (it & 1u) ? TM_D1B : TM_D1;
+    if (it > 0) {
+      // the previous chunk's state write and readout are complete
+      if (!wait_warp(&bars[2], (it - 1) & 1u)) bad = true;
+      tc::fence_after_sync();
+      if (!bad && warp >= 4) {
+        // TF32 remainder of the new state
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          float v[16];
+          tc::ld16(tmem + lb + TM_S + 16 * cc, v);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) v[k] -= tc::tf32_hi(v[k]);
+          tc::st16(tmem + lb + TM_L + 16 * cc, v);
+        }
+        tc::wait_st();
+      }
+    }
+    if (warp < 4) {
+      // Khat^T tile (row c, column s): k_s[c] e^{gamma_C - gamma_s}
+      const int s = 8 * warp + (lane & 7);
+      const float f = ek[s];
+      const int g0 = lane >> 3;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int c = 4 * (g0 + 4 * i);
+        store_split1(smem, OFF_KH, OFF_KL, kmaj_off(c + 0, s, T128_LBO), kreg[i][0] * f);
+        store_split1(smem, OFF_KH, OFF_KL, kmaj_off(c + 1, s, T128_LBO), kreg[i][1] * f);
+        store_split1(smem, OFF_KH, OFF_KL, kmaj_off(c + 2, s, T128_LBO), kreg[i][2] * f);
+        store_split1(smem, OFF_KH, OFF_KL, kmaj_off(c + 3, s, T128_LBO), kreg[i][3] * f);
+      }
+    } else {
+      // decay ratios e^{gamma_t - gamma_s} (s <= t) of the chunk, stored [s][t]
+      for (int idx = tid - 4 * 32; idx < TC_C * TC_C; idx += 4 * 32) {
+        const int s2 = idx >> 5, t = idx & 31;
+        RT[idx] = s2 <= t ? expf(gam[t] - gam[s2]) : 0.0f;
+      }
+    }
+    tc::fence_smem_to_async();
+    tc::fence_before_sync();
+    if ((bad = __syncthreads_or(bad) != 0)) break;  // (S1)
+    tc::fence_after_sync();
+
+    if (warp == 0) {  // the whole warp: one elected lane issues
+      // pair sums [K; Q] K^T  (exact inputs: one TF32 term; else hi hi, lo hi, hi lo)
+      const uint32_t xh = sbase + OFF_XH, xl = sbase + OFF_XL;
+      const int ng = exact ? 1 : 3;
+#pragma unroll 1
+      for (int gidx = 0; gidx < ng; ++gidx) {
+        const uint32_t a = gidx == 1 ? xl : xh, bb = gidx == 2 ? xl : xh;
+#pragma unroll
+        for (int i = 0; i < TD / 8; ++i)
+          tc::mma_ss(tmem + TM_PS, tc::smem_desc(a + 2 * i * X_LBO, X_LBO, SBO),
+                     tc::smem_desc(bb + 2 * i * X_LBO, X_LBO, SBO), IDESC_PS, (gidx | i) != 0);
+      }
+      tc::commit(&bars[0]);
+      // state read S^T [K; Q]^T  (A = S from TMEM: its fp32 bits read as TF32 are hi(S)):
+      // hi(S) X, lo(S) X (and hi(S) lo(X) for inexact inputs)
+#pragma unroll 1
+      for (int gidx = 0; gidx < 3; ++gidx) {
+        if (exact && gidx == 1) continue;
+        const uint32_t a = tmem + (gidx == 2 ? TM_L : TM_S), bb = gidx == 1 ? xl : xh;
+#pragma unroll
+        for (int i = 0; i < TD / 8; ++i)
+          tc::mma_ts(tmem + d1, a + 8 * i, tc::smem_desc(bb + 2 * i * X_LBO, X_LBO, SBO), IDESC_P1,
+                     (gidx | i) != 0);
+      }
+      tc::commit(&bars[1]);
+    } else if (warp >= 4 && it > 0) {
+      // the previous chunk's output, from the other buffer, while the MMAs run
+      store_output(d1 == TM_D1 ? TM_D1B : TM_D1, prev_t0, prev_n);
+    }
+
+    // ---- A (strictly lower, times beta) and P (lower with the diagonal) from the pair sums -----
+    // M = 64 accumulator: row m sits in lane 32 (m / 16) + m % 16; warps 0, 1 hold k.k rows
+    // t = 16 w + lane, warps 2, 3 the q.k rows t = 16 (w - 2) + lane (lanes < 16)
+    if (warp < 4) {
+      if (!wait_warp(&bars[0], it & 1u)) bad = true;
+      tc::fence_after_sync();
+      float ps[32];
+      {
+        float a0[16], a1[16];
+        tc::ld16(tmem + lb + TM_PS, a0);
+        tc::ld16(tmem + lb + TM_PS + 16, a1);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          ps[k] = a0[k];
+          ps[16 + k] = a1[k];
+        }
+      }
+      if (lane < 16) {
+        const int t = 16 * (warp & 1) + lane;
+        if (warp < 2) {
+          const float bt = bet[t] * skf[t];
+#pragma unroll
+          for (int s = 0; s < TC_C; ++s)
+            A[s * TC_ATS + t] = (s < t && !plain) ? bt * (ps[s] * skf[s]) * RT[s * TC_C + t] : 0.0f;
+        } else {
+          const float qt = sqf[t];
+#pragma unroll
+          for (int s4 = 0; s4 < TC_C; s4 += 4) {
+            float pv[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) pv[k] = qt * (ps[s4 + k] * skf[s4 + k]) * RT[(s4 + k) * TC_C + t];
+            store_split4(smem, OFF_PH, OFF_PL, kmaj_off(t, s4, P_LBO), pv[0], pv[1], pv[2], pv[3]);
+          }
+        }
+      }
+    }
+    tc::fence_smem_to_async();
+    if ((bad = __syncthreads_or(bad) != 0)) break;  // (S2) A and the P tile are complete
+
+    if (!wait_warp(&bars[1], it & 1u)) bad = true;
+    tc::fence_after_sync();
+    if (!bad) {
+      if (warp < 4) {
+        // ---- residuals, forward substitution (I + A) B = R, the B^T tile ---------------------
+        float bc[TC_C];
+        {
+          float d[16];
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            tc::ld16(tmem + lb + d1 + 16 * h2, d);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const int t = 16 * h2 + k;
+              const float vt = V[t * TD + j];
+              bc[t] = plain ? bet[t] * vt : bet[t] * (vt - (eg[t] * skf[t]) * d[k]);
+            }
+          }
+          // Y = e^{gamma_t} (q_t S0), in place: the readout MMA accumulates P B onto it
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            tc::ld16(tmem + lb + d1 + TC_C + 16 * h2, d);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) d[k] *= eg[16 * h2 + k] * sqf[16 * h2 + k];
+            tc::st16(tmem + lb + d1 + TC_C + 16 * h2, d);
+          }
+        }
+        if (!plain) {
+#pragma unroll
+          for (int s = 0; s < TC_C - 1; ++s) {
+            const float bs = bc[s];
+#pragma unroll
+            for (int t = s + 1; t < TC_C; ++t) bc[t] = fmaf(-A[s * TC_ATS + t], bs, bc[t]);
+          }
+        }
+#pragma unroll
+        for (int s4 = 0; s4 < TC_C; s4 += 4)
+          store_split4(smem, OFF_BH, OFF_BL, kmaj_off(j, s4, T128_LBO), bc[s4], bc[s4 + 1], bc[s4 + 2], bc[s4 + 3]);
+      } else {
+        // ---- decay of the state by e^{gamma_C} before the write accumulates onto it ---------
+        const float dC = eg[TC_C - 1];
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          float v[16];
+          tc::ld16(tmem + lb + TM_S + 16 * cc, v);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) v[k] *= dC;
+          tc::st16(tmem + lb + TM_S + 16 * cc, v);
+        }
+      }
+      tc::wait_st();
+    }
+    tc::fence_smem_to_async();
+    tc::fence_before_sync();
+    if ((bad = __syncthreads_or(bad) != 0)) break;  // (S3)
+    tc::fence_after_sync();
+
+    if (warp == 0) {
+      const uint32_t bh = sbase + OFF_BH, bl = sbase + OFF_BL;
+      const uint32_t kh = sbase + OFF_KH, kl = sbase + OFF_KL;
+      const uint32_t ph = sbase + OFF_PH, pl = sbase + OFF_PL;
+      // state write S^T += B^T Khat and readout O^T = Y^T + B^T P^T (3 x TF32 each)
+#pragma unroll 1
+      for (int gidx = 0; gidx < 3; ++gidx) {
+        const uint32_t a = gidx == 1 ? bl : bh;
+        const uint32_t bk = gidx == 2 ? kl : kh, bp = gidx == 2 ? pl : ph;
+#pragma unroll
+        for (int i = 0; i < TC_C / 8; ++i) {
+          const uint64_t ad = tc::smem_desc(a + 2 * i * T128_LBO, T128_LBO, SBO);
+          tc::mma_ss(tmem + TM_S, ad, tc::smem_desc(bk + 2 * i * T128_LBO, T128_LBO, SBO), IDESC_P2, 1u);
+          tc::mma_ss(tmem + d1 + TC_C, ad, tc::smem_desc(bp + 2 * i * P_LBO, P_LBO, SBO), IDESC_RO, 1u);
+        }
+      }
+      tc::commit(&bars[2]);
+    }
+    prev_t0 = t0;
+    prev_n = n;
+    ++it;
+    t0 += TC_C;
+    if (t0 >= n_tok) break;
+    n = n_tok - t0 < TC_C ? n_tok - t0 : TC_C;
+    token_stage(n);  // overlaps the MMAs just issued (they read B, Khat and P only)
+    if (t0 + TC_C < n_tok) prefetch(t0 + TC_C, n_tok - t0 - TC_C < TC_C ? n_tok - t0 - TC_C : TC_C);
+  }
+
+  if (!bad) {
+    if (!wait_warp(&bars[2], (it - 1) & 1u)) bad = true;
+    tc::fence_after_sync();
+    if (!bad && warp >= 4) store_output((it - 1) & 1u ? TM_D1B : TM_D1, prev_t0, prev_n);
+  }
+  bad = __syncthreads_or(bad) != 0;
+  if (bad) {
+    // let every MMA this CTA issued finish (bounded) before the tensor memory is released
+    if (warp == 0) tc::commit(&bars[3]);
+    (void)mbar_wait(&bars[3], 0u);
+    cp_async_wait_all();
+    if (tid == 0) atomic_status(p.status, GDN_STATUS_TIMEOUT);
+  } else {
+    // ---- the final state back to the pool row -------------------------------------------
+    const int c0 = 64 * (tid >> 7);
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      float v[16];
+      tc::ld16(tmem + lb + TM_S + c0 + 16 * cc, v);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) Sg[static_cast<size_t>(c0 + 16 * cc + k) * TD + j] = v[k];
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc(tmem, TM_COLS);
+}
+
+constexpr int kMaxDevices = 64;
+
+}  // namespace
+
+bool prefill_tc_supported(const DecodeParams& p) {
+  return p.D == TD && p.dlam == 1 && (p.flags & (GDN_FUSE_CONV | GDN_GATE_KDA | GDN_OUT_NORM_GATE)) == 0u;
+}
+
+cudaError_t launch_prefill_tc(const DecodeParams& p, cudaStream_t stream) {
+  static std::atomic<int> configured[kMaxDevices];
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!configured[dev].load(std::memory_order_relaxed)) {
+    err = cudaFuncSetAttribute(gdn_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(TC_SMEM));
+    if (err != cudaSuccess) return err;
+    configured[dev].store(1, std::memory_order_relaxed);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.B * p.H));
+  cfg.blockDim = dim3(TC_NT);
+  cfg.dynamicSmemBytes = TC_SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, gdn_prefill_tc_kernel, p);
+  if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -395,3 +395,42 @@ def test_prefill_strong_per_key_decay(lam_mean):
         pg = pool.cpu().numpy().astype(np.float64)
         serr = float(np.max(np.abs(pg - pool_ref))) / float(np.max(np.abs(pool_ref)))
         assert err / scale <= TOL and serr <= TOL, (lam_mean, err / scale, serr)
+
+
+def test_prefill_raw_value_update_per_head_decay():
+    """b = beta v (beta NULL: 1), raw q and k, with a per-head decay: the head-size-128 path
+    of this shape takes the tensor-core kernel, whose plain form skips the substitution."""
+    e_o, e_s, _ = _run(128, False, 64, np.array([64, 40, 3]), raw_value=True, seed=6)
+    assert e_o <= TOL and e_s <= TOL, (e_o, e_s)
+
+
+@pytest.mark.parametrize("lam_mean", [-6.0, -0.02])
+def test_prefill_strong_and_weak_per_head_decay(lam_mean):
+    """Per-head decay of mean -6 per token (e^gamma underflows inside a chunk: the decayed
+    key and query factors reach zero while the pair ratios e^{gamma_t - gamma_s} and the
+    Khat factors stay exact) and nearly no decay (the state grows over a long prompt);
+    outputs and states at the dense bar, across four chunks and a ragged tail."""
+    B, T, H, D = 3, 120, 2, 128
+    lens = np.array([120, 97, 33])
+    dev, ref = _inputs(B, T, H, D, 1, True, 95)
+    r = np.random.default_rng(96)
+    lam = np.minimum(lam_mean + 0.5 * abs(lam_mean) * r.standard_normal((B, T, H, 1)), 0).astype(np.float32)
+    dev["log_decay"] = dev_f32(lam)
+    ref["lam"] = lam.astype(np.float64)
+    slot = np.arange(B, dtype=np.int32)
+    pool0 = (0.1 * r.standard_normal((B, H, D, D))).astype(np.float32)
+    pool, pool_ref = dev_f32(pool0), pool0.astype(np.float64)
+    dims = gdn.make_dims(B, H, D, num_slots=B, flags=gdn.QKV_BF16, q_scale=D ** -0.5)
+    cfg = dict(batch=B, num_heads=H, dk=D, dv=D, num_slots=B, dlam=1, log_capacity=0,
+               flags=oracle.L2NORM, q_scale=D ** -0.5, l2_eps=1e-6)
+    o = torch.zeros((B, T, H, D), device="cuda")
+    gdn.prefill(dims, T, gdn.make_inputs(slot=dev_i32(slot), **dev), pool, o, seq_lens=dev_i32(lens))
+    o_ref = oracle.prefill_batch(cfg, pool_ref, slot, lens, **ref)
+    torch.cuda.synchronize()
+    og = o.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(og))
+    err = max(float(np.max(np.abs(og[b, :lens[b]] - o_ref[b, :lens[b]]))) for b in range(B))
+    scale = max(float(np.max(np.abs(o_ref[b, :lens[b]]))) for b in range(B))
+    pg = pool.cpu().numpy().astype(np.float64)
+    serr = float(np.max(np.abs(pg - pool_ref))) / float(np.max(np.abs(pool_ref)))
+    assert err / scale <= TOL and serr <= TOL, (lam_mean, err / scale, serr)
