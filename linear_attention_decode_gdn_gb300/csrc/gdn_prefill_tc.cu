@@ -22,8 +22,10 @@
 // column, TMEM column c = key channel), with its TF32 remainder lo(S) beside it; shared memory
 // holds the operand tiles only.  The forward substitution stays on the CUDA cores
 // (column-parallel, one thread per value column).  One CTA of 8 warps per (request, head):
-// warps 0-3 own value columns j = tid for the substitution and the output; warps 4-7 rescale
-// the state in TMEM meanwhile; one elected lane of warp 0 issues the MMAs.  The next chunk's token stage runs
+// warps 0-3 own value columns j = tid for the substitution; warps 4-7 (the same TMEM lanes)
+// form the pair-sum matrices, rescale the state and store the outputs meanwhile; a ninth warp
+// issues the MMAs (one elected lane) and does nothing else, so no compute warp ever waits on
+// the tensor core's issue queue.  The next chunk's token stage runs
 // while the state-write and readout MMAs of the current chunk execute.
 #include <atomic>
 
@@ -34,7 +36,8 @@ namespace {
 
 constexpr int TD = 128;      // head size of this kernel
 constexpr int TC_C = 32;     // tokens per chunk
-constexpr int TC_NT = 256;   // threads per CTA
+constexpr int TC_NT = 288;   // threads per CTA: 8 compute warps and the MMA-issuing warp
+constexpr int ISSUER = 8;    // the warp that issues every MMA and does nothing else
 constexpr int TC_ATS = TC_C + 4;
 
 // Operand tiles (K-major, no swizzle; element (r, k) at (r/8)*128 + (k/4)*LBO + (r%8)*16 + (k%4)*4,
@@ -45,7 +48,7 @@ constexpr uint32_t P_LBO = (TC_C / 8) * 128;       // P:            32 x 32     
 constexpr uint32_t SBO = 128;
 
 // Staging rows of the raw token inputs, one chunk ahead: q, k, v rows of 128 elements (bf16 or
-// fp32) at a padded stride, then the 32 log-decays and the 32 write strengths.
+// fp32) at a padded stride.
 constexpr uint32_t ST_ROW = 128 * 4 + 16;
 
 // shared-memory layout (bytes)
@@ -59,13 +62,13 @@ constexpr uint32_t OFF_PH = OFF_BL + TD * TC_C * 4;      // P hi 32 x 32
 constexpr uint32_t OFF_PL = OFF_PH + TC_C * TC_C * 4;
 constexpr uint32_t OFF_V = OFF_PL + TC_C * TC_C * 4;     // V row-major 32 x 128 fp32
 constexpr uint32_t OFF_A = OFF_V + TC_C * TD * 4;        // A column-major [s][TC_ATS]
-constexpr uint32_t OFF_RT = OFF_A + TC_C * TC_ATS * 4;   // e^{gamma_t - gamma_s} (s <= t), [s][t]
-constexpr uint32_t OFF_ST = OFF_RT + TC_C * TC_C * 4;    // staging: q, k, v rows, then gates
-constexpr uint32_t OFF_STG = OFF_ST + 3 * TC_C * ST_ROW;
-constexpr uint32_t OFF_G = OFF_STG + 2 * TC_C * 4;       // gamma, beta, e^gamma, e^{gamma_C - gamma},
-                                                         // key and query scale factors
-constexpr uint32_t OFF_BAR = OFF_G + 6 * TC_C * 4;       // mbarriers: ps, p1, p2, drain
-constexpr uint32_t OFF_TMEM = OFF_BAR + 4 * 8;
+constexpr uint32_t OFF_ST = OFF_A + TC_C * TC_ATS * 4;   // staging: q, k, v rows
+constexpr uint32_t OFF_G = OFF_ST + 3 * TC_C * ST_ROW;   // gamma, beta, e^gamma, e^{gamma_C - gamma},
+                                                         // key and query scale factors, e^-gamma, flags
+constexpr uint32_t OFF_OB = OFF_G + 8 * TC_C * 4;        // output rows of a chunk, [t][128] fp32
+constexpr uint32_t OFF_BAR = OFF_OB + TC_C * TD * 4;     // mbarriers: ps, p1, p2, drain, then one
+                                                         // per compute warp for its staged rows
+constexpr uint32_t OFF_TMEM = OFF_BAR + 12 * 8;
 constexpr uint32_t TC_SMEM = OFF_TMEM + 16;
 
 // TMEM columns
@@ -110,8 +113,38 @@ __device__ __forceinline__ float4 staged4(const unsigned char* row, int g, bool 
   return *reinterpret_cast<const float4*>(row + 16 * g);
 }
 
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// TMA bulk store shared -> global (16-byte aligned, size a multiple of 16) and its group
+// commit, called by a whole warp with warp-uniform operands: the lowest lane issues (so the
+// same lane always owns the bulk group and its waits). The waits, by that lane: until the
+// shared-memory source of every committed store has been read, or until every committed
+// store has completed.
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile(
+      "{\n .reg .pred e;\n .reg .b32 l;\n elect.sync l|e, 0xffffffff;\n"
+      " @e cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n}\n" ::"l"(gdst),
+      "r"(smem_addr(ssrc)), "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("{\n .reg .pred e;\n .reg .b32 l;\n elect.sync l|e, 0xffffffff;\n @e cp.async.bulk.commit_group;\n}\n" :::
+                   "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Named barrier over warps 4-7 (128 threads); the second form returns the OR of `pred`
+// over them.
+__device__ __forceinline__ void upper_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+__device__ __forceinline__ bool upper_sync_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred a, o;\n setp.ne.u32 a, %1, 0;\n bar.red.or.pred o, 2, 128, a;\n selp.u32 %0, 1, 0, o;\n}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred))
+      : "memory");
+  return r != 0u;
+}
 
 // Bounded wait for phase `parity` of `bar`, the same answer in every lane of the warp (the
 // TMEM loads and stores that follow are warp-collective).
@@ -156,36 +189,57 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
   float* ek = gam + 3 * TC_C;
   float* skf = gam + 4 * TC_C;  // per-token key scale applied to the products (1 when normalised in place)
   float* sqf = gam + 5 * TC_C;  // per-token query scale
+  float* ein = gam + 6 * TC_C;  // e^{-gamma}
+  int* ratio_split = reinterpret_cast<int*>(gam + 7 * TC_C);  // e^{gamma_t - gamma_s} as e^gamma_t e^-gamma_s
   float* V = reinterpret_cast<float*>(smem + OFF_V);
   float* A = reinterpret_cast<float*>(smem + OFF_A);
-  float* RT = reinterpret_cast<float*>(smem + OFF_RT);
-  const float* st_lam = reinterpret_cast<const float*>(smem + OFF_STG);
-  const float* st_beta = st_lam + TC_C;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* pbar = bars + 4;  // staged rows of compute warp w: pbar[w]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
   const uint32_t esz = bf16 ? 2u : 4u;
+  const int wq = warp & 3;
 
-  // ---- raw token rows and gates of the chunk at t0 into the staging rows (cp.async) ----------
+  bool bad = false;
+  if (tid == 0) {
+    for (int i = 0; i < 12; ++i) mbar_init(&bars[i], 1u);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // ---- raw token rows of the chunk at t0 into the staging rows (TMA bulk copies) --------------
+  // Each compute warp copies the rows it reads itself (warps 0-3: key and value rows
+  // 8w..8w+7; warps 4-7: query rows 8(w-4)..), one bulk copy per row issued by an elected
+  // lane and counted on the warp's own mbarrier, so the token stage needs no block barrier
+  // before it reads them. Warp 4 loads the chunk's gates into registers (lane = token).
+  const uint64_t pol_once = l2_policy_evict_first();
+  uint32_t pf_par = 0;   // phase of this warp's staging barrier the next token stage waits for
+  bool pf_pending = false;
+  float pf_lam = 0.0f, pf_beta = 0.0f;
   auto prefetch = [&](int t0, int n) {
-    const int cpr = bf16 ? 16 : 32;  // 16-byte pieces per row
-    for (int idx = tid; idx < 3 * TC_C * cpr; idx += TC_NT) {
-      const int tensor = idx / (TC_C * cpr);
-      const int rem = idx - tensor * TC_C * cpr;
-      const int t = rem / cpr, part = rem - t * cpr;
-      if (t < n) {
-        const void* base = tensor == 0 ? p.q : (tensor == 1 ? p.k : p.v);
-        const unsigned char* src = static_cast<const unsigned char*>(base) +
-                                   (((static_cast<size_t>(b) * T + t0 + t) * p.H + h) * TD) * esz + 16 * part;
-        cp_async16(smem + OFF_ST + (tensor * TC_C + t) * ST_ROW + 16 * part, src);
+    if (warp >= ISSUER) return;
+    const uint32_t rowb = static_cast<uint32_t>(TD) * esz;
+    const int nlive = n - 8 * wq < 0 ? 0 : (n - 8 * wq > 8 ? 8 : n - 8 * wq);
+    const int ntens = warp < 4 ? 2 : 1;
+    tc::expect_tx(&pbar[warp], static_cast<uint32_t>(nlive * ntens) * rowb);
+    for (int r = 0; r < nlive; ++r) {
+      const int t = 8 * wq + r;
+      const size_t off = (((static_cast<size_t>(b) * T + t0 + t) * p.H + h) * TD) * esz;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        if (k < ntens) {
+          const int tensor = warp >= 4 ? 0 : (k == 0 ? 1 : 2);  // staging block: 0 q, 1 k, 2 v
+          const void* base = tensor == 0 ? p.q : (tensor == 1 ? p.k : p.v);
+          tc::bulk_load(smem + OFF_ST + (tensor * TC_C + t) * ST_ROW, static_cast<const unsigned char*>(base) + off,
+                        rowb, &pbar[warp], pol_once);
+        }
       }
     }
-    if (tid < 2 * TC_C) {
-      const int t = tid & (TC_C - 1);
-      const float* g = tid < TC_C ? p.lam : p.beta;
-      if (t < n && g != nullptr)
-        cp_async4(smem + OFF_STG + 4 * tid, g + (static_cast<size_t>(b) * T + t0 + t) * p.H + h);
+    if (warp == 4) {
+      const size_t gi = (static_cast<size_t>(b) * T + t0 + lane) * p.H + h;
+      pf_lam = lane < n ? __ldg(p.lam + gi) : 0.0f;
+      pf_beta = lane < n ? (p.beta ? __ldg(p.beta + gi) : 1.0f) : 0.0f;
     }
-    cp_async_commit();
+    pf_pending = true;
   };
   prefetch(0, n_tok < TC_C ? n_tok : TC_C);
 
@@ -193,21 +247,18 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
     tc::tmem_alloc(tmem_slot, TM_COLS);
     tc::tmem_relinquish();
   }
-  if (tid == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1u);
-    fence_mbar_init();
-  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const uint32_t lb = tc::lane_base(warp);
   const int j = tid & (TD - 1);  // this thread's TMEM lane / value column
+  const uint32_t sbase = smem_addr(smem);
 
   float* Sg = p.state + (static_cast<size_t>(slot) * p.H + h) * static_cast<size_t>(TD * TD);
 
   // ---- the state into TMEM, transposed (lane j, column c), with its TF32 remainder ------------
-  {
+  if (warp < ISSUER) {
     const int c0 = 64 * (tid >> 7);  // warps 0-3 columns 0..63, warps 4-7 columns 64..127
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc) {
@@ -222,16 +273,18 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
     tc::wait_st();
   }
 
-  const uint32_t sbase = smem_addr(smem);
   float kreg[8][4];  // warps 0-3: the normalised key rows of the chunk (for the Khat tile)
 
   // ---- token stage (from the staging rows): [K; Q] tiles, V, gates, norm scales -------------
   // warps 0-3: key rows t = 8 w + (lane & 7), channel groups g = (lane >> 3) + 4 i (4 channels
-  // each); warps 4-7: query rows the same way, then the value rows; warp 4 also the gates.
+  // each), then the value rows 8w..8w+7; warps 4-7: query rows the same way; warp 4 also the
+  // gates.
+  // Ends with the pair-sum MMAs of the chunk issued (they need nothing of the state).
   auto token_stage = [&](int n) {
-    cp_async_wait_all();
-    __syncthreads();  // every thread's copies have landed
-    const int wq = warp & 3;
+   if (warp < ISSUER) {
+    if (!wait_warp(&pbar[warp], pf_par)) bad = true;  // this warp's own rows have landed
+    pf_par ^= 1u;
+    pf_pending = false;
     const int t = 8 * wq + (lane & 7);
     const int g0 = lane >> 3;
     const bool live = t < n;
@@ -242,8 +295,7 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
     for (int i = 0; i < 8; ++i) x[i] = live ? staged4(row, g0 + 4 * i, bf16) : make_float4(0.f, 0.f, 0.f, 0.f);
     if (warp == 4) {  // gates of the chunk, lane = token
       const bool lv = lane < n;
-      float lam = lv ? st_lam[lane] : 0.0f;
-      float be = lv ? (p.beta ? st_beta[lane] : 1.0f) : 0.0f;
+      float lam = pf_lam, be = pf_beta;
       if ((fl & GDN_GATE_RAW) && lv) {
         lam = log_sigmoidf_(lam);
         if (p.beta) be = sigmoidf_(be);
@@ -259,6 +311,11 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
       bet[lane] = be;
       eg[lane] = expf(g);
       ek[lane] = expf(gC - g);
+      // the ratio e^{gamma_t - gamma_s} (s <= t) splits into two exponentials while e^-gamma
+      // stays finite (the chunk's total log-decay above -80); else it is formed per pair
+      const bool split = gC >= -80.0f;
+      ein[lane] = split ? expf(-g) : 0.0f;
+      if (lane == 0) *ratio_split = split ? 1 : 0;
     }
     float ss = 0.0f;
 #pragma unroll
@@ -283,7 +340,7 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
         kreg[i][3] = a3;
       }
     }
-    if (!isk) {
+    if (isk) {
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int tv = 8 * wq + u;
@@ -291,7 +348,25 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
             tv < n ? staged4(smem + OFF_ST + (2 * TC_C + tv) * ST_ROW, lane, bf16) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
+   }
+    tc::fence_smem_to_async();
+    tc::fence_before_sync();
     __syncthreads();  // gates, scales, tiles visible; the staging rows are free again
+    tc::fence_after_sync();
+    if (warp == ISSUER) {
+      // pair sums [K; Q] K^T  (exact inputs: one TF32 term; else hi hi, lo hi, hi lo)
+      const uint32_t xh = sbase + OFF_XH, xl = sbase + OFF_XL;
+      const int ng = exact ? 1 : 3;
+#pragma unroll 1
+      for (int gidx = 0; gidx < ng; ++gidx) {
+        const uint32_t a = gidx == 1 ? xl : xh, bb = gidx == 2 ? xl : xh;
+#pragma unroll
+        for (int i = 0; i < TD / 8; ++i)
+          tc::mma_ss(tmem + TM_PS, tc::smem_desc(a + 2 * i * X_LBO, X_LBO, SBO),
+                     tc::smem_desc(bb + 2 * i * X_LBO, X_LBO, SBO), IDESC_PS, (gidx | i) != 0);
+      }
+      tc::commit(&bars[0]);
+    }
   };
 
   int t0 = 0;
@@ -299,21 +374,29 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
   token_stage(n);
   if (TC_C < n_tok) prefetch(TC_C, n_tok - TC_C < TC_C ? n_tok - TC_C : TC_C);
   int prev_t0 = 0, prev_n = 0;
-  bool bad = false;
   uint32_t it = 0;
 
-  // readout of a finished chunk from its output buffer: O^T[j][t] for t < cn (warps 4-7)
+  // readout of a finished chunk from its TMEM output buffer (warps 4-7): O^T[j][t] into the
+  // shared output rows, then one TMA bulk store per position t < cn (512 bytes each, eight
+  // positions per warp). The rows are rewritten only once the previous chunk's stores have
+  // read them.
+  float* OB = reinterpret_cast<float*>(smem + OFF_OB);
   auto store_output = [&](uint32_t d1, int ct0, int cn) {
+    if (lane == 0) bulk_wait_read();  // this warp's stores of the previous chunk have read their rows
+    upper_sync();
 #pragma unroll
     for (int h2 = 0; h2 < 2; ++h2) {
       float o[16];
       tc::ld16(tmem + lb + d1 + TC_C + 16 * h2, o);
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const int t = 16 * h2 + k;
-        if (t < cn) p.o[((static_cast<size_t>(b) * T + ct0 + t) * p.H + h) * TD + j] = o[k];
-      }
+      for (int k = 0; k < 16; ++k) OB[(16 * h2 + k) * TD + j] = o[k];
     }
+    tc::fence_smem_to_async();
+    upper_sync();
+    // warp 4 + w stores rows 8w .. 8w+7 (lane 0 issues, elected; the group is lane 0's)
+    for (int t = 8 * wq; t < 8 * wq + 8 && t < cn; ++t)
+      bulk_store(p.o + ((static_cast<size_t>(b) * T + ct0 + t) * p.H + h) * TD, OB + t * TD, TD * 4);
+    bulk_commit();
   };
 
   while (true) {
@@ -322,7 +405,7 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
       // the previous chunk's state write and readout are complete
       if (!wait_warp(&bars[2], (it - 1) & 1u)) bad = true;
       tc::fence_after_sync();
-      if (!bad && warp >= 4) {
+      if (!bad && warp >= 4 && warp < ISSUER) {
         // TF32 remainder of the new state
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
@@ -348,33 +431,16 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
         store_split1(smem, OFF_KH, OFF_KL, kmaj_off(c + 2, s, T128_LBO), kreg[i][2] * f);
         store_split1(smem, OFF_KH, OFF_KL, kmaj_off(c + 3, s, T128_LBO), kreg[i][3] * f);
       }
-    } else {
-      // decay ratios e^{gamma_t - gamma_s} (s <= t) of the chunk, stored [s][t]
-      for (int idx = tid - 4 * 32; idx < TC_C * TC_C; idx += 4 * 32) {
-        const int s2 = idx >> 5, t = idx & 31;
-        RT[idx] = s2 <= t ? expf(gam[t] - gam[s2]) : 0.0f;
-      }
     }
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     if ((bad = __syncthreads_or(bad) != 0)) break;  // (S1)
     tc::fence_after_sync();
 
-    if (warp == 0) {  // the whole warp: one elected lane issues
-      // pair sums [K; Q] K^T  (exact inputs: one TF32 term; else hi hi, lo hi, hi lo)
-      const uint32_t xh = sbase + OFF_XH, xl = sbase + OFF_XL;
-      const int ng = exact ? 1 : 3;
-#pragma unroll 1
-      for (int gidx = 0; gidx < ng; ++gidx) {
-        const uint32_t a = gidx == 1 ? xl : xh, bb = gidx == 2 ? xl : xh;
-#pragma unroll
-        for (int i = 0; i < TD / 8; ++i)
-          tc::mma_ss(tmem + TM_PS, tc::smem_desc(a + 2 * i * X_LBO, X_LBO, SBO),
-                     tc::smem_desc(bb + 2 * i * X_LBO, X_LBO, SBO), IDESC_PS, (gidx | i) != 0);
-      }
-      tc::commit(&bars[0]);
+    if (warp == ISSUER) {  // the whole warp: one elected lane issues
       // state read S^T [K; Q]^T  (A = S from TMEM: its fp32 bits read as TF32 are hi(S)):
       // hi(S) X, lo(S) X (and hi(S) lo(X) for inexact inputs)
+      const uint32_t xh = sbase + OFF_XH, xl = sbase + OFF_XL;
 #pragma unroll 1
       for (int gidx = 0; gidx < 3; ++gidx) {
         if (exact && gidx == 1) continue;
@@ -385,15 +451,11 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
                      (gidx | i) != 0);
       }
       tc::commit(&bars[1]);
-    } else if (warp >= 4 && it > 0) {
-      // the previous chunk's output, from the other buffer, while the MMAs run
-      store_output(d1 == TM_D1 ? TM_D1B : TM_D1, prev_t0, prev_n);
-    }
-
-    // ---- A (strictly lower, times beta) and P (lower with the diagonal) from the pair sums -----
-    // M = 64 accumulator: row m sits in lane 32 (m / 16) + m % 16; warps 0, 1 hold k.k rows
-    // t = 16 w + lane, warps 2, 3 the q.k rows t = 16 (w - 2) + lane (lanes < 16)
-    if (warp < 4) {
+    } else if (warp >= 4) {
+      // ---- A (strictly lower, times beta) and P (lower with the diagonal) from the pair sums
+      // (issued at the end of the token stage), while the state read runs. M = 64 accumulator:
+      // row m sits in lane 32 (m / 16) + m % 16, so warps 4, 5 hold the k.k rows
+      // t = 16 (w - 4) + lane and warps 6, 7 the q.k rows t = 16 (w - 6) + lane (lanes < 16)
       if (!wait_warp(&bars[0], it & 1u)) bad = true;
       tc::fence_after_sync();
       float ps[32];
@@ -407,20 +469,32 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
           ps[16 + k] = a1[k];
         }
       }
+      const bool split = *ratio_split != 0;
       if (lane < 16) {
         const int t = 16 * (warp & 1) + lane;
-        if (warp < 2) {
+        const float egt = eg[t], gt = gam[t];
+        if ((warp & 2) == 0) {
           const float bt = bet[t] * skf[t];
+          if (split) {
 #pragma unroll
-          for (int s = 0; s < TC_C; ++s)
-            A[s * TC_ATS + t] = (s < t && !plain) ? bt * (ps[s] * skf[s]) * RT[s * TC_C + t] : 0.0f;
+            for (int s2 = 0; s2 < TC_C; ++s2)
+              A[s2 * TC_ATS + t] = (s2 < t && !plain) ? bt * (ps[s2] * skf[s2]) * (egt * ein[s2]) : 0.0f;
+          } else {
+#pragma unroll
+            for (int s2 = 0; s2 < TC_C; ++s2)
+              A[s2 * TC_ATS + t] = (s2 < t && !plain) ? bt * (ps[s2] * skf[s2]) * expf(gt - gam[s2]) : 0.0f;
+          }
         } else {
           const float qt = sqf[t];
 #pragma unroll
           for (int s4 = 0; s4 < TC_C; s4 += 4) {
             float pv[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) pv[k] = qt * (ps[s4 + k] * skf[s4 + k]) * RT[(s4 + k) * TC_C + t];
+            for (int k = 0; k < 4; ++k) {
+              const int s2 = s4 + k;
+              const float rr = split ? egt * ein[s2] : expf(gt - gam[s2]);
+              pv[k] = s2 <= t ? qt * (ps[s2] * skf[s2]) * rr : 0.0f;
+            }
             store_split4(smem, OFF_PH, OFF_PL, kmaj_off(t, s4, P_LBO), pv[0], pv[1], pv[2], pv[3]);
           }
         }
@@ -431,10 +505,10 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
 
     if (!wait_warp(&bars[1], it & 1u)) bad = true;
     tc::fence_after_sync();
-    if (!bad) {
-      if (warp < 4) {
-        // ---- residuals, forward substitution (I + A) B = R, the B^T tile ---------------------
-        float bc[TC_C];
+    {
+      if (warp < 4 && !bad) {
+        // ---- residuals R, forward substitution, the B^T tile -------------------------------
+        float rr[TC_C];
         {
           float d[16];
 #pragma unroll
@@ -444,7 +518,7 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
             for (int k = 0; k < 16; ++k) {
               const int t = 16 * h2 + k;
               const float vt = V[t * TD + j];
-              bc[t] = plain ? bet[t] * vt : bet[t] * (vt - (eg[t] * skf[t]) * d[k]);
+              rr[t] = plain ? bet[t] * vt : bet[t] * (vt - (eg[t] * skf[t]) * d[k]);
             }
           }
           // Y = e^{gamma_t} (q_t S0), in place: the readout MMA accumulates P B onto it
@@ -456,37 +530,52 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
             tc::st16(tmem + lb + d1 + TC_C + 16 * h2, d);
           }
         }
+        // forward substitution (I + A) B = R, right-looking: once row s is final it is folded
+        // into every later row
+        float* bc = rr;
         if (!plain) {
 #pragma unroll
-          for (int s = 0; s < TC_C - 1; ++s) {
-            const float bs = bc[s];
+          for (int s2 = 0; s2 < TC_C - 1; ++s2) {
+            const float bs = bc[s2];
 #pragma unroll
-            for (int t = s + 1; t < TC_C; ++t) bc[t] = fmaf(-A[s * TC_ATS + t], bs, bc[t]);
+            for (int t4 = (s2 + 1) & ~3; t4 < TC_C; t4 += 4) {
+              const float4 a4 = *reinterpret_cast<const float4*>(A + s2 * TC_ATS + t4);
+              const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                if (t4 + k > s2) bc[t4 + k] = fmaf(-av[k], bs, bc[t4 + k]);
+            }
           }
         }
 #pragma unroll
         for (int s4 = 0; s4 < TC_C; s4 += 4)
           store_split4(smem, OFF_BH, OFF_BL, kmaj_off(j, s4, T128_LBO), bc[s4], bc[s4 + 1], bc[s4 + 2], bc[s4 + 3]);
-      } else {
+        tc::wait_st();
+      } else if (warp >= 4 && warp < ISSUER) {
         // ---- decay of the state by e^{gamma_C} before the write accumulates onto it ---------
-        const float dC = eg[TC_C - 1];
+        if (!bad) {
+          const float dC = eg[TC_C - 1];
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          float v[16];
-          tc::ld16(tmem + lb + TM_S + 16 * cc, v);
+          for (int cc = 0; cc < 8; ++cc) {
+            float v[16];
+            tc::ld16(tmem + lb + TM_S + 16 * cc, v);
 #pragma unroll
-          for (int k = 0; k < 16; ++k) v[k] *= dC;
-          tc::st16(tmem + lb + TM_S + 16 * cc, v);
+            for (int k = 0; k < 16; ++k) v[k] *= dC;
+            tc::st16(tmem + lb + TM_S + 16 * cc, v);
+          }
+          tc::wait_st();
         }
+        // the previous chunk's output, from the other TMEM buffer, while the substitution
+        // runs (decided jointly by warps 4-7: the store synchronises them)
+        if (!upper_sync_or(bad) && it > 0) store_output(d1 == TM_D1 ? TM_D1B : TM_D1, prev_t0, prev_n);
       }
-      tc::wait_st();
     }
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     if ((bad = __syncthreads_or(bad) != 0)) break;  // (S3)
     tc::fence_after_sync();
 
-    if (warp == 0) {
+    if (warp == ISSUER) {
       const uint32_t bh = sbase + OFF_BH, bl = sbase + OFF_BL;
       const uint32_t kh = sbase + OFF_KH, kl = sbase + OFF_KL;
       const uint32_t ph = sbase + OFF_PH, pl = sbase + OFF_PL;
@@ -517,16 +606,17 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
   if (!bad) {
     if (!wait_warp(&bars[2], (it - 1) & 1u)) bad = true;
     tc::fence_after_sync();
-    if (!bad && warp >= 4) store_output((it - 1) & 1u ? TM_D1B : TM_D1, prev_t0, prev_n);
   }
+  // decided for the whole CTA: the output store below synchronises warps 4-7
   bad = __syncthreads_or(bad) != 0;
+  if (!bad && warp >= 4 && warp < ISSUER) store_output((it - 1) & 1u ? TM_D1B : TM_D1, prev_t0, prev_n);
   if (bad) {
     // let every MMA this CTA issued finish (bounded) before the tensor memory is released
-    if (warp == 0) tc::commit(&bars[3]);
+    if (warp == ISSUER) tc::commit(&bars[3]);
     (void)mbar_wait(&bars[3], 0u);
-    cp_async_wait_all();
+    if (pf_pending && warp < ISSUER) (void)mbar_wait(&pbar[warp], pf_par);  // staged rows in flight
     if (tid == 0) atomic_status(p.status, GDN_STATUS_TIMEOUT);
-  } else {
+  } else if (warp < ISSUER) {
     // ---- the final state back to the pool row -------------------------------------------
     const int c0 = 64 * (tid >> 7);
 #pragma unroll
@@ -537,6 +627,7 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
       for (int k = 0; k < 16; ++k) Sg[static_cast<size_t>(c0 + 16 * cc + k) * TD + j] = v[k];
     }
   }
+  if (warp >= 4 && warp < ISSUER && lane == 0) bulk_wait_all();  // the output rows are written before the CTA exits
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();

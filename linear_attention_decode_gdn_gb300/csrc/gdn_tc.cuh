@@ -83,6 +83,27 @@ __device__ __forceinline__ void commit(uint64_t* bar) {
       : "memory");
 }
 
+// ---- TMA bulk loads counted on an mbarrier (whole warp, warp-uniform operands) -------------
+// One elected lane announces `bytes` on `bar` (arrival + expected transaction count)...
+__device__ __forceinline__ void expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n .reg .pred e;\n .reg .b32 l;\n elect.sync l|e, 0xffffffff;\n"
+      " @e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n}\n" ::"r"(smem_addr(bar)),
+      "r"(bytes)
+      : "memory");
+}
+// ... and issues the copies: global -> shared, contiguous, 16-byte aligned, a multiple of 16
+// bytes, completion counted on `bar`, with an L2 cache policy.
+__device__ __forceinline__ void bulk_load(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "{\n .reg .pred e;\n .reg .b32 l;\n elect.sync l|e, 0xffffffff;\n"
+      " @e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;\n}\n" ::"r"(
+          smem_addr(sdst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 // ---- TMEM <-> registers (warp w reaches lanes 32 (w % 4) .. + 31) --------------------------
 __device__ __forceinline__ uint32_t lane_base(int warp) { return static_cast<uint32_t>(32 * (warp & 3)) << 16; }
 
