@@ -204,12 +204,13 @@ class DecodeRunner:
     steps resident in HBM, the dense state pool and one DeltaLog pool set per merge
     interval (allocated on first use), and timed sequences of launches."""
 
-    def __init__(self, gdn, lib, w, dev, stream, rank, ring=RING, klog_prenorm=False, keep_host=False):
+    def __init__(self, gdn, lib, w, dev, stream, rank, ring=RING, klog_prenorm=False, keep_host=False,
+                 extra_flags=0):
         import torch
         from linear_attention_decode_gdn_gb300 import workloads as wl
         self.gdn, self.lib, self.w, self.dev, self.stream = gdn, lib, w, dev, stream
         self.sptr = ctypes.c_void_p(stream.cuda_stream)
-        self.flags = decode_flags(gdn, w, klog_prenorm)
+        self.flags = decode_flags(gdn, w, klog_prenorm) | extra_flags
         self.kda_dev = {}
         if w.kda_full:
             kp = wl.kda_gate_params(w)
@@ -349,9 +350,11 @@ def fractions(gbs, peak):
 
 
 # Decode-step sweeps reported beside the headline value (dense vs the merge interval on the
-# suite's decode workloads); M = 1 is the dense kernel.
-SWEEPS = (("headline", (1, 2, 4, 8, 16)), ("high_concurrency", (1, 2, 4, 8, 16)), ("kda", (1, 8)),
-          ("small_conv", (1, 8)), ("kda_full", (1, 8)), ("rwkv6", (1, 4)))
+# suite's decode workloads); M = 1 is the dense kernel. "split_dv": each head on two CTAs, one
+# per half of the value columns (GDN_SPLIT_DV), beside the one-CTA-per-head default.
+SWEEPS = (("headline", (1, 2, 4, 8, 16), ""), ("high_concurrency", (1, 2, 4, 8, 16), ""), ("kda", (1, 8), ""),
+          ("small_conv", (1, 8), ""), ("kda_full", (1, 8), ""), ("rwkv6", (1, 4), ""),
+          ("headline", (1, 8), "split_dv"), ("small_conv", (1, 8), "split_dv"))
 SWEEP_DECODE_STEPS = 256   # timed decode steps per sweep point (whole cycles)
 SWEEP_RING = 8
 
@@ -361,9 +364,10 @@ def run_sweeps(gdn, lib, dev, stream, rank, world, peak):
     GB/s of launches back to back over SWEEP_DECODE_STEPS decode steps after 3 warm-up cycles."""
     from linear_attention_decode_gdn_gb300 import workloads as wl
     out, launches = {}, 0
-    for name, Ms in SWEEPS:
+    for name, Ms, variant in SWEEPS:
         w = wl.WORKLOADS[name]
-        run = DecodeRunner(gdn, lib, w, dev, stream, rank, ring=SWEEP_RING)
+        extra = gdn.SPLIT_DV if variant == "split_dv" else 0
+        run = DecodeRunner(gdn, lib, w, dev, stream, rank, ring=SWEEP_RING, extra_flags=extra)
         klb, ulb = layout_bytes(run.flags, gdn)
         heads = w.batch * w.num_heads
         leg = {"batch": w.batch, "num_heads": w.num_heads, "dk": w.dk, "dv": w.dv,
@@ -387,7 +391,7 @@ def run_sweeps(gdn, lib, dev, stream, rank, world, peak):
                                           "speedup": leg[best]["head_steps_per_s"] / leg["dense"]["head_steps_per_s"]}
         launches += run.launches
         run.free()
-        out[name] = leg
+        out[name + (f"/{variant}" if variant else "")] = leg
     return out, launches
 
 

@@ -52,9 +52,13 @@
  *   - A negative slot index marks a padding request: it is skipped silently and
  *     its output row is left unchanged.
  *   - Slot indices of one call must be distinct (two requests on one slot race).
- *   - Supported head sizes: dk == dv in {16, 32, 64, 128}. Pointers that the
- *     kernels read or write as 16-byte vectors (state/base, q, k, v, mixed_qkv,
- *     conv_w, o, k_log, u_log) must be 16-byte aligned.
+ *   - Supported head sizes. The decode steps (dense, append, merge, step), the log
+ *     sizes and the slot reset: dk == dv in {16, 32, 64, 128}, dk = 128 with
+ *     dv = 64, and dk = 64 with dv = 128 (GDN_SPLIT_DV: dk == dv in {64, 128}).
+ *     The input stage, verify and prefill: dk == dv in {16, 32, 64, 128}. Other
+ *     shapes return GDN_ERR_UNSUPPORTED. Pointers that the kernels read or write
+ *     as 16-byte vectors (state/base, q, k, v, mixed_qkv, conv_w, o, k_log, u_log)
+ *     must be 16-byte aligned.
  */
 #ifndef GDN_H
 #define GDN_H
@@ -103,6 +107,17 @@ extern "C" {
 #define GDN_OUT_NORM_GATE (1u << 9) /* output epilogue of the same section: o <- RMSNorm(o) (.) w (.)
                                       sigmoid(g) per head over dv, RMSNorm(o) = o / sqrt(mean(o^2) +
                                       out_eps); g = in->out_gate, w = in->out_norm_w (NULL: 1) */
+#define GDN_SPLIT_DV (1u << 10)    /* decode steps: each (request, head) is handled by two CTAs (one
+                                      cluster), each the single writer of half the value columns of
+                                      the state tile, of the output row and of the U log (DeltaLog
+                                      notes, Sec. 2.6 / Fig. 5: the tile sliced along dv, B_V = dv/2);
+                                      the first CTA also commits the head's shared metadata (K_log[L],
+                                      Lambda_log[L], ell, L) and the q / k conv cache rows, after the
+                                      cluster barrier has seen the second read them. Needs dk == dv in
+                                      {64, 128}; excludes GDN_GATE_KDA and GDN_OUT_NORM_GATE. A bounded
+                                      wait that runs out skips the slice that saw it: the other slice
+                                      of the head may still commit. Same results as without the flag
+                                      up to the order of the column sums */
 #define GDN_TEST_STARVE_WAIT (1u << 31) /* test only: the decode kernels expect 16 bytes more than
                                            the first tile copy delivers, so that bounded wait runs
                                            out (about a second) and the call reports
@@ -113,7 +128,7 @@ extern "C" {
 typedef struct gdn_dims {
   int32_t batch;         /* B: requests in this decode batch (B == 0 is a no-op) */
   int32_t num_heads;     /* H */
-  int32_t dk, dv;        /* key / value head size; dk == dv in {16, 32, 64, 128} */
+  int32_t dk, dv;        /* key / value head size (shapes: see "Supported head sizes" above) */
   int32_t num_slots;     /* rows of the state, conv and log pools */
   int32_t decay_per_key; /* 0: per-head scalar log-decay (GDN); 1: per-key-channel (KDA) */
   int32_t log_capacity;  /* C = M - 1 log entries per slot-head, 0..63 (DeltaLog calls only);

@@ -37,6 +37,7 @@ KLOG_PRENORM = 1 << 6
 ULOG_BF16 = 1 << 7
 GATE_KDA = 1 << 8
 OUT_NORM_GATE = 1 << 9
+SPLIT_DV = 1 << 10
 TEST_STARVE_WAIT = 1 << 31
 
 # every symbol include/gdn.h declares

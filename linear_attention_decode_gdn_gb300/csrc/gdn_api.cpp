@@ -15,7 +15,7 @@ thread_local char g_last_error[512] = "";
 
 constexpr uint32_t kKnownFlags = GDN_QKV_BF16 | GDN_FUSE_CONV | GDN_NO_QK_L2NORM | GDN_GATE_RAW |
                                  GDN_PLAIN_UPDATE | GDN_KLOG_FP32 | GDN_KLOG_PRENORM | GDN_ULOG_BF16 |
-                                 GDN_GATE_KDA | GDN_OUT_NORM_GATE |
+                                 GDN_GATE_KDA | GDN_OUT_NORM_GATE | GDN_SPLIT_DV |
                                  GDN_TEST_STARVE_WAIT;
 constexpr int kMaxLogCapacity = 63;
 
@@ -31,17 +31,35 @@ constexpr int kMaxVerifyTokens = 16;  // positions per request in one verify cal
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0u; }
 
-int check_dims(const gdn_dims* d, bool log_call) {
+// What a call needs of dk and dv: the decode steps run every shape with a kernel
+// (gdn::decode_shape_built: square heads of 16..128, dk = 128 / dv = 64, dk = 64 / dv = 128,
+// and square heads of 64 or 128 split along dv); the host-side log sizes and the slot reset
+// accept the same shapes; the input stage, verify and prefill square heads only.
+enum class Shapes { kDecode, kSquare };
+
+int check_dims(const gdn_dims* d, bool log_call, Shapes shapes = Shapes::kSquare) {
   if (d == nullptr) return fail(GDN_ERR_INVALID_ARG, "dims is NULL");
   if (d->batch < 0 || d->num_heads <= 0 || d->dk <= 0 || d->dv <= 0 || d->num_slots <= 0)
     return fail(GDN_ERR_INVALID_ARG, "batch must be >= 0 and num_heads, dk, dv, num_slots > 0");
   if (d->decay_per_key != 0 && d->decay_per_key != 1)
     return fail(GDN_ERR_INVALID_ARG, "decay_per_key must be 0 or 1");
   if ((d->flags & ~kKnownFlags) != 0u) return fail(GDN_ERR_INVALID_ARG, "unknown flag bits");
-  if (d->dk != d->dv || (d->dk != 16 && d->dk != 32 && d->dk != 64 && d->dk != 128))
-    return fail(GDN_ERR_UNSUPPORTED, "head size dk=%d dv=%d not built (dk == dv in {16,32,64,128})",
-                d->dk, d->dv);
-  if (static_cast<long long>(d->batch) * d->num_heads > 0x7fffffffLL)
+  const int ns = (d->flags & GDN_SPLIT_DV) ? 2 : 1;
+  if (shapes == Shapes::kDecode) {
+    if (!gdn::decode_shape_built(d->dk, d->dv, ns))
+      return fail(GDN_ERR_UNSUPPORTED,
+                  "decode shape dk=%d dv=%d%s not built (dk == dv in {16,32,64,128}, dk=128/dv=64, "
+                  "dk=64/dv=128; GDN_SPLIT_DV: dk == dv in {64,128})",
+                  d->dk, d->dv, ns > 1 ? " split along dv" : "");
+    if (ns > 1 && (d->flags & (GDN_GATE_KDA | GDN_OUT_NORM_GATE)))
+      return fail(GDN_ERR_UNSUPPORTED, "GDN_SPLIT_DV is built without the KDA gate and output epilogue");
+  } else {
+    if (d->dk != d->dv || (d->dk != 16 && d->dk != 32 && d->dk != 64 && d->dk != 128))
+      return fail(GDN_ERR_UNSUPPORTED, "head size dk=%d dv=%d not built for this call (dk == dv in {16,32,64,128})",
+                  d->dk, d->dv);
+    if (ns > 1) return fail(GDN_ERR_UNSUPPORTED, "GDN_SPLIT_DV applies to the decode steps only");
+  }
+  if (static_cast<long long>(d->batch) * d->num_heads > 0x3fffffffLL)
     return fail(GDN_ERR_INVALID_ARG, "batch * num_heads too large");
   if (log_call) {
     if (d->log_capacity < 0) return fail(GDN_ERR_INVALID_ARG, "log_capacity < 0");
@@ -101,6 +119,7 @@ gdn::DecodeParams make_params(const gdn_dims* d, const gdn_inputs* in) {
   p.B = d->batch;
   p.H = d->num_heads;
   p.D = d->dk;
+  p.DV = d->dv;
   p.num_slots = d->num_slots;
   p.C = d->log_capacity;
   p.dlam = d->decay_per_key ? d->dk : 1;
@@ -137,7 +156,7 @@ int launched(cudaError_t err, const char* what) {
 int decode_common(int mode, const gdn_dims* dims, const gdn_inputs* in, float* pool,
                   const gdn_log* log, float* o, int32_t* status, void* stream, const char* name) {
   const bool log_call = mode != gdn::MODE_DENSE;
-  int rc = check_dims(dims, log_call);
+  int rc = check_dims(dims, log_call, Shapes::kDecode);
   if (rc != GDN_OK) return rc;
   if (dims->batch == 0) return GDN_OK;
   if ((rc = check_inputs(dims, in)) != GDN_OK) return rc;
@@ -147,7 +166,12 @@ int decode_common(int mode, const gdn_dims* dims, const gdn_inputs* in, float* p
   if (log_call && (rc = check_log(dims, log)) != GDN_OK) return rc;
   if (mode == gdn::MODE_APPEND && dims->log_capacity < 1)
     return fail(GDN_ERR_INVALID_ARG, "append needs log_capacity >= 1");
-  if (gdn::decode_smem_bytes(mode, dims->dk, log_call ? dims->log_capacity : 0,
+  // the split path addresses the pool's rows with 32-bit tensor-copy coordinates
+  if ((dims->flags & GDN_SPLIT_DV) &&
+      static_cast<long long>(dims->num_slots) * dims->num_heads * dims->dk > 0x7fffffffLL)
+    return fail(GDN_ERR_UNSUPPORTED, "GDN_SPLIT_DV: num_slots * num_heads * dk must stay below 2^31");
+  if (gdn::decode_smem_bytes(mode, dims->dk, dims->dv, (dims->flags & GDN_SPLIT_DV) ? 2 : 1,
+                             log_call ? dims->log_capacity : 0,
                              dims->decay_per_key ? dims->dk : 1,
                              (dims->flags & GDN_KLOG_FP32) ? 4 : 2,
                              (dims->flags & GDN_ULOG_BF16) ? 2 : 4) == 0)
@@ -291,7 +315,7 @@ int gdn_prefill(const gdn_dims* dims, int32_t num_tokens, const gdn_inputs* in, 
 }
 
 int gdn_log_bytes(const gdn_dims* dims, gdn_log_sizes* out) {
-  int rc = check_dims(dims, true);
+  int rc = check_dims(dims, true, Shapes::kDecode);
   if (rc != GDN_OK) return rc;
   if (out == nullptr) return fail(GDN_ERR_INVALID_ARG, "out is NULL");
   const size_t sh = static_cast<size_t>(dims->num_slots) * dims->num_heads;
@@ -310,7 +334,7 @@ int gdn_log_bytes(const gdn_dims* dims, gdn_log_sizes* out) {
 
 int gdn_slot_reset(const gdn_dims* dims, const gdn_log* log, void* conv_pool, float* state_pool,
                    const int32_t* slots, int32_t n, int32_t* status, void* stream) {
-  int rc = check_dims(dims, false);
+  int rc = check_dims(dims, false, Shapes::kDecode);
   if (rc != GDN_OK) return rc;
   if (n < 0) return fail(GDN_ERR_INVALID_ARG, "n < 0");
   if (n == 0) return GDN_OK;
@@ -320,6 +344,7 @@ int gdn_slot_reset(const gdn_dims* dims, const gdn_log* log, void* conv_pool, fl
   gdn::ResetParams p{};
   p.H = dims->num_heads;
   p.D = dims->dk;
+  p.DV = dims->dv;
   p.num_slots = dims->num_slots;
   p.dlam = dims->decay_per_key ? dims->dk : 1;
   p.channels = 2 * dims->num_heads * dims->dk + dims->num_heads * dims->dv;

@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(NT) gdn_slot_reset_kernel(const ResetParams p)
     }
   }
   if (p.state != nullptr) {
-    const size_t n4 = static_cast<size_t>(p.H) * p.D * p.D / 4;
+    const size_t n4 = static_cast<size_t>(p.H) * p.D * p.DV / 4;
     float4* row = reinterpret_cast<float4*>(p.state) + static_cast<size_t>(slot) * n4;
     const size_t per = (n4 + parts - 1) / parts;
     const size_t lo = per * part, hi = lo + per < n4 ? lo + per : n4;

@@ -1,4 +1,10 @@
-// gdn_decode.cu -- the decode-step kernels (dense, DeltaLog append, merge, auto step).
+// gdn_decode.cu -- the decode-step kernels (dense, DeltaLog append, merge, auto step) for
+// square heads handled by one CTA each (dk == dv in {16, 32, 64, 128}), and the shape dispatch
+// of every decode launch. gdn_decode_x.cu (kernel in gdn_decode_kernel.cuh) builds the other
+// shapes: dk != dv, and heads split along dv over two CTAs. That kernel computes the same step
+// for these shapes too, but measured about 2.5% slower on the append of square heads (a short,
+// latency-bound CTA: the compiler schedules the general form differently), so the square
+// one-CTA path keeps this kernel.
 //
 // One CTA owns one (request, head): it is the single writer of that head's
 // state / base tile, its output row and its log entries (DeltaLog notes,
@@ -31,6 +37,7 @@
 #include "gdn_device.cuh"
 
 namespace gdn {
+namespace {
 
 // Shared-memory layout of one decode CTA (bytes). Identical on host and device.
 struct Layout {
@@ -575,7 +582,6 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
 // ---------------------------------------------------------------------------------
 // launchers
 
-namespace {
 
 constexpr int kMaxDevices = 64;
 
@@ -660,20 +666,32 @@ cudaError_t launch_d(int mode, const DecodeParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-size_t decode_smem_bytes(int mode, int D, int C, int dlam, int klog_bytes, int ulog_bytes) {
+size_t decode_smem_bytes(int mode, int dk, int dv, int ns, int C, int dlam, int klog_bytes, int ulog_bytes) {
   (void)dlam;
-  if (D != 16 && D != 32 && D != 64 && D != 128) return 0;
-  return decode_layout(mode, D, C, klog_bytes, ulog_bytes).total;
+  if (!decode_shape_built(dk, dv, ns)) return 0;
+  if (ns == 1 && dk == dv) return decode_layout(mode, dk, C, klog_bytes, ulog_bytes).total;
+  return decode_smem_bytes_x(mode, dk, dv, ns, C, klog_bytes, ulog_bytes);
+}
+
+bool decode_shape_built(int dk, int dv, int ns) {
+  if (ns == 1)
+    return (dk == dv && (dk == 16 || dk == 32 || dk == 64 || dk == 128)) || (dk == 128 && dv == 64) ||
+           (dk == 64 && dv == 128);
+  if (ns == 2) return dk == dv && (dk == 64 || dk == 128);
+  return false;
 }
 
 cudaError_t launch_decode(int mode, const DecodeParams& p, cudaStream_t stream) {
-  switch (p.D) {
-    case 16: return launch_d<16>(mode, p, stream);
-    case 32: return launch_d<32>(mode, p, stream);
-    case 64: return launch_d<64>(mode, p, stream);
-    case 128: return launch_d<128>(mode, p, stream);
-    default: return cudaErrorInvalidValue;
+  if ((p.flags & GDN_SPLIT_DV) == 0u && p.D == p.DV) {
+    switch (p.D) {
+      case 16: return launch_d<16>(mode, p, stream);
+      case 32: return launch_d<32>(mode, p, stream);
+      case 64: return launch_d<64>(mode, p, stream);
+      case 128: return launch_d<128>(mode, p, stream);
+      default: return cudaErrorInvalidValue;
+    }
   }
+  return launch_decode_x(mode, p, stream);
 }
 
 }  // namespace gdn

@@ -19,6 +19,7 @@ enum Mode : int {
 
 struct DecodeParams {
   int32_t B, H, D, num_slots, C, dlam, channels;
+  int32_t DV;              // value head size (D is the key head size)
   int32_t prefetch_ahead;  // decode: CTAs resident at once (one wave); CTA i prefetches the inputs
                            // of item i + this into L2, the first wave its own tile (0: off)
   uint32_t flags;
@@ -60,7 +61,7 @@ struct DecodeParams {
 };
 
 struct ResetParams {
-  int32_t H, D, num_slots, dlam, channels, n;
+  int32_t H, D, DV, num_slots, dlam, channels, n;
   uint32_t flags;
   const int32_t* slots;
   float* ell;
@@ -72,6 +73,8 @@ struct ResetParams {
 
 // Kernel launchers (defined in the .cu files). Return cudaSuccess or the launch error.
 cudaError_t launch_decode(int mode, const DecodeParams& p, cudaStream_t stream);
+// the shapes gdn_decode.cu does not instantiate (dk != dv; heads split along dv)
+cudaError_t launch_decode_x(int mode, const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_conv_l2norm(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_slot_reset(const ResetParams& p, cudaStream_t stream);
 cudaError_t launch_verify(const DecodeParams& p, cudaStream_t stream);
@@ -83,7 +86,12 @@ cudaError_t launch_prefill_tc(const DecodeParams& p, cudaStream_t stream);
 // Dynamic shared memory of a prefill CTA (bytes).
 size_t prefill_smem_bytes(int D, int dlam);
 
+// the dynamic shared memory of those shapes (bytes)
+size_t decode_smem_bytes_x(int mode, int dk, int dv, int ns, int C, int klog_bytes, int ulog_bytes);
+
+// Decode shapes with kernels: dk x dv heads, ns CTAs per head along dv.
+bool decode_shape_built(int dk, int dv, int ns);
 // Dynamic shared memory a decode launch needs (bytes); 0 if the shape is not built.
-size_t decode_smem_bytes(int mode, int D, int C, int dlam, int klog_bytes, int ulog_bytes);
+size_t decode_smem_bytes(int mode, int dk, int dv, int ns, int C, int dlam, int klog_bytes, int ulog_bytes);
 
 }  // namespace gdn

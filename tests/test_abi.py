@@ -96,10 +96,19 @@ def test_validation_rejects_before_launch(gdn):
     assert b"dims" in lib.gdn_last_error()
     fake = 1 << 20  # never dereferenced: every call below fails validation first
     ok_in = gdn.make_inputs(q=fake, k=fake, v=fake, log_decay=fake, beta=fake, slot=fake)
-    # unsupported head sizes
-    for dk, dv in ((48, 48), (128, 64), (256, 256)):
+    # unsupported head sizes (the decode steps build square heads of 16..128, 128 x 64 and
+    # 64 x 128; splitting along dv needs a square head of 64 or 128 and no KDA gate / epilogue)
+    for dk, dv in ((48, 48), (128, 32), (32, 128), (256, 256)):
         d = gdn.make_dims(1, 1, dk, dv)
         _expect(gdn, lambda: gdn.decode_dense(d, ok_in, fake, fake, stream=0), _abi.GDN_ERR_UNSUPPORTED)
+    for dk, dv, extra in ((32, 32, 0), (128, 64, 0), (128, 128, gdn.GATE_KDA), (128, 128, gdn.OUT_NORM_GATE)):
+        d = gdn.make_dims(1, 1, dk, dv, flags=gdn.SPLIT_DV | extra)
+        _expect(gdn, lambda: gdn.decode_dense(d, ok_in, fake, fake, stream=0), _abi.GDN_ERR_UNSUPPORTED)
+    # the input stage, verify and prefill: square heads only, never split
+    for d in (gdn.make_dims(1, 1, 128, 64), gdn.make_dims(1, 1, 128, flags=gdn.SPLIT_DV)):
+        _expect(gdn, lambda: gdn.prefill(d, 4, ok_in, fake, fake, stream=0), _abi.GDN_ERR_UNSUPPORTED)
+        _expect(gdn, lambda: gdn.decode_verify(d, 2, ok_in, fake, fake, fake, fake, stream=0),
+                _abi.GDN_ERR_UNSUPPORTED)
     d = gdn.make_dims(1, 1, 128)
     # missing inputs
     _expect(gdn, lambda: gdn.decode_dense(d, gdn.make_inputs(q=fake, k=fake, log_decay=fake, beta=fake,
