@@ -667,6 +667,8 @@ def run_verify(args, w, flags, dev, stream, gdn, peak):
 
 
 FP32_FMA_PER_SM_CLK = 128   # GB300 SM: 4 partitions x 32 FP32 lanes
+TF32_PER_BF16 = 1.1 / 2.25  # nominal dense tensor-core rates of a GB300, TF32 : BF16
+FALLBACK_BF16_TFLOPS = 1900.0
 GB300_SMS = 152
 GB300_MAX_SM_MHZ = 2070.0
 
@@ -727,13 +729,44 @@ def run_prefill(args, w, flags, dev, stream, gdn):
     chunks = -(-T // 32)
     flops = 2.0 * prefill_chunk_fmas(D, 32, bool(pflags & gdn.PLAIN_UPDATE)) * chunks * B * H
     tflops = flops * calls / el / 1e12
-    peak = GB300_SMS * FP32_FMA_PER_SM_CLK * 2 * GB300_MAX_SM_MHZ * 1e6 / 1e12
-    return {"value": units / el, "unit": "positions x heads / s", "positions_per_request": T,
-            "ms_per_call": el / calls * 1e3, "calls": calls, "launches": calls + max(2, args.warmup // 2),
-            "roofline": {"bound": "alu", "achieved": tflops, "peak": peak, "unit": "TFLOP/s (fp32)",
-                         "frac": tflops / peak,
-                         "peak_derivation": "152 SMs x 128 FP32 FMA/clk x 2 FLOP x 2070 MHz",
-                         "algorithmic_flops_per_call": flops}}
+    alu_peak = GB300_SMS * FP32_FMA_PER_SM_CLK * 2 * GB300_MAX_SM_MHZ * 1e6 / 1e12
+    out = {"value": units / el, "unit": "positions x heads / s", "positions_per_request": T,
+           "ms_per_call": el / calls * 1e3, "calls": calls, "launches": calls + max(2, args.warmup // 2)}
+    if prefill_on_tensor_cores(D, w.decay_per_key, pflags, gdn):
+        # the products run as kind::tf32 MMAs, three per fp32-accurate product (3xTF32)
+        bf16, kind = measured_bf16_tflops()
+        tf32 = bf16 * TF32_PER_BF16
+        peak = tf32 / 3.0
+        out["kernel"] = "gdn_prefill_tc_kernel (tcgen05 kind::tf32, 3xTF32)"
+        out["roofline"] = {
+            "bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s (fp32-accurate, 3xTF32)",
+            "frac": tflops / peak,
+            "peak_derivation": f"{kind} bf16 {bf16:.0f} TFLOP/s x {TF32_PER_BF16:.3f} (nominal TF32/BF16 dense "
+                               f"ratio 1.1/2.25) = {tf32:.0f} TF32 TFLOP/s, / 3 MMAs per fp32-accurate product",
+            "frac_of_fp32_alu_peak": tflops / alu_peak, "fp32_alu_peak": alu_peak,
+            "algorithmic_flops_per_call": flops}
+    else:
+        out["kernel"] = "gdn_prefill_kernel (FP32 CUDA cores)"
+        out["roofline"] = {"bound": "alu", "achieved": tflops, "peak": alu_peak, "unit": "TFLOP/s (fp32)",
+                           "frac": tflops / alu_peak,
+                           "peak_derivation": "152 SMs x 128 FP32 FMA/clk x 2 FLOP x 2070 MHz",
+                           "algorithmic_flops_per_call": flops}
+    return out
+
+
+def prefill_on_tensor_cores(D, decay_per_key, flags, gdn) -> bool:
+    """The library's choice of prefill kernel: the tcgen05 one for 128-wide heads with a
+    per-head decay and neither the fused conv nor the KDA gate / epilogue."""
+    return D == 128 and not decay_per_key and not (flags & (gdn.FUSE_CONV | gdn.GATE_KDA | gdn.OUT_NORM_GATE))
+
+
+def measured_bf16_tflops():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def wl_bf16(a):

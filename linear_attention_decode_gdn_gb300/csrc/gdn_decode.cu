@@ -39,6 +39,23 @@
 namespace gdn {
 namespace {
 
+// Two fp32 lanes in one 64-bit register for the packed FMA (fma.rn.f32x2): one
+// instruction, two FMAs, each rounded as fmaf rounds.
+using f2 = unsigned long long;
+__device__ __forceinline__ f2 f2_pack(float lo, float hi) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(f2 v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
+  f2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 // Shared-memory layout of one decode CTA (bytes). Identical on host and device.
 struct Layout {
   uint32_t tile, bars, scal, vec, uni, us, kd, coef, total;
@@ -47,7 +64,12 @@ struct Layout {
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1u) / a * a; }
 
-__host__ __device__ inline Layout decode_layout(int mode, int D, int C, int klog_bytes, int ulog_bytes) {
+// `r3`: the three-per-SM merge form.  With C <= 8 its U entries go to registers (each
+// thread the four columns it folds, the q-owning threads their readout column) and ell'
+// takes d_lambda entries, so that a 128-wide head's merge CTA under a per-head decay fits
+// three to an SM like dense and append.
+__host__ __device__ inline Layout decode_layout(int mode, int D, int C, int dlam, int klog_bytes, int ulog_bytes,
+                                                bool r3) {
   Layout L{};
   const bool has_log = mode != MODE_DENSE;
   const bool can_merge = mode == MODE_MERGE || mode == MODE_STEP;
@@ -62,15 +84,17 @@ __host__ __device__ inline Layout decode_layout(int mode, int D, int C, int klog
   off += 64;
   L.scal = off;
   off += 128;
-  L.vec = off;  // q (later b), k, q*dec, k*dec, ell', [dec]
-  off += static_cast<uint32_t>(D * 4 * (writes_state ? 6 : 5));
+  L.vec = off;  // q (later b), k, q*dec, k*dec, ell', [dec]  (r3: ..., dec, ell' of d_lambda entries)
+  off += static_cast<uint32_t>(D * 4 * (writes_state ? 5 : 4)) +
+         (r3 ? align_up(static_cast<uint32_t>(dlam * 4), 16u) : static_cast<uint32_t>(D * 4));
   // K_log entries while the coefficients are formed, then the cross-warp partial sums.
   const uint32_t kbytes = has_log ? static_cast<uint32_t>(C * D * klog_bytes) : 0u;
   const uint32_t redbytes = static_cast<uint32_t>(8 * D * 4);
   L.uni = off;
   off += align_up(kbytes > redbytes ? kbytes : redbytes, 16u);
   L.us = off;
-  off += has_log ? align_up(static_cast<uint32_t>((can_merge ? L.cp : C) * D * ulog_bytes), 16u) : 0u;
+  const bool ureg = r3 && C <= 8;
+  off += (has_log && !ureg) ? align_up(static_cast<uint32_t>((can_merge ? L.cp : C) * D * ulog_bytes), 16u) : 0u;
   L.kd = off;
   off += can_merge ? static_cast<uint32_t>(D * L.cp * 4) : 0u;
   L.coef = off;  // c^k | c^q | per-head decay snapshots Lambda_i
@@ -80,10 +104,14 @@ __host__ __device__ inline Layout decode_layout(int mode, int D, int C, int klog
 }
 
 // The auto step carries both paths; its register cap keeps two CTAs per SM (its shared
-// memory allows two).  The other modes take no minimum (0: none).  EXT instances carry the
-// KDA gate parametrisation and output epilogue; the others compile them out.
-template <int D, int MODE, bool EXT>
-__global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_decode_kernel(const DecodeParams p) {
+// memory allows two).  The three-per-SM merge form (R3, layout above) caps registers for
+// three: with a third CTA resident, the fold's arithmetic hides behind the other CTAs'
+// copies.  The other instances take no minimum (0: none).  EXT instances carry the KDA gate
+// parametrisation and output epilogue; the others compile them out.
+template <int D, int MODE, bool EXT, bool R3>
+__global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : (R3 ? 3 : 0))
+    gdn_decode_kernel(const DecodeParams p) {
+  static_assert(!R3 || MODE == MODE_MERGE, "the three-per-SM form is a merge form");
   extern __shared__ __align__(128) unsigned char smem[];
 
   constexpr int NCHUNK = (D >= 128) ? 4 : 1;       // TMA row chunks of the tile
@@ -128,7 +156,11 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
   const uint32_t fl = p.flags;
   const int klb = (fl & GDN_KLOG_FP32) ? 4 : 2;
   const int ulb = (fl & GDN_ULOG_BF16) ? 2 : 4;
-  const Layout L = decode_layout(MODE, D, C, klb, ulb);
+  const Layout L = decode_layout(MODE, D, C, dlam, klb, ulb, R3);
+  // U entries in registers.  The host launches R3 only with C <= 8; the test stays a run-time
+  // one on purpose: with the shared-memory path compiled in as well, the instance fits its
+  // 72 registers without spilling and measured about 8% faster than with it compiled out.
+  const bool ureg = R3 && C <= 8;
   float* tile = reinterpret_cast<float*>(smem + L.tile);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   int* scal_i = reinterpret_cast<int*>(smem + L.scal);             // [0] L on entry, [1] status bits
@@ -139,8 +171,8 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
   float* k_s = q_s + D;
   float* qdec_s = q_s + 2 * D;
   float* kdec_s = q_s + 3 * D;
-  float* ellp_s = q_s + 4 * D;
-  float* dec_s = q_s + 5 * D;  // only when the state is written
+  float* ellp_s = q_s + (R3 ? 5 : 4) * D;  // (R3: d_lambda entries, last)
+  float* dec_s = q_s + (R3 ? 4 : 5) * D;   // only when the state is written
   unsigned char* uni = smem + L.uni;
   float* red = reinterpret_cast<float*>(uni);
   float* u_s = reinterpret_cast<float*>(smem + L.us);  // U entries (fp32, or bf16 bits)
@@ -194,7 +226,8 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
                                                          sh * C * D * ulb);
       const int kvec = nc * D * klb / 16, uvec = nc * D * ulb / 16;
       for (int i = lane; i < kvec; i += 32) cp_async16(reinterpret_cast<uint4*>(uni) + i, ksrc + i);
-      for (int i = lane; i < uvec; i += 32) cp_async16(reinterpret_cast<uint4*>(u_s) + i, usrc + i);
+      if (!ureg)
+        for (int i = lane; i < uvec; i += 32) cp_async16(reinterpret_cast<uint4*>(u_s) + i, usrc + i);
       if (dlam == 1)
         for (int e = lane; e < nc; e += 32) cp_async4(lam_s + e, p.lam_log + sh * C + e);
       else if (lane < nc)  // per-key snapshots stay in global memory: warm L2 for the replay
@@ -250,6 +283,21 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
     }
   }
   if ((EXT && (fl & GDN_OUT_NORM_GATE)) && is_q) og = __ldg(p.out_gate + (static_cast<size_t>(b) * p.H + h) * D + ii);
+  // U entries in registers: the q-owning threads fetch their readout column of every entry
+  // now (only the entries below L enter the readout)
+  float ucol[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) ucol[e] = 0.0f;
+  if (ureg && is_q) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      if (e < C) {
+        const size_t at = (sh * C + e) * D + tid;
+        ucol[e] = (ulb == 2) ? bf16_bits_to_float(static_cast<const uint16_t*>(p.u_log)[at])
+                             : static_cast<const float*>(p.u_log)[at];
+      }
+    }
+  }
   if (!ctrl) {
     beta = p.beta ? __ldg(p.beta + static_cast<size_t>(b) * p.H + h) : 1.0f;
     load_token(p, b, h, slot, tid, &x, &vj);
@@ -337,9 +385,11 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
         const int d = idx / cp, e = idx - d * cp;
         if (e >= n) kd_s[d * cp + e] = 0.0f;
       }
-      const int pad_words = (cp - n) * D * ulb / 4;
-      uint32_t* upad = reinterpret_cast<uint32_t*>(smem + L.us + static_cast<size_t>(n) * D * ulb);
-      for (int idx = tid; idx < pad_words; idx += NT) upad[idx] = 0u;
+      if (!ureg) {
+        const int pad_words = (cp - n) * D * ulb / 4;
+        uint32_t* upad = reinterpret_cast<uint32_t*>(smem + L.us + static_cast<size_t>(n) * D * ulb);
+        for (int idx = tid; idx < pad_words; idx += NT) upad[idx] = 0u;
+      }
     }
     for (int e = warp; e < n; e += NW) {
       const float* lam_e = p.lam_log + (sh * C + e) * dlam;
@@ -454,10 +504,20 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
     // (with or without log terms after it) on the same arithmetic
     rk = __fmul_rn(rk, kinv);
     rq = __fmul_rn(rq, qsc);
-    for (int e = 0; e < n; ++e) {
-      const float u = (ulb == 2) ? bf16_bits_to_float(u16_s[e * D + j]) : u_s[e * D + j];
-      rk = fmaf(ck_s[e], u, rk);
-      rq = fmaf(cq_s[e], u, rq);
+    if (ureg) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (e < n) {
+          rk = fmaf(ck_s[e], ucol[e], rk);
+          rq = fmaf(cq_s[e], ucol[e], rq);
+        }
+      }
+    } else {
+      for (int e = 0; e < n; ++e) {
+        const float u = (ulb == 2) ? bf16_bits_to_float(u16_s[e * D + j]) : u_s[e * D + j];
+        rk = fmaf(ck_s[e], u, rk);
+        rq = fmaf(cq_s[e], u, rq);
+      }
     }
     const float bj = (fl & GDN_PLAIN_UPDATE) ? beta * vj : beta * (vj - rk);
     oj = fmaf(scal_f[8] * qsc * kinv, bj, rq);
@@ -515,14 +575,42 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
     const int ng = (MODE == MODE_DENSE) ? 0 : (n + 7) / 8;
     for (int g = 0; g < ng; ++g) {
       float4 u[8];
+      if (ureg) {
+        // this thread's four columns of each entry, from global memory (the lines the
+        // readout-column fetch brought in); zero past L
+        const unsigned char* ub = static_cast<const unsigned char*>(p.u_log) + sh * C * D * ulb;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        if (ulb == 2) {
-          const uint2 raw = reinterpret_cast<const uint2*>(u16_s + (g * 8 + e) * D)[c4];
-          u[e] = make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u),
-                             __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u));
-        } else {
-          u[e] = reinterpret_cast<const float4*>(u_s + (g * 8 + e) * D)[c4];
+        for (int e = 0; e < 8; ++e) {
+          u[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (e < n) {
+            if (ulb == 2) {
+              const uint2 raw = reinterpret_cast<const uint2*>(ub + static_cast<size_t>(e) * D * 2)[c4];
+              u[e] = make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u),
+                                 __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u));
+            } else {
+              u[e] = reinterpret_cast<const float4*>(ub + static_cast<size_t>(e) * D * 4)[c4];
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (ulb == 2) {
+            const uint2 raw = reinterpret_cast<const uint2*>(u16_s + (g * 8 + e) * D)[c4];
+            u[e] = make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u),
+                               __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u));
+          } else {
+            u[e] = reinterpret_cast<const float4*>(u_s + (g * 8 + e) * D)[c4];
+          }
+        }
+      }
+      // (R3 folds with packed FMAs on column pairs: the same roundings, fewer instructions)
+      f2 u01[8], u23[8];
+      if (R3) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          u01[e] = f2_pack(u[e].x, u[e].y);
+          u23[e] = f2_pack(u[e].z, u[e].w);
         }
       }
 #pragma unroll
@@ -540,12 +628,24 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : 0) gdn_deco
           const float4 w0 = *reinterpret_cast<const float4*>(kd_s + r * cp + g * 8);
           const float4 w1 = *reinterpret_cast<const float4*>(kd_s + r * cp + g * 8 + 4);
           const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+          if (R3) {
+            f2 a01 = f2_pack(acc.x, acc.y), a23 = f2_pack(acc.z, acc.w);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            acc.x = fmaf(wv[e], u[e].x, acc.x);
-            acc.y = fmaf(wv[e], u[e].y, acc.y);
-            acc.z = fmaf(wv[e], u[e].z, acc.z);
-            acc.w = fmaf(wv[e], u[e].w, acc.w);
+            for (int e = 0; e < 8; ++e) {
+              const f2 ws = f2_pack(wv[e], wv[e]);
+              a01 = f2_fma(ws, u01[e], a01);
+              a23 = f2_fma(ws, u23[e], a23);
+            }
+            f2_unpack(a01, acc.x, acc.y);
+            f2_unpack(a23, acc.z, acc.w);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              acc.x = fmaf(wv[e], u[e].x, acc.x);
+              acc.y = fmaf(wv[e], u[e].y, acc.y);
+              acc.z = fmaf(wv[e], u[e].z, acc.z);
+              acc.w = fmaf(wv[e], u[e].w, acc.w);
+            }
           }
           if (g == ng - 1) {  // the current token's term, then the write-back
             const float kk = k_s[r] * kinv;
@@ -596,23 +696,23 @@ int sm_count(int dev) {
 }
 
 
-template <int D, int MODE, bool EXT>
+template <int D, int MODE, bool EXT, bool R3>
 cudaError_t launch_one(const DecodeParams& p, cudaStream_t stream) {
   static std::atomic<uint32_t> configured[kMaxDevices];
   const int klb = (p.flags & GDN_KLOG_FP32) ? 4 : 2;
   const int ulb = (p.flags & GDN_ULOG_BF16) ? 2 : 4;
-  const Layout L = decode_layout(MODE, D, p.C, klb, ulb);
+  const Layout L = decode_layout(MODE, D, p.C, p.dlam, klb, ulb, R3);
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (configured[dev].load(std::memory_order_relaxed) < L.total) {
-    err = cudaFuncSetAttribute(gdn_decode_kernel<D, MODE, EXT>,
+    err = cudaFuncSetAttribute(gdn_decode_kernel<D, MODE, EXT, R3>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(L.total));
     if (err != cudaSuccess) return err;
     // several 64 KiB-tile CTAs per SM only fit with the whole L1/shared array as shared memory
-    err = cudaFuncSetAttribute(gdn_decode_kernel<D, MODE, EXT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    err = cudaFuncSetAttribute(gdn_decode_kernel<D, MODE, EXT, R3>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                static_cast<int>(cudaSharedmemCarveoutMaxShared));
     if (err != cudaSuccess) return err;
     configured[dev].store(L.total, std::memory_order_relaxed);
@@ -623,7 +723,7 @@ cudaError_t launch_one(const DecodeParams& p, cudaStream_t stream) {
   uint64_t rc = resident[dev].load(std::memory_order_relaxed);
   if ((rc >> 32) != L.total) {
     int per_sm = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gdn_decode_kernel<D, MODE, EXT>, NT_DECODE,
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gdn_decode_kernel<D, MODE, EXT, R3>, NT_DECODE,
                                                         L.total);
     if (err != cudaSuccess) return err;
     rc = (static_cast<uint64_t>(L.total) << 32) | static_cast<uint32_t>(per_sm > 0 ? per_sm : 1);
@@ -642,18 +742,45 @@ cudaError_t launch_one(const DecodeParams& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, gdn_decode_kernel<D, MODE, EXT>, q);
+  err = cudaLaunchKernelEx(&cfg, gdn_decode_kernel<D, MODE, EXT, R3>, q);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
+}
+
+// Whether a merge of a 128-wide head takes the R3 form: C <= 8 and its layout fits three
+// CTAs in the SM's shared memory (each CTA also takes the per-block reservation).  Where
+// it does not (C > 8, or a per-key decay whose layout comes out larger), the general form
+// runs at two CTAs per SM without the register cap.
+bool merge_three_per_sm(const DecodeParams& p) {
+  if (p.D != 128 || p.C > 8) return false;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  static std::atomic<int> budget[kMaxDevices];
+  int b = budget[dev].load(std::memory_order_relaxed);
+  if (b == 0) {
+    int per_sm = 0, reserved = 0;
+    if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
+      return false;
+    b = per_sm / 3 - reserved;
+    budget[dev].store(b > 0 ? b : -1, std::memory_order_relaxed);
+  }
+  const int klb = (p.flags & GDN_KLOG_FP32) ? 4 : 2;
+  const int ulb = (p.flags & GDN_ULOG_BF16) ? 2 : 4;
+  return b > 0 && decode_layout(MODE_MERGE, 128, p.C, p.dlam, klb, ulb, true).total <= static_cast<uint32_t>(b);
 }
 
 template <int D, bool EXT>
 cudaError_t launch_de(int mode, const DecodeParams& p, cudaStream_t stream) {
   switch (mode) {
-    case MODE_DENSE: return launch_one<D, MODE_DENSE, EXT>(p, stream);
-    case MODE_APPEND: return launch_one<D, MODE_APPEND, EXT>(p, stream);
-    case MODE_MERGE: return launch_one<D, MODE_MERGE, EXT>(p, stream);
-    case MODE_STEP: return launch_one<D, MODE_STEP, EXT>(p, stream);
+    case MODE_DENSE: return launch_one<D, MODE_DENSE, EXT, false>(p, stream);
+    case MODE_APPEND: return launch_one<D, MODE_APPEND, EXT, false>(p, stream);
+    case MODE_MERGE:
+      if constexpr (D == 128) {
+        if (merge_three_per_sm(p)) return launch_one<D, MODE_MERGE, EXT, true>(p, stream);
+      }
+      return launch_one<D, MODE_MERGE, EXT, false>(p, stream);
+    case MODE_STEP: return launch_one<D, MODE_STEP, EXT, false>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -667,9 +794,8 @@ cudaError_t launch_d(int mode, const DecodeParams& p, cudaStream_t stream) {
 }  // namespace
 
 size_t decode_smem_bytes(int mode, int dk, int dv, int ns, int C, int dlam, int klog_bytes, int ulog_bytes) {
-  (void)dlam;
   if (!decode_shape_built(dk, dv, ns)) return 0;
-  if (ns == 1 && dk == dv) return decode_layout(mode, dk, C, klog_bytes, ulog_bytes).total;
+  if (ns == 1 && dk == dv) return decode_layout(mode, dk, C, dlam, klog_bytes, ulog_bytes, false).total;
   return decode_smem_bytes_x(mode, dk, dv, ns, C, klog_bytes, ulog_bytes);
 }
 
