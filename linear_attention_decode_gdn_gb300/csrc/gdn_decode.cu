@@ -64,12 +64,17 @@ struct Layout {
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1u) / a * a; }
 
-// `r3`: the three-per-SM merge form.  With C <= 8 its U entries go to registers (each
-// thread the four columns it folds, the q-owning threads their readout column) and ell'
-// takes d_lambda entries, so that a 128-wide head's merge CTA under a per-head decay fits
-// three to an SM like dense and append.
+// Merge forms.  FORM_GENERAL serves every mode and shape.  The three-per-SM merge forms
+// (C <= 8, 128-wide heads) fit three CTAs to an SM like dense and append: their U entries go
+// to registers (each thread the four columns it folds, the q-owning threads their readout
+// column) instead of shared memory.  Under a per-head decay (FORM_R3) ell' takes one entry;
+// under a per-key decay (FORM_R3_PER_KEY) e^{ell'} q and e^{ell'} k are not stored but formed
+// where phase 1 reads them (the same products, so the same bits).
+constexpr int FORM_GENERAL = 0, FORM_R3 = 1, FORM_R3_PER_KEY = 2;
+
 __host__ __device__ inline Layout decode_layout(int mode, int D, int C, int dlam, int klog_bytes, int ulog_bytes,
-                                                bool r3) {
+                                                int form) {
+  const bool r3 = form != FORM_GENERAL;
   Layout L{};
   const bool has_log = mode != MODE_DENSE;
   const bool can_merge = mode == MODE_MERGE || mode == MODE_STEP;
@@ -84,9 +89,16 @@ __host__ __device__ inline Layout decode_layout(int mode, int D, int C, int dlam
   off += 64;
   L.scal = off;
   off += 128;
-  L.vec = off;  // q (later b), k, q*dec, k*dec, ell', [dec]  (r3: ..., dec, ell' of d_lambda entries)
-  off += static_cast<uint32_t>(D * 4 * (writes_state ? 5 : 4)) +
-         (r3 ? align_up(static_cast<uint32_t>(dlam * 4), 16u) : static_cast<uint32_t>(D * 4));
+  // q (later b), k, q*dec, k*dec, ell', [dec]; FORM_R3: q, k, q*dec, k*dec, dec, ell' (d_lambda
+  // entries); FORM_R3_PER_KEY: q, k, dec, ell'.  (The per-key form launches only with
+  // d_lambda > 1; the test stays a run-time one, like `ureg` in the kernel: that instance
+  // measured about 10% faster so.)
+  L.vec = off;
+  if (form == FORM_R3_PER_KEY && dlam > 1)
+    off += static_cast<uint32_t>(D * 4 * 4);
+  else
+    off += static_cast<uint32_t>(D * 4 * (writes_state ? 5 : 4)) +
+           (r3 ? align_up(static_cast<uint32_t>(dlam * 4), 16u) : static_cast<uint32_t>(D * 4));
   // K_log entries while the coefficients are formed, then the cross-warp partial sums.
   const uint32_t kbytes = has_log ? static_cast<uint32_t>(C * D * klog_bytes) : 0u;
   const uint32_t redbytes = static_cast<uint32_t>(8 * D * 4);
@@ -104,14 +116,15 @@ __host__ __device__ inline Layout decode_layout(int mode, int D, int C, int dlam
 }
 
 // The auto step carries both paths; its register cap keeps two CTAs per SM (its shared
-// memory allows two).  The three-per-SM merge form (R3, layout above) caps registers for
-// three: with a third CTA resident, the fold's arithmetic hides behind the other CTAs'
-// copies.  The other instances take no minimum (0: none).  EXT instances carry the KDA gate
+// memory allows two).  The three-per-SM merge forms (layout above) cap registers for three:
+// with a third CTA resident, the fold's arithmetic hides behind the other CTAs' copies.  The
+// other instances take no minimum (0: none).  EXT instances carry the KDA gate
 // parametrisation and output epilogue; the others compile them out.
-template <int D, int MODE, bool EXT, bool R3>
-__global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : (R3 ? 3 : 0))
+template <int D, int MODE, bool EXT, int FORM>
+__global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : (FORM != FORM_GENERAL ? 3 : 0))
     gdn_decode_kernel(const DecodeParams p) {
-  static_assert(!R3 || MODE == MODE_MERGE, "the three-per-SM form is a merge form");
+  static_assert(FORM == FORM_GENERAL || MODE == MODE_MERGE, "the three-per-SM forms are merge forms");
+  constexpr bool R3 = FORM != FORM_GENERAL;
   extern __shared__ __align__(128) unsigned char smem[];
 
   constexpr int NCHUNK = (D >= 128) ? 4 : 1;       // TMA row chunks of the tile
@@ -156,11 +169,13 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : (R3 ? 3 : 0
   const uint32_t fl = p.flags;
   const int klb = (fl & GDN_KLOG_FP32) ? 4 : 2;
   const int ulb = (fl & GDN_ULOG_BF16) ? 2 : 4;
-  const Layout L = decode_layout(MODE, D, C, dlam, klb, ulb, R3);
-  // U entries in registers.  The host launches R3 only with C <= 8; the test stays a run-time
+  const Layout L = decode_layout(MODE, D, C, dlam, klb, ulb, FORM);
+  // U entries in registers.  The host launches the R3 forms only with C <= 8; the test stays a run-time
   // one on purpose: with the shared-memory path compiled in as well, the instance fits its
   // 72 registers without spilling and measured about 8% faster than with it compiled out.
   const bool ureg = R3 && C <= 8;
+  // (likewise the per-key form's test of d_lambda: it launches only with d_lambda > 1)
+  const bool pk3 = FORM == FORM_R3_PER_KEY && dlam > 1;
   float* tile = reinterpret_cast<float*>(smem + L.tile);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   int* scal_i = reinterpret_cast<int*>(smem + L.scal);             // [0] L on entry, [1] status bits
@@ -171,8 +186,8 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : (R3 ? 3 : 0
   float* k_s = q_s + D;
   float* qdec_s = q_s + 2 * D;
   float* kdec_s = q_s + 3 * D;
-  float* ellp_s = q_s + (R3 ? 5 : 4) * D;  // (R3: d_lambda entries, last)
-  float* dec_s = q_s + (R3 ? 4 : 5) * D;   // only when the state is written
+  float* ellp_s = q_s + (pk3 ? 3 : (R3 ? 5 : 4)) * D;  // (R3: d_lambda entries, last)
+  float* dec_s = q_s + (pk3 ? 2 : (R3 ? 4 : 5)) * D;   // only when the state is written
   unsigned char* uni = smem + L.uni;
   float* red = reinterpret_cast<float*>(uni);
   float* u_s = reinterpret_cast<float*>(smem + L.us);  // U entries (fp32, or bf16 bits)
@@ -316,12 +331,12 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : (R3 ? 3 : 0
   if (is_q) {
     const float dcy = expf(ellp);
     q_s[ii] = x;
-    qdec_s[ii] = x * dcy;
+    if (!pk3) qdec_s[ii] = x * dcy;
     if (MODE != MODE_APPEND) dec_s[ii] = dcy;
     if (ii < dlam) ellp_s[ii] = ellp;
   } else if (is_k) {
     k_s[ii] = x;
-    kdec_s[ii] = x * expf(ellp);
+    if (!pk3) kdec_s[ii] = x * expf(ellp);
   }
   __syncthreads();  // (A) raw and decayed q, k, decays, norm partials, L and status bits
   if (ctrl) return;  // from here on only the compute warps (named barrier 1)
@@ -437,7 +452,7 @@ __global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : (R3 ? 3 : 0
       const int r = it * RPI + warp * RPW + rsub;
       if (r < D) {
         const float4 s = tile4[r * VPR + c4];
-        const float kd = kdec_s[r], qd = qdec_s[r];
+        const float kd = pk3 ? k_s[r] * dec_s[r] : kdec_s[r], qd = pk3 ? q_s[r] * dec_s[r] : qdec_s[r];
         ak[0] = fmaf(s.x, kd, ak[0]);
         ak[1] = fmaf(s.y, kd, ak[1]);
         ak[2] = fmaf(s.z, kd, ak[2]);
@@ -696,23 +711,23 @@ int sm_count(int dev) {
 }
 
 
-template <int D, int MODE, bool EXT, bool R3>
+template <int D, int MODE, bool EXT, int FORM>
 cudaError_t launch_one(const DecodeParams& p, cudaStream_t stream) {
   static std::atomic<uint32_t> configured[kMaxDevices];
   const int klb = (p.flags & GDN_KLOG_FP32) ? 4 : 2;
   const int ulb = (p.flags & GDN_ULOG_BF16) ? 2 : 4;
-  const Layout L = decode_layout(MODE, D, p.C, p.dlam, klb, ulb, R3);
+  const Layout L = decode_layout(MODE, D, p.C, p.dlam, klb, ulb, FORM);
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (configured[dev].load(std::memory_order_relaxed) < L.total) {
-    err = cudaFuncSetAttribute(gdn_decode_kernel<D, MODE, EXT, R3>,
+    err = cudaFuncSetAttribute(gdn_decode_kernel<D, MODE, EXT, FORM>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(L.total));
     if (err != cudaSuccess) return err;
     // several 64 KiB-tile CTAs per SM only fit with the whole L1/shared array as shared memory
-    err = cudaFuncSetAttribute(gdn_decode_kernel<D, MODE, EXT, R3>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    err = cudaFuncSetAttribute(gdn_decode_kernel<D, MODE, EXT, FORM>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                static_cast<int>(cudaSharedmemCarveoutMaxShared));
     if (err != cudaSuccess) return err;
     configured[dev].store(L.total, std::memory_order_relaxed);
@@ -723,7 +738,7 @@ cudaError_t launch_one(const DecodeParams& p, cudaStream_t stream) {
   uint64_t rc = resident[dev].load(std::memory_order_relaxed);
   if ((rc >> 32) != L.total) {
     int per_sm = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gdn_decode_kernel<D, MODE, EXT, R3>, NT_DECODE,
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gdn_decode_kernel<D, MODE, EXT, FORM>, NT_DECODE,
                                                         L.total);
     if (err != cudaSuccess) return err;
     rc = (static_cast<uint64_t>(L.total) << 32) | static_cast<uint32_t>(per_sm > 0 ? per_sm : 1);
@@ -742,45 +757,52 @@ cudaError_t launch_one(const DecodeParams& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, gdn_decode_kernel<D, MODE, EXT, R3>, q);
+  err = cudaLaunchKernelEx(&cfg, gdn_decode_kernel<D, MODE, EXT, FORM>, q);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
-// Whether a merge of a 128-wide head takes the R3 form: C <= 8 and its layout fits three
-// CTAs in the SM's shared memory (each CTA also takes the per-block reservation).  Where
-// it does not (C > 8, or a per-key decay whose layout comes out larger), the general form
-// runs at two CTAs per SM without the register cap.
-bool merge_three_per_sm(const DecodeParams& p) {
-  if (p.D != 128 || p.C > 8) return false;
+// The form a merge of a 128-wide head takes: a three-per-SM form when C <= 8, the U log is
+// fp32 and its layout fits three CTAs in the SM's shared memory (each CTA also takes the
+// per-block reservation); otherwise the general form, two CTAs per SM without the register
+// cap.  (A bf16 U log unpacks every entry in the fold: the one such workload, RWKV6, measured
+// its merge 5% slower in the three-per-SM form.)
+int merge_form(const DecodeParams& p) {
+  if (p.D != 128 || p.C > 8 || (p.flags & GDN_ULOG_BF16)) return FORM_GENERAL;
+  const int form = p.dlam == 1 ? FORM_R3 : FORM_R3_PER_KEY;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FORM_GENERAL;
   static std::atomic<int> budget[kMaxDevices];
   int b = budget[dev].load(std::memory_order_relaxed);
   if (b == 0) {
     int per_sm = 0, reserved = 0;
     if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
-      return false;
+      return FORM_GENERAL;
     b = per_sm / 3 - reserved;
     budget[dev].store(b > 0 ? b : -1, std::memory_order_relaxed);
   }
   const int klb = (p.flags & GDN_KLOG_FP32) ? 4 : 2;
   const int ulb = (p.flags & GDN_ULOG_BF16) ? 2 : 4;
-  return b > 0 && decode_layout(MODE_MERGE, 128, p.C, p.dlam, klb, ulb, true).total <= static_cast<uint32_t>(b);
+  const bool fits = b > 0 && decode_layout(MODE_MERGE, 128, p.C, p.dlam, klb, ulb, form).total <= static_cast<uint32_t>(b);
+  return fits ? form : FORM_GENERAL;
 }
 
 template <int D, bool EXT>
 cudaError_t launch_de(int mode, const DecodeParams& p, cudaStream_t stream) {
   switch (mode) {
-    case MODE_DENSE: return launch_one<D, MODE_DENSE, EXT, false>(p, stream);
-    case MODE_APPEND: return launch_one<D, MODE_APPEND, EXT, false>(p, stream);
+    case MODE_DENSE: return launch_one<D, MODE_DENSE, EXT, FORM_GENERAL>(p, stream);
+    case MODE_APPEND: return launch_one<D, MODE_APPEND, EXT, FORM_GENERAL>(p, stream);
     case MODE_MERGE:
       if constexpr (D == 128) {
-        if (merge_three_per_sm(p)) return launch_one<D, MODE_MERGE, EXT, true>(p, stream);
+        switch (merge_form(p)) {
+          case FORM_R3: return launch_one<D, MODE_MERGE, EXT, FORM_R3>(p, stream);
+          case FORM_R3_PER_KEY: return launch_one<D, MODE_MERGE, EXT, FORM_R3_PER_KEY>(p, stream);
+          default: break;
+        }
       }
-      return launch_one<D, MODE_MERGE, EXT, false>(p, stream);
-    case MODE_STEP: return launch_one<D, MODE_STEP, EXT, false>(p, stream);
+      return launch_one<D, MODE_MERGE, EXT, FORM_GENERAL>(p, stream);
+    case MODE_STEP: return launch_one<D, MODE_STEP, EXT, FORM_GENERAL>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -795,7 +817,7 @@ cudaError_t launch_d(int mode, const DecodeParams& p, cudaStream_t stream) {
 
 size_t decode_smem_bytes(int mode, int dk, int dv, int ns, int C, int dlam, int klog_bytes, int ulog_bytes) {
   if (!decode_shape_built(dk, dv, ns)) return 0;
-  if (ns == 1 && dk == dv) return decode_layout(mode, dk, C, dlam, klog_bytes, ulog_bytes, false).total;
+  if (ns == 1 && dk == dv) return decode_layout(mode, dk, C, dlam, klog_bytes, ulog_bytes, FORM_GENERAL).total;
   return decode_smem_bytes_x(mode, dk, dv, ns, C, klog_bytes, ulog_bytes);
 }
 
