@@ -129,7 +129,7 @@ def pin_delta_wy(lib, T=64, dk=16, dv=16, C=16, per_key=False, seed=1):
 
 def pin_transition_form(lib, dk=7, dv=5, seed=2):
     """One step equals the affine form S_t = (I - beta k k^T) D(lambda) S_{t-1} + beta k v^T
-    (the state-transition form the benchmark spec states, with D on the rows)."""
+    (the state-transition form of the gated delta rule, with D on the rows)."""
     r = _rng(seed)
     for per_key in (False, True):
         S0 = r.standard_normal((dk, dv))
