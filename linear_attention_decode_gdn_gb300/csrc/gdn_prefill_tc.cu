@@ -65,8 +65,7 @@ constexpr uint32_t OFF_A = OFF_V + TC_C * TD * 4;        // A column-major [s][T
 constexpr uint32_t OFF_ST = OFF_A + TC_C * TC_ATS * 4;   // staging: q, k, v rows
 constexpr uint32_t OFF_G = OFF_ST + 3 * TC_C * ST_ROW;   // gamma, beta, e^gamma, e^{gamma_C - gamma},
                                                          // key and query scale factors, e^-gamma, flags
-constexpr uint32_t OFF_OB = OFF_G + 8 * TC_C * 4;        // output rows of a chunk, [t][128] fp32
-constexpr uint32_t OFF_BAR = OFF_OB + TC_C * TD * 4;     // mbarriers: ps, p1, p2, drain, then one
+constexpr uint32_t OFF_BAR = OFF_G + 8 * TC_C * 4;       // mbarriers: ps, p1, p2, drain, then one
                                                          // per compute warp for its staged rows
 constexpr uint32_t OFF_TMEM = OFF_BAR + 12 * 8;
 constexpr uint32_t TC_SMEM = OFF_TMEM + 16;
@@ -113,38 +112,6 @@ __device__ __forceinline__ float4 staged4(const unsigned char* row, int g, bool 
   return *reinterpret_cast<const float4*>(row + 16 * g);
 }
 
-
-// TMA bulk store shared -> global (16-byte aligned, size a multiple of 16) and its group
-// commit, called by a whole warp with warp-uniform operands: the lowest lane issues (so the
-// same lane always owns the bulk group and its waits). The waits, by that lane: until the
-// shared-memory source of every committed store has been read, or until every committed
-// store has completed.
-__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
-  asm volatile(
-      "{\n .reg .pred e;\n .reg .b32 l;\n elect.sync l|e, 0xffffffff;\n"
-      " @e cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n}\n" ::"l"(gdst),
-      "r"(smem_addr(ssrc)), "r"(bytes)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("{\n .reg .pred e;\n .reg .b32 l;\n elect.sync l|e, 0xffffffff;\n @e cp.async.bulk.commit_group;\n}\n" :::
-                   "memory");
-}
-__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-// Named barrier over warps 4-7 (128 threads); the second form returns the OR of `pred`
-// over them.
-__device__ __forceinline__ void upper_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
-__device__ __forceinline__ bool upper_sync_or(bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred a, o;\n setp.ne.u32 a, %1, 0;\n bar.red.or.pred o, 2, 128, a;\n selp.u32 %0, 1, 0, o;\n}\n"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(pred))
-      : "memory");
-  return r != 0u;
-}
 
 // Bounded wait for phase `parity` of `bar`, the same answer in every lane of the warp (the
 // TMEM loads and stores that follow are warp-collective).
@@ -201,39 +168,38 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
 
   bool bad = false;
   if (tid == 0) {
-    for (int i = 0; i < 12; ++i) mbar_init(&bars[i], 1u);
+    for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1u);
+    for (int i = 4; i < 12; ++i) mbar_init(&bars[i], 32u);  // staging: one cp.async arrival per lane
     fence_mbar_init();
   }
   __syncthreads();
 
-  // ---- raw token rows of the chunk at t0 into the staging rows (TMA bulk copies) --------------
+  // ---- raw token rows of the chunk at t0 into the staging rows (16-byte cp.async) ------------
   // Each compute warp copies the rows it reads itself (warps 0-3: key and value rows
-  // 8w..8w+7; warps 4-7: query rows 8(w-4)..), one bulk copy per row issued by an elected
-  // lane and counted on the warp's own mbarrier, so the token stage needs no block barrier
-  // before it reads them. Warp 4 loads the chunk's gates into registers (lane = token).
-  const uint64_t pol_once = l2_policy_evict_first();
+  // 8w..8w+7; warps 4-7: query rows 8(w-4)..), every lane a share of the 16-byte pieces, each
+  // lane then arriving once on the warp's own mbarrier when its copies have landed, so the
+  // token stage needs no block barrier before it reads them.  (One TMA bulk copy per row,
+  // issued by one lane, cost about 2.5 K cycles a chunk in issue alone.)  Warp 4 loads the
+  // chunk's gates into registers (lane = token).
   uint32_t pf_par = 0;   // phase of this warp's staging barrier the next token stage waits for
   bool pf_pending = false;
   float pf_lam = 0.0f, pf_beta = 0.0f;
   auto prefetch = [&](int t0, int n) {
     if (warp >= ISSUER) return;
-    const uint32_t rowb = static_cast<uint32_t>(TD) * esz;
+    const int cpr = TD * static_cast<int>(esz) / 16;  // 16-byte pieces per row
     const int nlive = n - 8 * wq < 0 ? 0 : (n - 8 * wq > 8 ? 8 : n - 8 * wq);
     const int ntens = warp < 4 ? 2 : 1;
-    tc::expect_tx(&pbar[warp], static_cast<uint32_t>(nlive * ntens) * rowb);
-    for (int r = 0; r < nlive; ++r) {
+    const int total = ntens * nlive * cpr;
+    for (int idx = lane; idx < total; idx += 32) {
+      const int piece = idx % cpr, kr = idx / cpr;
+      const int k = kr / nlive, r = kr - k * nlive;
       const int t = 8 * wq + r;
-      const size_t off = (((static_cast<size_t>(b) * T + t0 + t) * p.H + h) * TD) * esz;
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        if (k < ntens) {
-          const int tensor = warp >= 4 ? 0 : (k == 0 ? 1 : 2);  // staging block: 0 q, 1 k, 2 v
-          const void* base = tensor == 0 ? p.q : (tensor == 1 ? p.k : p.v);
-          tc::bulk_load(smem + OFF_ST + (tensor * TC_C + t) * ST_ROW, static_cast<const unsigned char*>(base) + off,
-                        rowb, &pbar[warp], pol_once);
-        }
-      }
+      const int tensor = warp >= 4 ? 0 : (k == 0 ? 1 : 2);  // staging block: 0 q, 1 k, 2 v
+      const void* base = tensor == 0 ? p.q : (tensor == 1 ? p.k : p.v);
+      const size_t off = (((static_cast<size_t>(b) * T + t0 + t) * p.H + h) * TD) * esz + 16u * piece;
+      cp_async16(smem + OFF_ST + (tensor * TC_C + t) * ST_ROW + 16 * piece, static_cast<const unsigned char*>(base) + off);
     }
+    cp_async_arrive(&pbar[warp]);
     if (warp == 4) {
       const size_t gi = (static_cast<size_t>(b) * T + t0 + lane) * p.H + h;
       pf_lam = lane < n ? __ldg(p.lam + gi) : 0.0f;
@@ -376,27 +342,21 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
   int prev_t0 = 0, prev_n = 0;
   uint32_t it = 0;
 
-  // readout of a finished chunk from its TMEM output buffer (warps 4-7): O^T[j][t] into the
-  // shared output rows, then one TMA bulk store per position t < cn (512 bytes each, eight
-  // positions per warp). The rows are rewritten only once the previous chunk's stores have
-  // read them.
-  float* OB = reinterpret_cast<float*>(smem + OFF_OB);
+  // readout of a finished chunk from its TMEM output buffer (warps 4-7): lane j of warp 4 + w
+  // holds O^T[32 w + j][t]; for each position t < cn the warp stores its 32 columns of the
+  // output row (128 contiguous bytes).  (One TMA bulk store per row cost about 2 K cycles a
+  // chunk in issue.)
   auto store_output = [&](uint32_t d1, int ct0, int cn) {
-    if (lane == 0) bulk_wait_read();  // this warp's stores of the previous chunk have read their rows
-    upper_sync();
+    float* orow = p.o + ((static_cast<size_t>(b) * T + ct0) * p.H + h) * TD + j;
+    const size_t tstride = static_cast<size_t>(p.H) * TD;
 #pragma unroll
     for (int h2 = 0; h2 < 2; ++h2) {
       float o[16];
       tc::ld16(tmem + lb + d1 + TC_C + 16 * h2, o);
 #pragma unroll
-      for (int k = 0; k < 16; ++k) OB[(16 * h2 + k) * TD + j] = o[k];
+      for (int k = 0; k < 16; ++k)
+        if (16 * h2 + k < cn) orow[(16 * h2 + k) * tstride] = o[k];
     }
-    tc::fence_smem_to_async();
-    upper_sync();
-    // warp 4 + w stores rows 8w .. 8w+7 (lane 0 issues, elected; the group is lane 0's)
-    for (int t = 8 * wq; t < 8 * wq + 8 && t < cn; ++t)
-      bulk_store(p.o + ((static_cast<size_t>(b) * T + ct0 + t) * p.H + h) * TD, OB + t * TD, TD * 4);
-    bulk_commit();
   };
 
   while (true) {
@@ -451,52 +411,55 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
                      (gidx | i) != 0);
       }
       tc::commit(&bars[1]);
-    } else if (warp >= 4) {
+    } else {
       // ---- A (strictly lower, times beta) and P (lower with the diagonal) from the pair sums
-      // (issued at the end of the token stage), while the state read runs. M = 64 accumulator:
-      // row m sits in lane 32 (m / 16) + m % 16, so warps 4, 5 hold the k.k rows
-      // t = 16 (w - 4) + lane and warps 6, 7 the q.k rows t = 16 (w - 6) + lane (lanes < 16)
+      // (issued at the end of the token stage), while the state read runs, on all eight compute
+      // warps. M = 64 accumulator: row m sits in lane 32 (m / 16) + m % 16, so warps w and w + 4
+      // (the same lane quarter) hold the k.k rows t = 16 (w % 2) + lane for w % 4 < 2 and the q.k
+      // rows for w % 4 >= 2 (lanes < 16). Warp group G = w / 4 takes the source tokens
+      // s = 16 G .. 16 G + 15: lanes < 16 the first eight, lanes >= 16 the last eight of their
+      // row (shuffled from lane - 16).
       if (!wait_warp(&bars[0], it & 1u)) bad = true;
       tc::fence_after_sync();
-      float ps[32];
-      {
-        float a0[16], a1[16];
-        tc::ld16(tmem + lb + TM_PS, a0);
-        tc::ld16(tmem + lb + TM_PS + 16, a1);
+      const int G = warp >> 2, half = lane >> 4;
+      float a16[16], ps[8];
+      tc::ld16(tmem + lb + TM_PS + 16 * G, a16);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          ps[k] = a0[k];
-          ps[16 + k] = a1[k];
-        }
+      for (int k = 0; k < 8; ++k) {
+        const float up = __shfl_sync(0xffffffffu, a16[8 + k], lane & 15);
+        ps[k] = half ? up : a16[k];
       }
       const bool split = *ratio_split != 0;
-      if (lane < 16) {
-        const int t = 16 * (warp & 1) + lane;
-        const float egt = eg[t], gt = gam[t];
-        if ((warp & 2) == 0) {
-          const float bt = bet[t] * skf[t];
-          if (split) {
+      const int t = 16 * (warp & 1) + (lane & 15);
+      const int sb = 16 * G + 8 * half;  // this thread's first source token
+      const float egt = eg[t], gt = gam[t];
+      if ((warp & 2) == 0) {
+        const float bt = bet[t] * skf[t];
+        if (split) {
 #pragma unroll
-            for (int s2 = 0; s2 < TC_C; ++s2)
-              A[s2 * TC_ATS + t] = (s2 < t && !plain) ? bt * (ps[s2] * skf[s2]) * (egt * ein[s2]) : 0.0f;
-          } else {
-#pragma unroll
-            for (int s2 = 0; s2 < TC_C; ++s2)
-              A[s2 * TC_ATS + t] = (s2 < t && !plain) ? bt * (ps[s2] * skf[s2]) * expf(gt - gam[s2]) : 0.0f;
+          for (int k = 0; k < 8; ++k) {
+            const int s2 = sb + k;
+            A[s2 * TC_ATS + t] = (s2 < t && !plain) ? bt * (ps[k] * skf[s2]) * (egt * ein[s2]) : 0.0f;
           }
         } else {
-          const float qt = sqf[t];
 #pragma unroll
-          for (int s4 = 0; s4 < TC_C; s4 += 4) {
-            float pv[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int s2 = s4 + k;
-              const float rr = split ? egt * ein[s2] : expf(gt - gam[s2]);
-              pv[k] = s2 <= t ? qt * (ps[s2] * skf[s2]) * rr : 0.0f;
-            }
-            store_split4(smem, OFF_PH, OFF_PL, kmaj_off(t, s4, P_LBO), pv[0], pv[1], pv[2], pv[3]);
+          for (int k = 0; k < 8; ++k) {
+            const int s2 = sb + k;
+            A[s2 * TC_ATS + t] = (s2 < t && !plain) ? bt * (ps[k] * skf[s2]) * expf(gt - gam[s2]) : 0.0f;
           }
+        }
+      } else {
+        const float qt = sqf[t];
+#pragma unroll
+        for (int s4 = 0; s4 < 8; s4 += 4) {
+          float pv[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int s2 = sb + s4 + k;
+            const float rr = split ? egt * ein[s2] : expf(gt - gam[s2]);
+            pv[k] = s2 <= t ? qt * (ps[s4 + k] * skf[s2]) * rr : 0.0f;
+          }
+          store_split4(smem, OFF_PH, OFF_PL, kmaj_off(t, sb + s4, P_LBO), pv[0], pv[1], pv[2], pv[3]);
         }
       }
     }
@@ -565,9 +528,8 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
           }
           tc::wait_st();
         }
-        // the previous chunk's output, from the other TMEM buffer, while the substitution
-        // runs (decided jointly by warps 4-7: the store synchronises them)
-        if (!upper_sync_or(bad) && it > 0) store_output(d1 == TM_D1 ? TM_D1B : TM_D1, prev_t0, prev_n);
+        // the previous chunk's output, from the other TMEM buffer, while the substitution runs
+        if (!bad && it > 0) store_output(d1 == TM_D1 ? TM_D1B : TM_D1, prev_t0, prev_n);
       }
     }
     tc::fence_smem_to_async();
@@ -607,7 +569,6 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
     if (!wait_warp(&bars[2], (it - 1) & 1u)) bad = true;
     tc::fence_after_sync();
   }
-  // decided for the whole CTA: the output store below synchronises warps 4-7
   bad = __syncthreads_or(bad) != 0;
   if (!bad && warp >= 4 && warp < ISSUER) store_output((it - 1) & 1u ? TM_D1B : TM_D1, prev_t0, prev_n);
   if (bad) {
@@ -627,7 +588,6 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
       for (int k = 0; k < 16; ++k) Sg[static_cast<size_t>(c0 + 16 * cc + k) * TD + j] = v[k];
     }
   }
-  if (warp >= 4 && warp < ISSUER && lane == 0) bulk_wait_all();  // the output rows are written before the CTA exits
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
