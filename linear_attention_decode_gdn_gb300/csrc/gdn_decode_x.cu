@@ -4,33 +4,16 @@
 // gdn_decode.cu (gdn_decode_kernel.cuh), separate translation unit so the two compile in
 // parallel.
 #include "gdn_decode_kernel.cuh"
+#include "gdn_tmap.h"
 
 namespace gdn {
 namespace shaped {
 
 cudaError_t encode_state_map(CUtensorMap* map, const float* pool, size_t rows, int DV, int box_cols, int box_rows) {
-  using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-  static std::atomic<Encode> fn{nullptr};
-  Encode f = fn.load(std::memory_order_relaxed);
-  if (f == nullptr) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    const cudaError_t err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q);
-    if (err != cudaSuccess) return err;
-    if (q != cudaDriverEntryPointSuccess || ptr == nullptr) return cudaErrorNotSupported;
-    f = reinterpret_cast<Encode>(ptr);
-    fn.store(f, std::memory_order_relaxed);
-  }
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(DV), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(DV) * 4u};
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
-  const cuuint32_t estr[2] = {1u, 1u};
-  const CUresult r = f(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(pool), dims, strides, box, estr,
-                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, pool, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 }  // namespace shaped

@@ -30,6 +30,7 @@
 #include <atomic>
 
 #include "gdn_tc.cuh"
+#include "gdn_tmap.h"
 
 namespace gdn {
 namespace {
@@ -47,9 +48,12 @@ constexpr uint32_t T128_LBO = (TD / 8) * 128;      // Khat^T, B^T:  128 x 32    
 constexpr uint32_t P_LBO = (TC_C / 8) * 128;       // P:            32 x 32      (512)
 constexpr uint32_t SBO = 128;
 
-// Staging rows of the raw token inputs, one chunk ahead: q, k, v rows of 128 elements (bf16 or
-// fp32) at a padded stride.
-constexpr uint32_t ST_ROW = 128 * 4 + 16;
+// Staging of the raw token inputs, one chunk ahead: per tensor (q, k, v) the chunk's 32 rows
+// of 128 elements as 128-byte column boxes ([box][row][128 bytes]: 2 boxes for bf16, 4 for
+// fp32), each written by one 3-D TMA copy with the 128-byte swizzle (16-byte chunk c of row t
+// at chunk position c ^ (t % 8)), so that both the row-wise token stage and the copies see no
+// bank conflicts.
+constexpr uint32_t ST_BOX = TC_C * 128;  // bytes of one box
 
 // shared-memory layout (bytes)
 constexpr uint32_t OFF_XH = 0;                      // [K; Q] hi  64 x 128
@@ -62,8 +66,8 @@ constexpr uint32_t OFF_PH = OFF_BL + TD * TC_C * 4;      // P hi 32 x 32
 constexpr uint32_t OFF_PL = OFF_PH + TC_C * TC_C * 4;
 constexpr uint32_t OFF_V = OFF_PL + TC_C * TC_C * 4;     // V row-major 32 x 128 fp32
 constexpr uint32_t OFF_A = OFF_V + TC_C * TD * 4;        // A column-major [s][TC_ATS]
-constexpr uint32_t OFF_ST = OFF_A + TC_C * TC_ATS * 4;   // staging: q, k, v rows
-constexpr uint32_t OFF_G = OFF_ST + 3 * TC_C * ST_ROW;   // gamma, beta, e^gamma, e^{gamma_C - gamma},
+constexpr uint32_t OFF_ST = (OFF_A + TC_C * TC_ATS * 4 + 1023u) & ~1023u;  // staging (1024-aligned: swizzle atoms)
+constexpr uint32_t OFF_G = OFF_ST + 3 * TC_C * TD * 4;   // gamma, beta, e^gamma, e^{gamma_C - gamma},
                                                          // key and query scale factors, e^-gamma, flags
 constexpr uint32_t OFF_BAR = OFF_G + 8 * TC_C * 4;       // mbarriers: ps, p1, p2, drain, then one
                                                          // per compute warp for its staged rows
@@ -102,16 +106,38 @@ __device__ __forceinline__ void store_split1(unsigned char* smem, uint32_t hi_ba
   *reinterpret_cast<float*>(smem + lo_base + off) = a - ha;
 }
 
-// four elements 4g .. 4g+3 of a staged row (bf16 or fp32), as float
-__device__ __forceinline__ float4 staged4(const unsigned char* row, int g, bool bf16) {
+// Elements 4g .. 4g+3 of row t of staged tensor `tensor` (0 q, 1 k, 2 v; bf16 or fp32), as
+// float: the 128-byte box that holds them, then the swizzled 16-byte chunk.
+__device__ __forceinline__ float4 staged4(const unsigned char* st, int tensor, int t, int g, bool bf16) {
+  const uint32_t esz = bf16 ? 2u : 4u;
+  const uint32_t byte = 4u * static_cast<uint32_t>(g) * esz;
+  const uint32_t inb = byte & 127u;
+  const unsigned char* at = st + static_cast<uint32_t>(tensor) * (TC_C * TD * esz) + (byte >> 7) * ST_BOX +
+                            static_cast<uint32_t>(t) * 128u +
+                            ((((inb >> 4) ^ (static_cast<uint32_t>(t) & 7u)) << 4) | (inb & 15u));
   if (bf16) {
-    const uint2 u = *reinterpret_cast<const uint2*>(row + 8 * g);
+    const uint2 u = *reinterpret_cast<const uint2*>(at);
     return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
                        __uint_as_float(u.y & 0xffff0000u));
   }
-  return *reinterpret_cast<const float4*>(row + 16 * g);
+  return *reinterpret_cast<const float4*>(at);
 }
 
+// The token tensors q, k, v as 3-D tensor maps (element, head, position over all requests):
+// dims {128, H, B*T}, boxes {128 bytes of elements, 1, 32}, 128-byte swizzle.
+struct TokenMaps {
+  CUtensorMap q, k, v;
+};
+
+// One 3-D box of a tensor map into shared memory, completion counted on `bar`; called by a
+// whole warp with warp-uniform operands, one elected lane issues.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n .reg .b32 l;\n elect.sync l|e, 0xffffffff;\n"
+      " @e cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n}\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+      : "memory");
+}
 
 // Bounded wait for phase `parity` of `bar`, the same answer in every lane of the warp (the
 // TMEM loads and stores that follow are warp-collective).
@@ -119,7 +145,7 @@ __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
-__global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodeParams p, const __grid_constant__ TokenMaps maps) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.x / p.H;
@@ -161,51 +187,46 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
   float* V = reinterpret_cast<float*>(smem + OFF_V);
   float* A = reinterpret_cast<float*>(smem + OFF_A);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint64_t* pbar = bars + 4;  // staged rows of compute warp w: pbar[w]
+  uint64_t* stbar = bars + 4;  // the staging copies of a chunk
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
   const uint32_t esz = bf16 ? 2u : 4u;
   const int wq = warp & 3;
 
   bool bad = false;
   if (tid == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1u);
-    for (int i = 4; i < 12; ++i) mbar_init(&bars[i], 32u);  // staging: one cp.async arrival per lane
+    for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1u);
     fence_mbar_init();
   }
   __syncthreads();
 
-  // ---- raw token rows of the chunk at t0 into the staging rows (16-byte cp.async) ------------
-  // Each compute warp copies the rows it reads itself (warps 0-3: key and value rows
-  // 8w..8w+7; warps 4-7: query rows 8(w-4)..), every lane a share of the 16-byte pieces, each
-  // lane then arriving once on the warp's own mbarrier when its copies have landed, so the
-  // token stage needs no block barrier before it reads them.  (One TMA bulk copy per row,
-  // issued by one lane, cost about 2.5 K cycles a chunk in issue alone.)  Warp 4 loads the
-  // chunk's gates into registers (lane = token).
-  uint32_t pf_par = 0;   // phase of this warp's staging barrier the next token stage waits for
-  bool pf_pending = false;
+  // ---- raw token rows of the chunk at t0 into the staging boxes (3-D TMA) --------------------
+  // The MMA-issuing warp copies the chunk's q, k and v rows as 128-byte column boxes of the
+  // token tensor maps (one copy per box, all counted on one mbarrier); it is idle while the
+  // compute warps run the token stage, so the copies cost the chunk's critical path nothing.
+  // (Per-row bulk copies, and per-lane 16-byte cp.async, each held the compute warps about
+  // 2.5 K cycles a chunk.)  Warp 4 loads the chunk's gates into registers (lane = token).
+  uint32_t st_par = 0;     // (compute warps) phase of the staging barrier the next token stage waits for
+  uint32_t st_loads = 0;   // (issuer) staging loads issued; the last one completes phase (st_loads - 1) & 1
   float pf_lam = 0.0f, pf_beta = 0.0f;
+  const int nbox = bf16 ? 2 : 4;
   auto prefetch = [&](int t0, int n) {
-    if (warp >= ISSUER) return;
-    const int cpr = TD * static_cast<int>(esz) / 16;  // 16-byte pieces per row
-    const int nlive = n - 8 * wq < 0 ? 0 : (n - 8 * wq > 8 ? 8 : n - 8 * wq);
-    const int ntens = warp < 4 ? 2 : 1;
-    const int total = ntens * nlive * cpr;
-    for (int idx = lane; idx < total; idx += 32) {
-      const int piece = idx % cpr, kr = idx / cpr;
-      const int k = kr / nlive, r = kr - k * nlive;
-      const int t = 8 * wq + r;
-      const int tensor = warp >= 4 ? 0 : (k == 0 ? 1 : 2);  // staging block: 0 q, 1 k, 2 v
-      const void* base = tensor == 0 ? p.q : (tensor == 1 ? p.k : p.v);
-      const size_t off = (((static_cast<size_t>(b) * T + t0 + t) * p.H + h) * TD) * esz + 16u * piece;
-      cp_async16(smem + OFF_ST + (tensor * TC_C + t) * ST_ROW + 16 * piece, static_cast<const unsigned char*>(base) + off);
+    if (warp == ISSUER) {
+      tc::expect_tx(stbar, 3u * static_cast<uint32_t>(nbox) * ST_BOX);
+      const int z = b * T + t0;
+#pragma unroll
+      for (int tensor = 0; tensor < 3; ++tensor) {
+        const CUtensorMap* map = tensor == 0 ? &maps.q : (tensor == 1 ? &maps.k : &maps.v);
+        for (int bx = 0; bx < nbox; ++bx)
+          tma_load_3d(smem_addr(smem + OFF_ST + static_cast<uint32_t>(tensor) * (TC_C * TD * esz) + bx * ST_BOX), map,
+                      bx * static_cast<int>(128u / esz), h, z, stbar);
+      }
+      ++st_loads;
     }
-    cp_async_arrive(&pbar[warp]);
     if (warp == 4) {
       const size_t gi = (static_cast<size_t>(b) * T + t0 + lane) * p.H + h;
       pf_lam = lane < n ? __ldg(p.lam + gi) : 0.0f;
       pf_beta = lane < n ? (p.beta ? __ldg(p.beta + gi) : 1.0f) : 0.0f;
     }
-    pf_pending = true;
   };
   prefetch(0, n_tok < TC_C ? n_tok : TC_C);
 
@@ -239,7 +260,6 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
     tc::wait_st();
   }
 
-  float kreg[8][4];  // warps 0-3: the normalised key rows of the chunk (for the Khat tile)
 
   // ---- token stage (from the staging rows): [K; Q] tiles, V, gates, norm scales -------------
   // warps 0-3: key rows t = 8 w + (lane & 7), channel groups g = (lane >> 3) + 4 i (4 channels
@@ -248,17 +268,16 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
   // Ends with the pair-sum MMAs of the chunk issued (they need nothing of the state).
   auto token_stage = [&](int n) {
    if (warp < ISSUER) {
-    if (!wait_warp(&pbar[warp], pf_par)) bad = true;  // this warp's own rows have landed
-    pf_par ^= 1u;
-    pf_pending = false;
+    if (!wait_warp(stbar, st_par)) bad = true;  // the chunk's rows have landed
+    st_par ^= 1u;
     const int t = 8 * wq + (lane & 7);
     const int g0 = lane >> 3;
     const bool live = t < n;
     const bool isk = warp < 4;
-    const unsigned char* row = smem + OFF_ST + ((isk ? TC_C : 0) + t) * ST_ROW;
+    const unsigned char* st = smem + OFF_ST;
     float4 x[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) x[i] = live ? staged4(row, g0 + 4 * i, bf16) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < 8; ++i) x[i] = live ? staged4(st, isk ? 1 : 0, t, g0 + 4 * i, bf16) : make_float4(0.f, 0.f, 0.f, 0.f);
     if (warp == 4) {  // gates of the chunk, lane = token
       const bool lv = lane < n;
       float lam = pf_lam, be = pf_beta;
@@ -299,19 +318,13 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
         *reinterpret_cast<float4*>(smem + OFF_XH + kmaj_off(r, 4 * g, X_LBO)) = x[i];
       else
         store_split4(smem, OFF_XH, OFF_XL, kmaj_off(r, 4 * g, X_LBO), a0, a1, a2, a3);
-      if (isk) {
-        kreg[i][0] = a0;
-        kreg[i][1] = a1;
-        kreg[i][2] = a2;
-        kreg[i][3] = a3;
-      }
     }
     if (isk) {
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int tv = 8 * wq + u;
         reinterpret_cast<float4*>(V + tv * TD)[lane] =
-            tv < n ? staged4(smem + OFF_ST + (2 * TC_C + tv) * ST_ROW, lane, bf16) : make_float4(0.f, 0.f, 0.f, 0.f);
+            tv < n ? staged4(st, 2, tv, lane, bf16) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
    }
@@ -379,17 +392,34 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
       }
     }
     if (warp < 4) {
-      // Khat^T tile (row c, column s): k_s[c] e^{gamma_C - gamma_s}
+      // Khat^T tile (row c, column s): k_s[c] e^{gamma_C - gamma_s}, the normalised key read
+      // back from the [K; Q] tile this thread wrote in the token stage (the raw key times its
+      // scale for exact inputs, else hi + lo: the same values, kept out of registers across
+      // the chunk)
       const int s = 8 * warp + (lane & 7);
-      const float f = ek[s];
+      const float f = ek[s], sk = skf[s];
       const int g0 = lane >> 3;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int c = 4 * (g0 + 4 * i);
-        store_split1(smem, OFF_KH, OFF_KL, kmaj_off(c + 0, s, T128_LBO), kreg[i][0] * f);
-        store_split1(smem, OFF_KH, OFF_KL, kmaj_off(c + 1, s, T128_LBO), kreg[i][1] * f);
-        store_split1(smem, OFF_KH, OFF_KL, kmaj_off(c + 2, s, T128_LBO), kreg[i][2] * f);
-        store_split1(smem, OFF_KH, OFF_KL, kmaj_off(c + 3, s, T128_LBO), kreg[i][3] * f);
+        const uint32_t xo = kmaj_off(s, c, X_LBO);
+        float4 a = *reinterpret_cast<const float4*>(smem + OFF_XH + xo);
+        if (exact) {
+          a.x *= sk;
+          a.y *= sk;
+          a.z *= sk;
+          a.w *= sk;
+        } else {
+          const float4 l = *reinterpret_cast<const float4*>(smem + OFF_XL + xo);
+          a.x += l.x;
+          a.y += l.y;
+          a.z += l.z;
+          a.w += l.w;
+        }
+        store_split1(smem, OFF_KH, OFF_KL, kmaj_off(c + 0, s, T128_LBO), a.x * f);
+        store_split1(smem, OFF_KH, OFF_KL, kmaj_off(c + 1, s, T128_LBO), a.y * f);
+        store_split1(smem, OFF_KH, OFF_KL, kmaj_off(c + 2, s, T128_LBO), a.z * f);
+        store_split1(smem, OFF_KH, OFF_KL, kmaj_off(c + 3, s, T128_LBO), a.w * f);
       }
     }
     tc::fence_smem_to_async();
@@ -575,7 +605,7 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
     // let every MMA this CTA issued finish (bounded) before the tensor memory is released
     if (warp == ISSUER) tc::commit(&bars[3]);
     (void)mbar_wait(&bars[3], 0u);
-    if (pf_pending && warp < ISSUER) (void)mbar_wait(&pbar[warp], pf_par);  // staged rows in flight
+    if (warp == ISSUER && st_loads > 0) (void)mbar_wait(stbar, (st_loads - 1u) & 1u);  // staging copies in flight
     if (tid == 0) atomic_status(p.status, GDN_STATUS_TIMEOUT);
   } else if (warp < ISSUER) {
     // ---- the final state back to the pool row -------------------------------------------
@@ -599,7 +629,9 @@ constexpr int kMaxDevices = 64;
 }  // namespace
 
 bool prefill_tc_supported(const DecodeParams& p) {
-  return p.D == TD && p.dlam == 1 && (p.flags & (GDN_FUSE_CONV | GDN_GATE_KDA | GDN_OUT_NORM_GATE)) == 0u;
+  // (the token tensors' position coordinate b*T + t is a 32-bit tensor-copy coordinate)
+  return p.D == TD && p.dlam == 1 && (p.flags & (GDN_FUSE_CONV | GDN_GATE_KDA | GDN_OUT_NORM_GATE)) == 0u &&
+         static_cast<long long>(p.B) * p.T <= 0x7fffffffLL;
 }
 
 cudaError_t launch_prefill_tc(const DecodeParams& p, cudaStream_t stream) {
@@ -614,6 +646,20 @@ cudaError_t launch_prefill_tc(const DecodeParams& p, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     configured[dev].store(1, std::memory_order_relaxed);
   }
+  // q, k, v as [B*T][H][128] tensors: boxes of 128 bytes of elements x 1 head x 32 positions
+  TokenMaps maps;
+  const bool bf16 = (p.flags & GDN_QKV_BF16) != 0u;
+  const cuuint64_t esz = bf16 ? 2u : 4u;
+  const cuuint64_t dims[3] = {TD, static_cast<cuuint64_t>(p.H), static_cast<cuuint64_t>(p.B) * static_cast<cuuint64_t>(p.T)};
+  const cuuint64_t strides[2] = {TD * esz, static_cast<cuuint64_t>(p.H) * TD * esz};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128u / esz), 1u, static_cast<cuuint32_t>(TC_C)};
+  const CUtensorMapDataType ty = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const void* bases[3] = {p.q, p.k, p.v};
+  CUtensorMap* out[3] = {&maps.q, &maps.k, &maps.v};
+  for (int i = 0; i < 3; ++i) {
+    err = encode_tiled(out[i], ty, 3, bases[i], dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (err != cudaSuccess) return err;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.B * p.H));
   cfg.blockDim = dim3(TC_NT);
@@ -624,7 +670,7 @@ cudaError_t launch_prefill_tc(const DecodeParams& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, gdn_prefill_tc_kernel, p);
+  err = cudaLaunchKernelEx(&cfg, gdn_prefill_tc_kernel, p, maps);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
