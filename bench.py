@@ -205,7 +205,7 @@ class DecodeRunner:
     interval (allocated on first use), and timed sequences of launches."""
 
     def __init__(self, gdn, lib, w, dev, stream, rank, ring=RING, klog_prenorm=False, keep_host=False,
-                 extra_flags=0):
+                 extra_flags=0, use_step=False, stagger=False):
         import torch
         from linear_attention_decode_gdn_gb300 import workloads as wl
         self.gdn, self.lib, self.w, self.dev, self.stream = gdn, lib, w, dev, stream
@@ -242,6 +242,11 @@ class DecodeRunner:
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.sets = {}
         self.launches = 0
+        # every DeltaLog launch through gdn_decode_step (each slot-head picks append or merge
+        # from its own log length) instead of the phase-specific entries; with `stagger`,
+        # request b enters the timed steps with b % M entries in its log, so every launch
+        # mixes appends and merges (about one request in M merging)
+        self.use_step, self.stagger, self.staggered = use_step, stagger, set()
 
     def _set(self, M):
         """(dims, pools, per-ring-step inputs, log) of merge interval M (0: dense)."""
@@ -267,7 +272,8 @@ class DecodeRunner:
                                            self.status.data_ptr(), self.sptr)
         else:
             dims, pools, ins, log = self._set(M)
-            fn = self.lib.gdn_decode_append if kind == "append" else self.lib.gdn_decode_merge
+            fn = (self.lib.gdn_decode_step if self.use_step
+                  else self.lib.gdn_decode_append if kind == "append" else self.lib.gdn_decode_merge)
             rc = fn(P(dims), P(ins[r]), pools.state.data_ptr(), P(log), self.o.data_ptr(),
                     self.status.data_ptr(), self.sptr)
         if rc:
@@ -287,6 +293,8 @@ class DecodeRunner:
         kinds = self.cycle_kinds(mode, M)
         r, n = 0, len(self.ring)
         self._set(0 if mode == "dense" else M)  # allocate outside the timed region
+        if self.stagger and mode != "dense" and M not in self.staggered:
+            self._stagger(M)
         for _ in range(warmup):
             for k in kinds:
                 self.launch(k, r % n, M)
@@ -321,6 +329,27 @@ class DecodeRunner:
             raise RuntimeError(f"device status {int(self.status.item())} in the {self.w.name} run")
         return elapsed, per
 
+    def _stagger(self, M):
+        """Pre-roll of the staggered phases: M - 1 steps in which only the requests with
+        b % M > r take part (the others are padding, slot -1)."""
+        import torch
+        dims, pools, _, log = self._set(M)
+        P = ctypes.byref
+        b = torch.arange(self.w.batch, device=self.dev)
+        for r in range(M - 1):
+            sl = torch.where(b % M > r, self.slot, torch.full_like(self.slot, -1))
+            d = dict(self.ring[r % len(self.ring)], **self.kda_dev)
+            if self.w.conv:
+                d.update(conv_w=self.conv_w, conv_pool=pools.conv)
+            ins = self.gdn.make_inputs(slot=sl, **d)
+            rc = self.lib.gdn_decode_step(P(dims), P(ins), pools.state.data_ptr(), P(log), self.o.data_ptr(),
+                                          self.status.data_ptr(), self.sptr)
+            if rc:
+                self.gdn._abi.check(rc, "step")
+            self.launches += 1
+        torch.cuda.synchronize(self.dev)
+        self.staggered.add(M)
+
     def free(self):
         import torch
         self.sets.clear()
@@ -351,10 +380,15 @@ def fractions(gbs, peak):
 
 # Decode-step sweeps reported beside the headline value (dense vs the merge interval on the
 # suite's decode workloads); M = 1 is the dense kernel. "split_dv": each head on two CTAs, one
-# per half of the value columns (GDN_SPLIT_DV), beside the one-CTA-per-head default.
+# per half of the value columns (GDN_SPLIT_DV), beside the one-CTA-per-head default. "step": the
+# same cycle through gdn_decode_step, the entry for batches whose requests sit at different
+# points of their cycle (each slot-head appends or merges by its own log length);
+# "step_staggered": the same with request b's cycle offset by b % M steps, so that every launch
+# mixes appends and merges (the serving case).
 SWEEPS = (("headline", (1, 2, 4, 8, 16), ""), ("high_concurrency", (1, 2, 4, 8, 16), ""), ("kda", (1, 8), ""),
           ("small_conv", (1, 8), ""), ("kda_full", (1, 8), ""), ("rwkv6", (1, 4), ""),
-          ("headline", (1, 8), "split_dv"), ("small_conv", (1, 8), "split_dv"))
+          ("headline", (1, 8), "split_dv"), ("small_conv", (1, 8), "split_dv"), ("headline", (8,), "step"),
+          ("headline", (8,), "step_staggered"))
 SWEEP_DECODE_STEPS = 256   # timed decode steps per sweep point (whole cycles)
 SWEEP_RING = 8
 
@@ -367,7 +401,8 @@ def run_sweeps(gdn, lib, dev, stream, rank, world, peak):
     for name, Ms, variant in SWEEPS:
         w = wl.WORKLOADS[name]
         extra = gdn.SPLIT_DV if variant == "split_dv" else 0
-        run = DecodeRunner(gdn, lib, w, dev, stream, rank, ring=SWEEP_RING, extra_flags=extra)
+        run = DecodeRunner(gdn, lib, w, dev, stream, rank, ring=SWEEP_RING, extra_flags=extra,
+                           use_step=variant.startswith("step"), stagger=variant == "step_staggered")
         klb, ulb = layout_bytes(run.flags, gdn)
         heads = w.batch * w.num_heads
         leg = {"batch": w.batch, "num_heads": w.num_heads, "dk": w.dk, "dv": w.dv,
@@ -387,8 +422,9 @@ def run_sweeps(gdn, lib, dev, stream, rank, world, peak):
                 "algorithmic_gbs": gbs, **fractions(gbs, peak)}
             run.sets.clear()
         best = max((k for k in leg if k.startswith("M")), key=lambda k: leg[k]["head_steps_per_s"])
-        leg["speedup_best_M_vs_dense"] = {"M": int(best[1:]),
-                                          "speedup": leg[best]["head_steps_per_s"] / leg["dense"]["head_steps_per_s"]}
+        if "dense" in leg:
+            leg["speedup_best_M_vs_dense"] = {"M": int(best[1:]),
+                                              "speedup": leg[best]["head_steps_per_s"] / leg["dense"]["head_steps_per_s"]}
         launches += run.launches
         run.free()
         out[name + (f"/{variant}" if variant else "")] = leg

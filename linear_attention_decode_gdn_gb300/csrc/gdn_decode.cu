@@ -121,9 +121,10 @@ __host__ __device__ inline Layout decode_layout(int mode, int D, int C, int dlam
 // other instances take no minimum (0: none).  EXT instances carry the KDA gate
 // parametrisation and output epilogue; the others compile them out.
 template <int D, int MODE, bool EXT, int FORM>
-__global__ void __launch_bounds__(NT_DECODE, MODE == MODE_STEP ? 2 : (FORM != FORM_GENERAL ? 3 : 0))
+__global__ void __launch_bounds__(NT_DECODE, FORM != FORM_GENERAL ? 3 : (MODE == MODE_STEP ? 2 : 0))
     gdn_decode_kernel(const DecodeParams p) {
-  static_assert(FORM == FORM_GENERAL || MODE == MODE_MERGE, "the three-per-SM forms are merge forms");
+  static_assert(FORM == FORM_GENERAL || MODE == MODE_MERGE || MODE == MODE_STEP,
+                "the three-per-SM forms are merge forms (also in the auto step)");
   constexpr bool R3 = FORM != FORM_GENERAL;
   extern __shared__ __align__(128) unsigned char smem[];
 
@@ -802,7 +803,15 @@ cudaError_t launch_de(int mode, const DecodeParams& p, cudaStream_t stream) {
         }
       }
       return launch_one<D, MODE_MERGE, EXT, FORM_GENERAL>(p, stream);
-    case MODE_STEP: return launch_one<D, MODE_STEP, EXT, FORM_GENERAL>(p, stream);
+    case MODE_STEP:
+      if constexpr (D == 128) {
+        switch (merge_form(p)) {
+          case FORM_R3: return launch_one<D, MODE_STEP, EXT, FORM_R3>(p, stream);
+          case FORM_R3_PER_KEY: return launch_one<D, MODE_STEP, EXT, FORM_R3_PER_KEY>(p, stream);
+          default: break;
+        }
+      }
+      return launch_one<D, MODE_STEP, EXT, FORM_GENERAL>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }
