@@ -768,7 +768,7 @@ def run_prefill(args, w, flags, dev, stream, gdn):
     alu_peak = GB300_SMS * FP32_FMA_PER_SM_CLK * 2 * GB300_MAX_SM_MHZ * 1e6 / 1e12
     out = {"value": units / el, "unit": "positions x heads / s", "positions_per_request": T,
            "ms_per_call": el / calls * 1e3, "calls": calls, "launches": calls + max(2, args.warmup // 2)}
-    if prefill_on_tensor_cores(D, w.decay_per_key, pflags, gdn):
+    if prefill_on_tensor_cores(D, w.decay_per_key, pflags, gdn, B, T):
         # the products run as kind::tf32 MMAs, three per fp32-accurate product (3xTF32)
         bf16, kind = measured_bf16_tflops()
         tf32 = bf16 * TF32_PER_BF16
@@ -790,10 +790,12 @@ def run_prefill(args, w, flags, dev, stream, gdn):
     return out
 
 
-def prefill_on_tensor_cores(D, decay_per_key, flags, gdn) -> bool:
+def prefill_on_tensor_cores(D, decay_per_key, flags, gdn, B=1, T=1) -> bool:
     """The library's choice of prefill kernel: the tcgen05 one for 128-wide heads with a
-    per-head decay and neither the fused conv nor the KDA gate / epilogue."""
-    return D == 128 and not decay_per_key and not (flags & (gdn.FUSE_CONV | gdn.GATE_KDA | gdn.OUT_NORM_GATE))
+    per-head decay and neither the fused conv nor the KDA gate / epilogue (and B * T below
+    2^31, the 32-bit position coordinate of its token copies)."""
+    return (D == 128 and not decay_per_key and not (flags & (gdn.FUSE_CONV | gdn.GATE_KDA | gdn.OUT_NORM_GATE))
+            and B * T < 2 ** 31)
 
 
 def measured_bf16_tflops():
