@@ -79,6 +79,22 @@ def test_high_concurrency_merge_sweep():
     _check(Lockstep(w, [Variant("dense")] + [Variant("deltalog", M) for M in (2, 4, 8, 16)]).run())
 
 
+def test_full_register_group_of_log_entries():
+    """C = 8 (M = 9): the largest log the three-per-SM merge forms take, all eight U entries of
+    the register group live (no zero padding), per-head and per-key decay, through the merge
+    and the auto step, with exact key logs held to the dense bar."""
+    for name in ("headline", "kda"):
+        w = wl.WORKLOADS[name]
+        ls = Lockstep(w, [Variant("dense"),
+                          Variant("deltalog", 9, extra_flags=gdn.KLOG_PRENORM, name="M=9/prenorm"),
+                          Variant("deltalog", 9, "step", extra_flags=gdn.KLOG_PRENORM, name="M=9/step/prenorm"),
+                          Variant("deltalog", 9, name="M=9")],
+                      batch=32).run(steps=36)
+        rep = _check(ls)
+        for v in ls.variants[1:3]:
+            assert v.rel_err <= DENSE_TOL and v.state_rel_err <= DENSE_TOL, rep
+
+
 def test_kda():
     w = wl.WORKLOADS["kda"]
     _check(Lockstep(w, [Variant("dense"), Variant("deltalog", 8),
