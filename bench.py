@@ -612,10 +612,26 @@ def run_gpu(args, rank, local_rank, world):
         **({"sweeps": dict(sweeps, clocks=sweep_clocks)} if sweeps else {}),
         **({"verify": verify} if verify else {}),
         **({"prefill": prefill} if prefill else {}),
+        "pages_context": PAGES_CONTEXT,
         "gpu_launches": launches,
         "clocks": {k: v for k, v in clocks.summary().items()},
     }
     return out
+
+
+# The pages' own measurements, quoted beside this bench's as context only: other hardware,
+# other kernels, not the target (DeltaLog reading notes, Sec. 4.1 Figs. 6-7, Sec. 4.2 Fig. 8,
+# Sec. 4.4 Fig. 10, Sec. 4.6 Table 4). This bench's counterparts: `modes.speedup_deltalog_vs_dense`,
+# the measured `modes.traffic` reductions and `modes.deltalog_M8.us_per_decode_step`.
+PAGES_CONTEXT = {
+    "note": "the pages' numbers on other GPUs, against other kernels; context, not the target",
+    "deltalog_speedup_vs_fla_rtx4090_gdn_m8": "up to 1.86x (B = 64 .. 512)",
+    "deltalog_speedup_vs_fla_h200_gdn_m8": "1.34 / 1.45 / 1.53 / 1.60x at B = 64 / 128 / 256 / 512",
+    "write_traffic_reduction_vs_dense_h200_b128_m8": 7.83,
+    "total_traffic_reduction_vs_dense_h200_b128_m8": 1.64,
+    "end_to_end_tpot_speedup_h200": "1.05 - 1.20x (two hybrid models; needs trained weights, not run here)",
+    "amortised_step_latency_h200_b128_m8_ms": 0.103,
+}
 
 
 def _packed(arrays: dict, align: int = 256):
