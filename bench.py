@@ -789,7 +789,8 @@ def run_prefill(args, w, flags, dev, stream, gdn):
         bf16, kind = measured_bf16_tflops()
         tf32 = bf16 * TF32_PER_BF16
         peak = tf32 / 3.0
-        out["kernel"] = "gdn_prefill_tc_kernel (tcgen05 kind::tf32, 3xTF32)"
+        out["kernel"] = ("gdn_prefill_tc_pk_kernel" if w.decay_per_key else "gdn_prefill_tc_kernel") + \
+            " (tcgen05 kind::tf32, 3xTF32)"
         out["roofline"] = {
             "bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s (fp32-accurate, 3xTF32)",
             "frac": tflops / peak,
@@ -807,11 +808,11 @@ def run_prefill(args, w, flags, dev, stream, gdn):
 
 
 def prefill_on_tensor_cores(D, decay_per_key, flags, gdn, B=1, T=1) -> bool:
-    """The library's choice of prefill kernel: the tcgen05 one for 128-wide heads with a
-    per-head decay and neither the fused conv nor the KDA gate / epilogue (and B * T below
-    2^31, the 32-bit position coordinate of its token copies)."""
-    return (D == 128 and not decay_per_key and not (flags & (gdn.FUSE_CONV | gdn.GATE_KDA | gdn.OUT_NORM_GATE))
-            and B * T < 2 ** 31)
+    """The library's choice of prefill kernel: a tcgen05 one for 128-wide heads with neither
+    the fused conv nor the KDA gate / epilogue (and B * T below 2^31, the 32-bit position
+    coordinate of its token copies) -- for a per-key decay with bf16 q, k, v."""
+    return (D == 128 and not (flags & (gdn.FUSE_CONV | gdn.GATE_KDA | gdn.OUT_NORM_GATE))
+            and (not decay_per_key or bool(flags & gdn.QKV_BF16)) and B * T < 2 ** 31)
 
 
 def measured_bf16_tflops():

@@ -20,6 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libgdn.so")
 SOURCES = ["gdn_decode.cu", "gdn_decode_x.cu", "gdn_verify.cu", "gdn_prefill.cu", "gdn_prefill_tc.cu",
+           "gdn_prefill_tc_pk.cu",
            "gdn_conv.cu", "gdn_api.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

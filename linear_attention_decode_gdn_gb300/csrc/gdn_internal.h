@@ -82,6 +82,8 @@ cudaError_t launch_prefill(const DecodeParams& p, cudaStream_t stream);
 // the tensor-core prefill (head size 128, per-head decay, no fused conv / KDA gate / epilogue)
 bool prefill_tc_supported(const DecodeParams& p);
 cudaError_t launch_prefill_tc(const DecodeParams& p, cudaStream_t stream);
+bool prefill_tc_pk_supported(const DecodeParams& p);
+cudaError_t launch_prefill_tc_pk(const DecodeParams& p, cudaStream_t stream);
 
 // Dynamic shared memory of a prefill CTA (bytes).
 size_t prefill_smem_bytes(int D, int dlam);

@@ -811,6 +811,7 @@ size_t prefill_smem_bytes(int D, int dlam) { return prefill_layout(D, dlam).tota
 
 cudaError_t launch_prefill(const DecodeParams& p, cudaStream_t stream) {
   if (prefill_tc_supported(p)) return launch_prefill_tc(p, stream);
+  if (prefill_tc_pk_supported(p)) return launch_prefill_tc_pk(p, stream);
   switch (p.D) {
     case 16: return launch_prefill_d<16>(p, stream);
     case 32: return launch_prefill_d<32>(p, stream);

@@ -107,6 +107,20 @@ def test_prefill_raw_value_update():
     assert e_o <= TOL and e_s <= TOL, (e_o, e_s)
 
 
+def test_prefill_per_key_bf16_raw_gates_padding():
+    """Per-key decay from raw gates (logsigmoid per channel in the decay scan, sigmoid write
+    strength) with bf16 inputs -- the tensor-core kernel for a per-key decay -- across padded
+    and permuted slots and a ragged tail chunk."""
+    e_o, e_s, _ = _run(128, True, 80, np.array([80, 17, 80, 5]), gate_raw=True, slot=[2, -1, 0, 4], seed=7)
+    assert e_o <= TOL and e_s <= TOL, (e_o, e_s)
+
+
+def test_prefill_long_prompt_per_key_from_zero():
+    """A fresh request over a long prompt of many chunks with a per-key decay."""
+    e_o, e_s, _ = _run(128, True, 300, np.array([300, 257]), H=4, seed=8, init_scale=0.0)
+    assert e_o <= TOL and e_s <= TOL, (e_o, e_s)
+
+
 def test_prefill_long_prompt_from_zero():
     """A fresh request (zero state) over a long prompt of many chunks."""
     e_o, e_s, _ = _run(128, False, 300, np.array([300, 257]), H=4, seed=5, init_scale=0.0)
