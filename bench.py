@@ -754,10 +754,21 @@ def run_prefill(args, w, flags, dev, stream, gdn):
         x[n] = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16) if w.qkv_bf16 \
             else torch.from_numpy(a).to(dev)
     a_raw = rng.standard_normal((B, T, H, w.dlam), dtype=np.float32) + np.float32(3)
-    x["log_decay"] = torch.from_numpy((-np.log1p(np.exp(-a_raw))).astype(np.float32)).to(dev)
-    if not w.raw_value:
-        b_raw = rng.standard_normal((B, T, H), dtype=np.float32)
-        x["beta"] = torch.from_numpy((1 / (1 + np.exp(-b_raw))).astype(np.float32)).to(dev)
+    b_raw = rng.standard_normal((B, T, H), dtype=np.float32)
+    if w.kda_full:
+        # the KDA gate parametrisation (raw gate f = decay draw - 3, write logit) and the
+        # output epilogue, as in the decode workload
+        from linear_attention_decode_gdn_gb300 import workloads as wl
+        pflags |= gdn.GATE_KDA | gdn.OUT_NORM_GATE
+        kp = wl.kda_gate_params(w)
+        x.update({n: torch.from_numpy(kp[n]).to(dev) for n in ("a_log", "dt_bias", "out_norm_w")})
+        x["log_decay"] = torch.from_numpy(a_raw - np.float32(3)).to(dev)
+        x["beta"] = torch.from_numpy(b_raw).to(dev)
+        x["out_gate"] = torch.from_numpy(rng.standard_normal((B, T, H, D), dtype=np.float32)).to(dev)
+    else:
+        x["log_decay"] = torch.from_numpy((-np.log1p(np.exp(-a_raw))).astype(np.float32)).to(dev)
+        if not w.raw_value:
+            x["beta"] = torch.from_numpy((1 / (1 + np.exp(-b_raw))).astype(np.float32)).to(dev)
     slot = torch.arange(B, dtype=torch.int32, device=dev)
     inp = gdn.make_inputs(slot=slot, **x)
     dims = gdn.make_dims(B, H, D, num_slots=B, decay_per_key=w.decay_per_key, flags=pflags)
@@ -808,11 +819,14 @@ def run_prefill(args, w, flags, dev, stream, gdn):
 
 
 def prefill_on_tensor_cores(D, decay_per_key, flags, gdn, B=1, T=1) -> bool:
-    """The library's choice of prefill kernel: a tcgen05 one for 128-wide heads with neither
-    the fused conv nor the KDA gate / epilogue (and B * T below 2^31, the 32-bit position
-    coordinate of its token copies) -- for a per-key decay with bf16 q, k, v."""
-    return (D == 128 and not (flags & (gdn.FUSE_CONV | gdn.GATE_KDA | gdn.OUT_NORM_GATE))
-            and (not decay_per_key or bool(flags & gdn.QKV_BF16)) and B * T < 2 ** 31)
+    """The library's choice of prefill kernel: a tcgen05 one for 128-wide heads without the
+    fused conv (and B * T below 2^31, the 32-bit position coordinate of its token copies):
+    with a per-head decay and no KDA gate / epilogue, or a per-key decay with bf16 q, k, v."""
+    if D != 128 or flags & gdn.FUSE_CONV or B * T >= 2 ** 31:
+        return False
+    if decay_per_key:  # bf16 q, k, v; the KDA gate and epilogue included
+        return bool(flags & gdn.QKV_BF16)
+    return not flags & (gdn.GATE_KDA | gdn.OUT_NORM_GATE)
 
 
 def measured_bf16_tflops():

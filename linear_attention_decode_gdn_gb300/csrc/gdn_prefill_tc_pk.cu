@@ -13,6 +13,9 @@
 // gdn_prefill_tc.cu): pair sums [Ktil; Qtil] Kbar^T (M = 64, N = 32, K = 128), state read
 // S^T [Ktil; Qtil]^T, state write S^T += B^T Khat, readout O^T = O^T + B^T P^T.
 //
+// The operand factors use the fast exponential (__expf: a few parts in 10^6 at |gamma| <= 80,
+// far inside the fp32-accuracy bar of the products; 8% of the kernel's time against expf).
+//
 // Kbar needs e^{-gamma_s} finite: a chunk whose cumulative decay falls below e^{-80} in some
 // channel forms its pair sums on the CUDA cores instead, term by term with e^{gamma_t -
 // gamma_s} (exact, slow, and only for such extreme decays; the other products are unchanged).
@@ -67,7 +70,8 @@ constexpr uint32_t OFF_SV = OFF_SK + 2 * ST_BOX;           // staging v
 constexpr uint32_t OFF_SL = OFF_SV + 2 * ST_BOX;           // staging log decays / gamma
 constexpr uint32_t OFF_DC = OFF_SL + 4 * ST_BOX;           // gamma_C[c], e^{gamma_C[c]}
 constexpr uint32_t OFF_G = OFF_DC + 2 * TD * 4;            // beta, key scale, query scale per token
-constexpr uint32_t OFF_BAR = OFF_G + 3 * TC_C * 4;         // mbarriers: ps, p1, p2, drain, staging q, k, v
+constexpr uint32_t OFF_EP = OFF_G + 3 * TC_C * 4;          // output epilogue: 4 x 32 partial sums, 32 scales
+constexpr uint32_t OFF_BAR = OFF_EP + 5 * TC_C * 4;        // mbarriers: ps, p1, p2, drain, staging q, k, v
 constexpr uint32_t OFF_TMEM = OFF_BAR + 8 * 8;
 constexpr uint32_t PK_SMEM = OFF_TMEM + 16;
 
@@ -135,6 +139,35 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Named barrier over warps 4-7 (128 threads) returning the OR of `pred` over them, and the
+// plain form.
+__device__ __forceinline__ bool upper_sync_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred a, o;\n setp.ne.u32 a, %1, 0;\n bar.red.or.pred o, 2, 128, a;\n selp.u32 %0, 1, 0, o;\n}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred))
+      : "memory");
+  return r != 0u;
+}
+__device__ __forceinline__ void upper_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+
+// v[i] of every lane -> the return value of lane l is the sum over the warp of v[l]
+// (recursive halving: at each step a lane keeps half its partial sums and adds the partner's).
+__device__ __forceinline__ float transpose_sum32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int k = 16; k >= 1; k >>= 1) {
+    const bool upper = (lane & k) != 0;
+#pragma unroll
+    for (int i = 0; i < k; ++i) {
+      const float send = upper ? v[i] : v[i + k];
+      const float keep = upper ? v[i + k] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, k);
+    }
+  }
+  return v[0];
+}
+
 // Bounded wait for phase `parity` of `bar`, the same answer in every lane of the warp.
 __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
@@ -150,6 +183,8 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_pk_kernel(const Decod
   const bool plain = (fl & GDN_PLAIN_UPDATE) != 0u;
   const bool l2 = (fl & GDN_NO_QK_L2NORM) == 0u;
   const bool graw = (fl & GDN_GATE_RAW) != 0u;
+  const bool kda = (fl & GDN_GATE_KDA) != 0u;          // KDA gate parametrisation of the decays
+  const bool epi = (fl & GDN_OUT_NORM_GATE) != 0u;     // KDA output epilogue
   const int T = p.T;
 
   griddep_launch_dependents();
@@ -270,14 +305,28 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_pk_kernel(const Decod
     if (warp < ISSUER) {
       if (!wait_warp(stq, it & 1u)) bad = true;
       if (!wait_warp(stk, it & 1u)) bad = true;
+      unsigned char* sl = smem + OFF_SL;
+      if (graw || kda) {
+        // the gate parametrisation of every live decay, in place, on all compute warps:
+        // logsigmoid (raw gates) or KDA's lambda = lower_bound sigmoid(e^{A_log[h]} (f + dt_bias[h][c]))
+        const int c = tid & (TD - 1);
+        const float ga = kda ? expf(__ldg(p.a_log + h)) : 0.0f;
+        const float dtb = kda ? __ldg(p.dt_bias + static_cast<size_t>(h) * TD + c) : 0.0f;
+        for (int t = tid >> 7; t < n; t += 2) {
+          float* at = reinterpret_cast<float*>(const_cast<unsigned char*>(staged_at(sl, t, c, 4u)));
+          // (KDA's sigmoid through the fast intrinsics: relative error a few parts in 10^7 also
+          // where it is tiny; the log-sigmoid of raw gates keeps log1pf, which carries the
+          // whole value of a decay near zero)
+          *at = kda ? p.lower_bound * __fdividef(1.0f, 1.0f + __expf(-ga * (*at + dtb))) : log_sigmoidf_(*at);
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");  // the compute warps
+      }
       if (warp < 4) {
-        unsigned char* sl = smem + OFF_SL;
         float g = 0.0f;
 #pragma unroll 4
         for (int t = 0; t < TC_C; ++t) {
           float* at = reinterpret_cast<float*>(const_cast<unsigned char*>(staged_at(sl, t, tid, 4u)));
-          float lam = t < n ? *at : 0.0f;
-          if (graw && t < n) lam = log_sigmoidf_(lam);
+          const float lam = t < n ? *at : 0.0f;
           g += lam;
           *at = g;
         }
@@ -287,7 +336,7 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_pk_kernel(const Decod
       }
       if (warp == 4) {
         float be = pf_beta;
-        if (graw && p.beta && lane < n) be = sigmoidf_(be);
+        if ((graw || kda) && p.beta && lane < n) be = sigmoidf_(be);
         bet[lane] = be;
       }
     }
@@ -315,11 +364,11 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_pk_kernel(const Decod
         const int c = 4 * (g0 + 4 * i);
         const float4 g4 = *reinterpret_cast<const float4*>(staged_at(gl, t, c, 4u));
         const float a0 = x[i].x * sc, a1 = x[i].y * sc, a2 = x[i].z * sc, a3 = x[i].w * sc;
-        store_split4(smem, OFF_XH, OFF_XL, kmaj_off(r, c, X_LBO), a0 * expf(g4.x), a1 * expf(g4.y), a2 * expf(g4.z),
-                     a3 * expf(g4.w));
+        store_split4(smem, OFF_XH, OFF_XL, kmaj_off(r, c, X_LBO), a0 * __expf(g4.x), a1 * __expf(g4.y), a2 * __expf(g4.z),
+                     a3 * __expf(g4.w));
         if (isk && split)
-          store_split4(smem, OFF_NH, OFF_NL, kmaj_off(t, c, N_LBO), a0 * expf(-g4.x), a1 * expf(-g4.y),
-                       a2 * expf(-g4.z), a3 * expf(-g4.w));
+          store_split4(smem, OFF_NH, OFF_NL, kmaj_off(t, c, N_LBO), a0 * __expf(-g4.x), a1 * __expf(-g4.y),
+                       a2 * __expf(-g4.z), a3 * __expf(-g4.w));
       }
     }
     tc::fence_smem_to_async();
@@ -354,17 +403,52 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_pk_kernel(const Decod
   }
   int prev_t0 = 0, prev_n = 0;
 
-  // readout of a finished chunk from its TMEM output buffer (warps 4-7), coalesced row stores
-  auto store_output = [&](uint32_t d1, int ct0, int cn) {
-    float* orow = p.o + ((static_cast<size_t>(b) * T + ct0) * p.H + h) * TD + j;
+  // readout of a finished chunk from its TMEM output buffer (warps 4-7, called by all four
+  // together), coalesced row stores; with the KDA epilogue each position's row is first
+  // normalised by its RMS over the 128 value columns (four warps' partial sums) and gated:
+  // o <- o / sqrt(mean(o^2) + eps) w sigmoid(g)
+  float* ep_part = reinterpret_cast<float*>(smem + OFF_EP);
+  float* ep_inv = ep_part + 4 * TC_C;
+  // the output gates of the positions a store_output call writes, loaded ahead of it (the
+  // output stores may alias them, so they cannot be hoisted past the stores)
+  auto load_gates = [&](int ct0, int cn, float (&gv)[32]) {
+    const size_t obase = ((static_cast<size_t>(b) * T + ct0) * p.H + h) * TD + j;
     const size_t tstride = static_cast<size_t>(p.H) * TD;
 #pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) {
-      float o[16];
-      tc::ld16(tmem + lb + d1 + TC_C + 16 * h2, o);
+    for (int k = 0; k < 32; ++k) gv[k] = k < cn ? __ldg(p.out_gate + obase + k * tstride) : 0.0f;
+  };
+  auto store_output = [&](uint32_t d1, int ct0, int cn, const float (&gv)[32]) {
+    float o[32], o1[16];
+    tc::ld16(tmem + lb + d1 + TC_C, o1);
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
-        if (16 * h2 + k < cn) orow[(16 * h2 + k) * tstride] = o[k];
+    for (int k = 0; k < 16; ++k) o[k] = o1[k];
+    tc::ld16(tmem + lb + d1 + TC_C + 16, o1);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) o[16 + k] = o1[k];
+    const size_t obase = ((static_cast<size_t>(b) * T + ct0) * p.H + h) * TD + j;
+    const size_t tstride = static_cast<size_t>(p.H) * TD;
+    if (epi) {
+      float sq[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) sq[k] = o[k] * o[k];
+      ep_part[(warp - 4) * TC_C + lane] = transpose_sum32(sq, lane);
+      upper_sync();
+      if (warp == 4) {
+        const float ms = (ep_part[lane] + ep_part[TC_C + lane] + ep_part[2 * TC_C + lane] + ep_part[3 * TC_C + lane]) /
+                         static_cast<float>(TD);
+        ep_inv[lane] = 1.0f / sqrtf(ms + p.out_eps);
+      }
+      upper_sync();
+      const float w = p.out_norm_w ? __ldg(p.out_norm_w + j) : 1.0f;
+      // (the gate's sigmoid through the fast intrinsics: a few parts in 10^7)
+#pragma unroll
+      for (int k = 0; k < 32; ++k)
+        if (k < cn) p.o[obase + k * tstride] = o[k] * ep_inv[k] * w * __fdividef(1.0f, 1.0f + __expf(-gv[k]));
+      upper_sync();  // (the partial sums are rewritten by the next chunk's call)
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k)
+        if (k < cn) p.o[obase + k * tstride] = o[k];
     }
   };
 
@@ -401,10 +485,10 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_pk_kernel(const Decod
         const float4 kx = s < n ? staged4_bf16(kl, s, g0 + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
         const float4 g4 = *reinterpret_cast<const float4*>(staged_at(gl, s, c, 4u));
         const float4 c4 = *reinterpret_cast<const float4*>(gC + c);
-        store_split1(smem, OFF_KH, OFF_KL, kmaj_off(c + 0, s, T128_LBO), kx.x * sk * expf(c4.x - g4.x));
-        store_split1(smem, OFF_KH, OFF_KL, kmaj_off(c + 1, s, T128_LBO), kx.y * sk * expf(c4.y - g4.y));
-        store_split1(smem, OFF_KH, OFF_KL, kmaj_off(c + 2, s, T128_LBO), kx.z * sk * expf(c4.z - g4.z));
-        store_split1(smem, OFF_KH, OFF_KL, kmaj_off(c + 3, s, T128_LBO), kx.w * sk * expf(c4.w - g4.w));
+        store_split1(smem, OFF_KH, OFF_KL, kmaj_off(c + 0, s, T128_LBO), kx.x * sk * __expf(c4.x - g4.x));
+        store_split1(smem, OFF_KH, OFF_KL, kmaj_off(c + 1, s, T128_LBO), kx.y * sk * __expf(c4.y - g4.y));
+        store_split1(smem, OFF_KH, OFF_KL, kmaj_off(c + 2, s, T128_LBO), kx.z * sk * __expf(c4.z - g4.z));
+        store_split1(smem, OFF_KH, OFF_KL, kmaj_off(c + 3, s, T128_LBO), kx.w * sk * __expf(c4.w - g4.w));
       }
     }
     tc::fence_smem_to_async();
@@ -542,6 +626,8 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_pk_kernel(const Decod
       for (int s4 = 0; s4 < TC_C; s4 += 4)
         store_split4(smem, OFF_BH, OFF_BL, kmaj_off(j, s4, T128_LBO), bc[s4], bc[s4 + 1], bc[s4 + 2], bc[s4 + 3]);
     } else if (warp >= 4 && warp < ISSUER) {
+      float gv[32];
+      if (epi && it > 0) load_gates(prev_t0, prev_n, gv);
       // ---- decay of the state, column c by e^{gamma_C[c]}, before the write accumulates ------
       if (!bad) {
 #pragma unroll
@@ -555,7 +641,8 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_pk_kernel(const Decod
         tc::wait_st();
       }
       // the previous chunk's output, from the other TMEM buffer, while the substitution runs
-      if (!bad && it > 0) store_output(d1 == TM_D1 ? TM_D1B : TM_D1, prev_t0, prev_n);
+      // (decided jointly by warps 4-7: the epilogue synchronises them)
+      if (!upper_sync_or(bad) && it > 0) store_output(d1 == TM_D1 ? TM_D1B : TM_D1, prev_t0, prev_n, gv);
     }
     tc::fence_smem_to_async();
     tc::fence_before_sync();
@@ -564,6 +651,10 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_pk_kernel(const Decod
 
     if (warp == ISSUER) {
       if (nt0 < n_tok) copy_v(nt0);  // the staged v rows are free
+      if (epi && (reinterpret_cast<uintptr_t>(p.out_gate) & 15u) == 0u && lane < n) {
+        // this chunk's output gates into L2, a chunk before the epilogue reads them
+        bulk_prefetch_l2(p.out_gate + ((static_cast<size_t>(b) * T + t0 + lane) * p.H + h) * TD, TD * 4u);
+      }
       const uint32_t bh = sbase + OFF_BH, bl = sbase + OFF_BL;
       const uint32_t kh = sbase + OFF_KH, kl = sbase + OFF_KL;
       const uint32_t ph = sbase + OFF_PH, pl = sbase + OFF_PL;
@@ -601,7 +692,11 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_pk_kernel(const Decod
     tc::fence_after_sync();
   }
   bad = __syncthreads_or(bad) != 0;
-  if (!bad && warp >= 4 && warp < ISSUER) store_output((it - 1) & 1u ? TM_D1B : TM_D1, prev_t0, prev_n);
+  if (!bad && warp >= 4 && warp < ISSUER) {
+    float gv[32];
+    if (epi) load_gates(prev_t0, prev_n, gv);
+    store_output((it - 1) & 1u ? TM_D1B : TM_D1, prev_t0, prev_n, gv);
+  }
   if (bad) {
     // let every MMA and copy this CTA issued finish (bounded) before the memory is released
     if (warp == ISSUER) {
@@ -636,7 +731,7 @@ constexpr int kMaxDevices = 64;
 bool prefill_tc_pk_supported(const DecodeParams& p) {
   // bf16 q, k, v; the decays are fp32; the position coordinate b*T + t is a 32-bit copy coordinate
   return p.D == TD && p.DV == TD && p.dlam == TD && (p.flags & GDN_QKV_BF16) != 0u &&
-         (p.flags & (GDN_FUSE_CONV | GDN_GATE_KDA | GDN_OUT_NORM_GATE)) == 0u &&
+         (p.flags & GDN_FUSE_CONV) == 0u &&
          static_cast<long long>(p.B) * p.T <= 0x7fffffffLL &&
          (reinterpret_cast<uintptr_t>(p.lam) & 15u) == 0u;  // (the decays' tensor map needs it)
 }
