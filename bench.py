@@ -743,16 +743,26 @@ def run_prefill(args, w, flags, dev, stream, gdn):
     derived from the SM count, the FP32 lanes per SM and the maximum SM clock."""
     import torch
     B, H, D, T = w.batch, w.num_heads, w.dk, args.prefill
-    if w.conv:
-        return {"unavailable": "the prefill path does not fuse the conv"}
-    pflags = flags & (gdn.QKV_BF16 | gdn.NO_QK_L2NORM | gdn.PLAIN_UPDATE)
+    pflags = flags & (gdn.QKV_BF16 | gdn.NO_QK_L2NORM | gdn.PLAIN_UPDATE | gdn.FUSE_CONV)
     rng = np.random.default_rng(w.seed + 99)
     x = {}
-    for n in ("q", "k", "v"):
-        a = rng.standard_normal((B, T, H, D), dtype=np.float32) * np.float32(1.0 if n == "v" else w.qk_mult)
+    if w.conv:
+        # mixed_qkv rows [B][T][channels] through the width-4 conv, the workload's conv weights,
+        # a zero conv state (each call leaves the prompt's last three inputs there)
+        from linear_attention_decode_gdn_gb300 import workloads as wl
+        a = rng.standard_normal((B, T, w.channels), dtype=np.float32)
         bits, _ = wl_bf16(a)
-        x[n] = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16) if w.qkv_bf16 \
+        x["mixed_qkv"] = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16) if w.qkv_bf16 \
             else torch.from_numpy(a).to(dev)
+        x["conv_w"] = torch.from_numpy(wl.conv_weights(w)).to(dev)
+        x["conv_pool"] = torch.zeros((B, w.channels, 3), device=dev,
+                                     dtype=torch.bfloat16 if w.qkv_bf16 else torch.float32)
+    else:
+        for n in ("q", "k", "v"):
+            a = rng.standard_normal((B, T, H, D), dtype=np.float32) * np.float32(1.0 if n == "v" else w.qk_mult)
+            bits, _ = wl_bf16(a)
+            x[n] = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16) if w.qkv_bf16 \
+                else torch.from_numpy(a).to(dev)
     a_raw = rng.standard_normal((B, T, H, w.dlam), dtype=np.float32) + np.float32(3)
     b_raw = rng.standard_normal((B, T, H), dtype=np.float32)
     if w.kda_full:
@@ -801,7 +811,7 @@ def run_prefill(args, w, flags, dev, stream, gdn):
         tf32 = bf16 * TF32_PER_BF16
         peak = tf32 / 3.0
         out["kernel"] = ("gdn_prefill_tc_pk_kernel" if w.decay_per_key else "gdn_prefill_tc_kernel") + \
-            " (tcgen05 kind::tf32, 3xTF32)"
+            (" with the fused conv" if pflags & gdn.FUSE_CONV else "") + " (tcgen05 kind::tf32, 3xTF32)"
         out["roofline"] = {
             "bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s (fp32-accurate, 3xTF32)",
             "frac": tflops / peak,
@@ -819,13 +829,16 @@ def run_prefill(args, w, flags, dev, stream, gdn):
 
 
 def prefill_on_tensor_cores(D, decay_per_key, flags, gdn, B=1, T=1) -> bool:
-    """The library's choice of prefill kernel: a tcgen05 one for 128-wide heads without the
-    fused conv (and B * T below 2^31, the 32-bit position coordinate of its token copies):
-    with a per-head decay and no KDA gate / epilogue, or a per-key decay with bf16 q, k, v."""
-    if D != 128 or flags & gdn.FUSE_CONV or B * T >= 2 ** 31:
+    """The library's choice of prefill kernel: a tcgen05 one for 128-wide heads (and B * T
+    below 2^31, the 32-bit position coordinate of its token copies): with a per-head decay and
+    no KDA gate / epilogue (the fused conv with bf16 mixed_qkv included), or a per-key decay
+    with bf16 q, k, v and no fused conv."""
+    if D != 128 or B * T >= 2 ** 31:
         return False
     if decay_per_key:  # bf16 q, k, v; the KDA gate and epilogue included
-        return bool(flags & gdn.QKV_BF16)
+        return bool(flags & gdn.QKV_BF16) and not flags & gdn.FUSE_CONV
+    if flags & gdn.FUSE_CONV and not flags & gdn.QKV_BF16:
+        return False
     return not flags & (gdn.GATE_KDA | gdn.OUT_NORM_GATE)
 
 

@@ -303,13 +303,13 @@ int gdn_decode_verify(const gdn_dims *dims, int32_t num_tokens, const gdn_inputs
  *   GDN_GATE_KDA and GDN_OUT_NORM_GATE (in->out_gate [B][T][H][dv]).
  * The DeltaLog flags are rejected with GDN_ERR_UNSUPPORTED. Requires num_tokens >= 0.
  * Precision and path: the state and every product stay at fp32 accuracy. Head size 128
- * without GDN_FUSE_CONV (and B * T below 2^31) runs its matrix products on the tensor
- * cores as three TF32 products per fp32 product (hi*hi + lo*hi + hi*lo, relative error
- * about 2^-20 per term): with a per-head decay (bf16 or fp32 inputs, no KDA flags), or with
- * a per-key decay (bf16 inputs, a 16-byte aligned log_decay, the KDA gate and epilogue
- * included); a chunk whose per-key decay falls below e^-80 forms its pair sums term by
- * term on the CUDA cores. Every other case runs on the FP32 CUDA cores. All agree with
- * token-by-token decode to 1e-4.
+ * (and B * T below 2^31) runs its matrix products on the tensor cores as three TF32
+ * products per fp32 product (hi*hi + lo*hi + hi*lo, relative error about 2^-20 per term):
+ * with a per-head decay (bf16 or fp32 q/k/v, or bf16 mixed_qkv through GDN_FUSE_CONV; no
+ * KDA flags), or with a per-key decay (bf16 q/k/v without GDN_FUSE_CONV, a 16-byte aligned
+ * log_decay, the KDA gate and epilogue included); a chunk whose per-key decay falls below
+ * e^-80 forms its pair sums term by term on the CUDA cores. Every other case runs on the
+ * FP32 CUDA cores. All agree with token-by-token decode to 1e-4.
  */
 int gdn_prefill(const gdn_dims *dims, int32_t num_tokens, const gdn_inputs *in,
                 const int32_t *seq_lens, float *state_pool, float *o, int32_t *status, void *stream);

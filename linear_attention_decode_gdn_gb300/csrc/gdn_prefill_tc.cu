@@ -27,6 +27,11 @@
 // issues the MMAs (one elected lane) and does nothing else, so no compute warp ever waits on
 // the tensor core's issue queue.  The next chunk's token stage runs
 // while the state-write and readout MMAs of the current chunk execute.
+//
+// With the fused conv (evolution article, "去掉分母引入卷积") the token stage stages bf16 mixed_qkv
+// rows with a three-position halo and runs the width-4 conv + SiLU there (taps and biases in
+// shared memory, the slot's conv state standing in for the positions before the prompt); the
+// conv outputs are fp32 and take the three-term split like fp32 inputs.
 #include <atomic>
 
 #include "gdn_tc.cuh"
@@ -69,6 +74,16 @@ constexpr uint32_t OFF_A = OFF_V + TC_C * TD * 4;        // A column-major [s][T
 constexpr uint32_t OFF_ST = (OFF_A + TC_C * TC_ATS * 4 + 1023u) & ~1023u;  // staging (1024-aligned: swizzle atoms)
 constexpr uint32_t OFF_G = OFF_ST + 3 * TC_C * TD * 4;   // gamma, beta, e^gamma, e^{gamma_C - gamma},
                                                          // key and query scale factors, e^-gamma, flags
+// Fused conv (GDN_FUSE_CONV, bf16 mixed_qkv; evolution article, "去掉分母引入卷积"): every staged
+// box holds the chunk's rows with the three positions before them (35 rows, position t0 - 3 + r
+// in row r), padded to whole 1024-byte swizzle atoms (in the first chunk the slot's conv state
+// replaces rows 0-2); the head's conv taps and biases sit in the rest of the staging area.
+constexpr int CV_ROWS = TC_C + 3;
+constexpr uint32_t CV_BOX = 5 * 1024;
+constexpr uint32_t CV_CH = 3 * TD;                         // the head's q, k and v channels
+constexpr uint32_t OFF_CW = OFF_ST + 3 * 2 * CV_BOX;       // taps of channel c as one float4
+constexpr uint32_t OFF_CB = OFF_CW + CV_CH * 16;           // biases
+static_assert(CV_ROWS * 128 <= CV_BOX && OFF_CB + CV_CH * 4 <= OFF_G, "fused-conv staging");
 constexpr uint32_t OFF_BAR = OFF_G + 8 * TC_C * 4;       // mbarriers: ps, p1, p2, drain, then one
                                                          // per compute warp for its staged rows
 constexpr uint32_t OFF_TMEM = OFF_BAR + 12 * 8;
@@ -123,6 +138,48 @@ __device__ __forceinline__ float4 staged4(const unsigned char* st, int tensor, i
   return *reinterpret_cast<const float4*>(at);
 }
 
+// Fused conv: byte offset of bf16 element c of tensor `tensor` at staged row r
+__device__ __forceinline__ uint32_t conv_at(int tensor, int r, int c) {
+  const uint32_t byte = 2u * static_cast<uint32_t>(c);
+  const uint32_t inb = byte & 127u;
+  return OFF_ST + static_cast<uint32_t>(tensor) * (2 * CV_BOX) + (byte >> 7) * CV_BOX + static_cast<uint32_t>(r) * 128u +
+         ((((inb >> 4) ^ (static_cast<uint32_t>(r) & 7u)) << 4) | (inb & 15u));
+}
+
+// Fused conv: pre-conv inputs, channels 4g .. 4g+3 of tensor `tensor`, at staged row r (position
+// t0 - 3 + r).
+__device__ __forceinline__ float4 conv_in4(const unsigned char* smem, int tensor, int r, int g) {
+  const uint32_t byte = 8u * static_cast<uint32_t>(g);
+  const uint32_t inb = byte & 127u;
+  const unsigned char* at = smem + OFF_ST + static_cast<uint32_t>(tensor) * (2 * CV_BOX) + (byte >> 7) * CV_BOX +
+                            static_cast<uint32_t>(r) * 128u +
+                            ((((inb >> 4) ^ (static_cast<uint32_t>(r) & 7u)) << 4) | (inb & 15u));
+  const uint2 u = *reinterpret_cast<const uint2*>(at);
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                     __uint_as_float(u.y & 0xffff0000u));
+}
+
+// Width-4 causal conv + SiLU of one channel from its inputs at positions t-3 .. t (tap 3 on the
+// current one), in the decode kernels' product order (a missing bias is staged as 0); the SiLU
+// through the fast intrinsics (relative error a few parts in 10^7; z e^-z -> 0 below -88).
+__device__ __forceinline__ float conv1(float x0, float x1, float x2, float x3, float4 w, float bias) {
+  float acc = x0 * w.x;
+  acc = fmaf(x1, w.y, acc);
+  acc = fmaf(x2, w.z, acc);
+  acc = fmaf(x3, w.w, acc);
+  const float z = acc + bias;
+  return z * __fdividef(1.0f, 1.0f + __expf(-z));
+}
+
+// Four channels (4g .. 4g+3 of tensor `tensor`) of the conv output from their four input rows.
+__device__ __forceinline__ float4 conv4(const unsigned char* smem, int tensor, int g, float4 a, float4 b, float4 c,
+                                        float4 d) {
+  const float4* w = reinterpret_cast<const float4*>(smem + OFF_CW) + tensor * TD + 4 * g;
+  const float4 cb = *(reinterpret_cast<const float4*>(smem + OFF_CB) + tensor * (TD / 4) + g);
+  return make_float4(conv1(a.x, b.x, c.x, d.x, w[0], cb.x), conv1(a.y, b.y, c.y, d.y, w[1], cb.y),
+                     conv1(a.z, b.z, c.z, d.z, w[2], cb.z), conv1(a.w, b.w, c.w, d.w, w[3], cb.w));
+}
+
 // The token tensors q, k, v as 3-D tensor maps (element, head, position over all requests):
 // dims {128, H, B*T}, boxes {128 bytes of elements, 1, 32}, 128-byte swizzle.
 struct TokenMaps {
@@ -145,6 +202,9 @@ __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
+// CONV: q, k, v are the width-4 conv + SiLU of bf16 mixed_qkv rows (the maps cover its q, k and
+// v thirds), through the slot's conv state, which afterwards holds the prompt's last three inputs.
+template <bool CONV>
 __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodeParams p, const __grid_constant__ TokenMaps maps) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -156,8 +216,8 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
   const bool l2 = (fl & GDN_NO_QK_L2NORM) == 0u;
   // bf16 inputs are exact TF32 values: the products run on the raw q and k (one TF32 term
   // for the pair sums, two for the state read) and the L2-norm scales are applied to the
-  // results; fp32 inputs are split into hi and lo after normalisation
-  const bool exact = bf16;
+  // results; fp32 inputs (and conv outputs) are split into hi and lo after normalisation
+  const bool exact = bf16 && !CONV;
   const int T = p.T;
 
   griddep_launch_dependents();
@@ -211,14 +271,28 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
   const int nbox = bf16 ? 2 : 4;
   auto prefetch = [&](int t0, int n) {
     if (warp == ISSUER) {
-      tc::expect_tx(stbar, 3u * static_cast<uint32_t>(nbox) * ST_BOX);
-      const int z = b * T + t0;
+      if (CONV) {
+        // 35 rows from position t0 - 3 (before the request's first row the copy reads the
+        // previous request's rows or, at coordinate -3, the fill value: the conv state stands in)
+        tc::expect_tx(stbar, 3u * 2u * CV_ROWS * 128u);
+        const int z = b * T + t0 - 3;
 #pragma unroll
-      for (int tensor = 0; tensor < 3; ++tensor) {
-        const CUtensorMap* map = tensor == 0 ? &maps.q : (tensor == 1 ? &maps.k : &maps.v);
-        for (int bx = 0; bx < nbox; ++bx)
-          tma_load_3d(smem_addr(smem + OFF_ST + static_cast<uint32_t>(tensor) * (TC_C * TD * esz) + bx * ST_BOX), map,
-                      bx * static_cast<int>(128u / esz), h, z, stbar);
+        for (int tensor = 0; tensor < 3; ++tensor) {
+          const CUtensorMap* map = tensor == 0 ? &maps.q : (tensor == 1 ? &maps.k : &maps.v);
+          for (int bx = 0; bx < 2; ++bx)
+            tma_load_3d(smem_addr(smem + OFF_ST + static_cast<uint32_t>(tensor) * (2 * CV_BOX) + bx * CV_BOX), map,
+                        bx * 64, h, z, stbar);
+        }
+      } else {
+        tc::expect_tx(stbar, 3u * static_cast<uint32_t>(nbox) * ST_BOX);
+        const int z = b * T + t0;
+#pragma unroll
+        for (int tensor = 0; tensor < 3; ++tensor) {
+          const CUtensorMap* map = tensor == 0 ? &maps.q : (tensor == 1 ? &maps.k : &maps.v);
+          for (int bx = 0; bx < nbox; ++bx)
+            tma_load_3d(smem_addr(smem + OFF_ST + static_cast<uint32_t>(tensor) * (TC_C * TD * esz) + bx * ST_BOX),
+                        map, bx * static_cast<int>(128u / esz), h, z, stbar);
+        }
       }
       ++st_loads;
     }
@@ -229,6 +303,16 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
     }
   };
   prefetch(0, n_tok < TC_C ? n_tok : TC_C);
+
+  if (CONV && warp < ISSUER) {
+    // the head's conv taps and biases for the compute warps (visible after the barrier that
+    // follows the TMEM allocation)
+    for (int i = tid; i < static_cast<int>(CV_CH); i += ISSUER * 32) {
+      const int ch = (i >> 7) * p.H * TD + h * TD + (i & (TD - 1));
+      reinterpret_cast<float4*>(smem + OFF_CW)[i] = __ldg(reinterpret_cast<const float4*>(p.conv_w) + ch);
+      reinterpret_cast<float*>(smem + OFF_CB)[i] = p.conv_b != nullptr ? __ldg(p.conv_b + ch) : 0.0f;
+    }
+  }
 
   if (warp == 0) {
     tc::tmem_alloc(tmem_slot, TM_COLS);
@@ -266,6 +350,7 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
   // each), then the value rows 8w..8w+7; warps 4-7: query rows the same way; warp 4 also the
   // gates.
   // Ends with the pair-sum MMAs of the chunk issued (they need nothing of the state).
+  int t0 = 0;  // the chunk's first position
   auto token_stage = [&](int n) {
    if (warp < ISSUER) {
     if (!wait_warp(stbar, st_par)) bad = true;  // the chunk's rows have landed
@@ -275,9 +360,29 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
     const bool live = t < n;
     const bool isk = warp < 4;
     const unsigned char* st = smem + OFF_ST;
+    const int r = isk ? t : TC_C + t;
     float4 x[8];
+    float ss = 0.0f;
+    if (CONV) {
+      // position t's conv output from staged rows t .. t+3 (positions t-3 .. t), parked in the
+      // hi tile at the place its normalised hi part goes (this thread reads it back below)
+      const int tensor = isk ? 1 : 0;
+#pragma unroll 2
+      for (int i = 0; i < 8; ++i) {
+        const int g = g0 + 4 * i;
+        const float4 y = live ? conv4(smem, tensor, g, conv_in4(smem, tensor, t, g), conv_in4(smem, tensor, t + 1, g),
+                                      conv_in4(smem, tensor, t + 2, g), conv_in4(smem, tensor, t + 3, g))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        ss += y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
+        *reinterpret_cast<float4*>(smem + OFF_XH + kmaj_off(r, 4 * g, X_LBO)) = y;
+      }
+    } else {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) x[i] = live ? staged4(st, isk ? 1 : 0, t, g0 + 4 * i, bf16) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i = 0; i < 8; ++i)
+        x[i] = live ? staged4(st, isk ? 1 : 0, t, g0 + 4 * i, bf16) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss += x[i].x * x[i].x + x[i].y * x[i].y + x[i].z * x[i].z + x[i].w * x[i].w;
+    }
     if (warp == 4) {  // gates of the chunk, lane = token
       const bool lv = lane < n;
       float lam = pf_lam, be = pf_beta;
@@ -302,24 +407,44 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
       ein[lane] = split ? expf(-g) : 0.0f;
       if (lane == 0) *ratio_split = split ? 1 : 0;
     }
-    float ss = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) ss += x[i].x * x[i].x + x[i].y * x[i].y + x[i].z * x[i].z + x[i].w * x[i].w;
     ss += __shfl_xor_sync(0xffffffffu, ss, 8);
     ss += __shfl_xor_sync(0xffffffffu, ss, 16);
     const float sc = (l2 ? rsqrtf(ss + p.l2_eps) : 1.0f) * (isk ? 1.0f : p.q_scale);
-    const int r = isk ? t : TC_C + t;
     if ((lane >> 3) == 0) (isk ? skf : sqf)[t] = exact ? sc : 1.0f;
+    if (CONV) {
+#pragma unroll 2
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t off = kmaj_off(r, 4 * (g0 + 4 * i), X_LBO);
+        const float4 y = *reinterpret_cast<const float4*>(smem + OFF_XH + off);
+        store_split4(smem, OFF_XH, OFF_XL, off, y.x * sc, y.y * sc, y.z * sc, y.w * sc);
+      }
+    } else {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int g = g0 + 4 * i;
-      const float a0 = x[i].x * sc, a1 = x[i].y * sc, a2 = x[i].z * sc, a3 = x[i].w * sc;
-      if (exact)  // the raw values: exact TF32, no remainder
-        *reinterpret_cast<float4*>(smem + OFF_XH + kmaj_off(r, 4 * g, X_LBO)) = x[i];
-      else
-        store_split4(smem, OFF_XH, OFF_XL, kmaj_off(r, 4 * g, X_LBO), a0, a1, a2, a3);
+      for (int i = 0; i < 8; ++i) {
+        const int g = g0 + 4 * i;
+        const float a0 = x[i].x * sc, a1 = x[i].y * sc, a2 = x[i].z * sc, a3 = x[i].w * sc;
+        if (exact)  // the raw values: exact TF32, no remainder
+          *reinterpret_cast<float4*>(smem + OFF_XH + kmaj_off(r, 4 * g, X_LBO)) = x[i];
+        else
+          store_split4(smem, OFF_XH, OFF_XL, kmaj_off(r, 4 * g, X_LBO), a0, a1, a2, a3);
+      }
     }
-    if (isk) {
+    if (CONV) {
+      // value rows v0 .. v0+3 (four per compute warp), channels 4 lane .. 4 lane + 3: a sliding
+      // window of input rows
+      const int v0 = 16 * (warp >> 2) + 4 * wq;
+      float4 xa = conv_in4(smem, 2, v0, lane), xb = conv_in4(smem, 2, v0 + 1, lane), xc = conv_in4(smem, 2, v0 + 2, lane);
+#pragma unroll 1
+      for (int u = 0; u < 4; ++u) {
+        const int tv = v0 + u;
+        const float4 xd = conv_in4(smem, 2, tv + 3, lane);
+        reinterpret_cast<float4*>(V + tv * TD)[lane] =
+            tv < n ? conv4(smem, 2, lane, xa, xb, xc, xd) : make_float4(0.f, 0.f, 0.f, 0.f);
+        xa = xb;
+        xb = xc;
+        xc = xd;
+      }
+    } else if (isk) {
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int tv = 8 * wq + u;
@@ -348,8 +473,20 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
     }
   };
 
-  int t0 = 0;
   int n = n_tok < TC_C ? n_tok : TC_C;
+  if (CONV && warp < ISSUER) {
+    // first chunk: the slot's conv state (pre-conv inputs at positions -3 .. -1) over staged
+    // rows 0-2, once the copy has landed there (the token stage's wait then finds it complete)
+    if (!wait_warp(stbar, 0u)) bad = true;
+    const uint16_t* cp = static_cast<const uint16_t*>(p.conv_pool);
+    for (int i = tid; i < static_cast<int>(CV_CH); i += ISSUER * 32) {
+      const int tensor = i >> 7, c = i & (TD - 1);
+      const uint16_t* cs = cp + (static_cast<size_t>(slot) * p.channels + tensor * p.H * TD + h * TD + c) * 3;
+#pragma unroll
+      for (int r = 0; r < 3; ++r) *reinterpret_cast<uint16_t*>(smem + conv_at(tensor, r, c)) = cs[r];
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");  // the compute warps
+  }
   token_stage(n);
   if (TC_C < n_tok) prefetch(TC_C, n_tok - TC_C < TC_C ? n_tok - TC_C : TC_C);
   int prev_t0 = 0, prev_n = 0;
@@ -399,7 +536,7 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
       const int s = 8 * warp + (lane & 7);
       const float f = ek[s], sk = skf[s];
       const int g0 = lane >> 3;
-#pragma unroll
+#pragma unroll(CONV ? 2 : 8)
       for (int i = 0; i < 8; ++i) {
         const int c = 4 * (g0 + 4 * i);
         const uint32_t xo = kmaj_off(s, c, X_LBO);
@@ -617,6 +754,24 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
 #pragma unroll
       for (int k = 0; k < 16; ++k) Sg[static_cast<size_t>(c0 + 16 * cc + k) * TD + j] = v[k];
     }
+    if (CONV) {
+      // the conv state keeps the last three inputs of (old state, prompt), bit-exact; each
+      // thread reads all three of a channel's before it writes them
+      uint16_t* cp = static_cast<uint16_t*>(p.conv_pool);
+      const uint16_t* mx = static_cast<const uint16_t*>(p.mixed);
+      for (int i = tid; i < static_cast<int>(CV_CH); i += ISSUER * 32) {
+        const int ch = (i >> 7) * p.H * TD + h * TD + (i & (TD - 1));
+        uint16_t* cs = cp + (static_cast<size_t>(slot) * p.channels + ch) * 3;
+        uint16_t nb[3];
+#pragma unroll
+        for (int col = 0; col < 3; ++col) {
+          const int pos = n_tok - 3 + col;
+          nb[col] = pos >= 0 ? __ldg(mx + (static_cast<size_t>(b) * T + pos) * p.channels + ch) : cs[pos + 3];
+        }
+#pragma unroll
+        for (int col = 0; col < 3; ++col) cs[col] = nb[col];
+      }
+    }
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -629,32 +784,42 @@ constexpr int kMaxDevices = 64;
 }  // namespace
 
 bool prefill_tc_supported(const DecodeParams& p) {
-  // (the token tensors' position coordinate b*T + t is a 32-bit tensor-copy coordinate)
-  return p.D == TD && p.dlam == 1 && (p.flags & (GDN_FUSE_CONV | GDN_GATE_KDA | GDN_OUT_NORM_GATE)) == 0u &&
-         static_cast<long long>(p.B) * p.T <= 0x7fffffffLL;
+  // (the token tensors' position coordinate b*T + t is a 32-bit tensor-copy coordinate; the
+  // fused conv stages bf16 mixed_qkv rows only)
+  const bool conv = (p.flags & GDN_FUSE_CONV) != 0u;
+  return p.D == TD && p.dlam == 1 && (p.flags & (GDN_GATE_KDA | GDN_OUT_NORM_GATE)) == 0u &&
+         (!conv || (p.flags & GDN_QKV_BF16) != 0u) && static_cast<long long>(p.B) * p.T <= 0x7fffffffLL;
 }
 
-cudaError_t launch_prefill_tc(const DecodeParams& p, cudaStream_t stream) {
+namespace {
+
+template <bool CONV>
+cudaError_t launch_prefill_tc_k(const DecodeParams& p, cudaStream_t stream) {
   static std::atomic<int> configured[kMaxDevices];
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (!configured[dev].load(std::memory_order_relaxed)) {
-    err = cudaFuncSetAttribute(gdn_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err = cudaFuncSetAttribute(gdn_prefill_tc_kernel<CONV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(TC_SMEM));
     if (err != cudaSuccess) return err;
     configured[dev].store(1, std::memory_order_relaxed);
   }
   // q, k, v as [B*T][H][128] tensors: boxes of 128 bytes of elements x 1 head x 32 positions
+  // (fused conv: the q, k and v thirds of the [B*T][3*H*128] mixed_qkv rows, 35 positions)
   TokenMaps maps;
   const bool bf16 = (p.flags & GDN_QKV_BF16) != 0u;
   const cuuint64_t esz = bf16 ? 2u : 4u;
+  const cuuint64_t row = CONV ? static_cast<cuuint64_t>(p.channels) : static_cast<cuuint64_t>(p.H) * TD;
   const cuuint64_t dims[3] = {TD, static_cast<cuuint64_t>(p.H), static_cast<cuuint64_t>(p.B) * static_cast<cuuint64_t>(p.T)};
-  const cuuint64_t strides[2] = {TD * esz, static_cast<cuuint64_t>(p.H) * TD * esz};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128u / esz), 1u, static_cast<cuuint32_t>(TC_C)};
+  const cuuint64_t strides[2] = {TD * esz, row * esz};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128u / esz), 1u, static_cast<cuuint32_t>(CONV ? CV_ROWS : TC_C)};
   const CUtensorMapDataType ty = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const size_t third = static_cast<size_t>(p.H) * TD * esz;
   const void* bases[3] = {p.q, p.k, p.v};
+  if (CONV)
+    for (int i = 0; i < 3; ++i) bases[i] = static_cast<const unsigned char*>(p.mixed) + i * third;
   CUtensorMap* out[3] = {&maps.q, &maps.k, &maps.v};
   for (int i = 0; i < 3; ++i) {
     err = encode_tiled(out[i], ty, 3, bases[i], dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -670,9 +835,15 @@ cudaError_t launch_prefill_tc(const DecodeParams& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, gdn_prefill_tc_kernel, p, maps);
+  err = cudaLaunchKernelEx(&cfg, gdn_prefill_tc_kernel<CONV>, p, maps);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const DecodeParams& p, cudaStream_t stream) {
+  return (p.flags & GDN_FUSE_CONV) ? launch_prefill_tc_k<true>(p, stream) : launch_prefill_tc_k<false>(p, stream);
 }
 
 }  // namespace gdn

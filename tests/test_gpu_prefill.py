@@ -448,3 +448,14 @@ def test_prefill_strong_and_weak_per_head_decay(lam_mean):
     pg = pool.cpu().numpy().astype(np.float64)
     serr = float(np.max(np.abs(pg - pool_ref))) / float(np.max(np.abs(pool_ref)))
     assert err / scale <= TOL and serr <= TOL, (lam_mean, err / scale, serr)
+
+
+def test_prefill_fused_conv_tensor_core_ragged_chunks_no_bias():
+    """The fused conv on the 128-wide tensor-core prefill: three heads (the q, k and v thirds
+    of mixed_qkv at every head offset), prompts that end inside the conv state's reach (1, 3),
+    at and around chunk edges (31, 32, 35, 64) and over several chunks (97, 200), no bias;
+    request 0 is live (its copies start before the first row of the tensor); conv states
+    bit-exact afterwards."""
+    e_o, e_s, ok, _ = _run_ext(128, False, 200, np.array([200, 3, 1, 31, 32, 35, 97, 64]), conv=True,
+                               bias=False, H=3, slot=[0, 5, 2, 7, 1, 3, 6, 4], seed=81)
+    assert e_o <= TOL and e_s <= TOL and ok, (e_o, e_s, ok)
