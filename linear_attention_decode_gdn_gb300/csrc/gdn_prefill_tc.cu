@@ -171,13 +171,19 @@ __device__ __forceinline__ float conv1(float x0, float x1, float x2, float x3, f
   return z * __fdividef(1.0f, 1.0f + __expf(-z));
 }
 
-// Four channels (4g .. 4g+3 of tensor `tensor`) of the conv output from their four input rows.
-__device__ __forceinline__ float4 conv4(const unsigned char* smem, int tensor, int g, float4 a, float4 b, float4 c,
-                                        float4 d) {
+// The taps (one float4 per channel) and biases of channels 4g .. 4g+3 of tensor `tensor`.
+struct ConvW4 {
+  float4 w0, w1, w2, w3, cb;
+};
+__device__ __forceinline__ ConvW4 conv_w4(const unsigned char* smem, int tensor, int g) {
   const float4* w = reinterpret_cast<const float4*>(smem + OFF_CW) + tensor * TD + 4 * g;
-  const float4 cb = *(reinterpret_cast<const float4*>(smem + OFF_CB) + tensor * (TD / 4) + g);
-  return make_float4(conv1(a.x, b.x, c.x, d.x, w[0], cb.x), conv1(a.y, b.y, c.y, d.y, w[1], cb.y),
-                     conv1(a.z, b.z, c.z, d.z, w[2], cb.z), conv1(a.w, b.w, c.w, d.w, w[3], cb.w));
+  return {w[0], w[1], w[2], w[3], *(reinterpret_cast<const float4*>(smem + OFF_CB) + tensor * (TD / 4) + g)};
+}
+
+// Four channels of the conv output from their input rows at positions t-3 .. t.
+__device__ __forceinline__ float4 conv4(const ConvW4& w, float4 a, float4 b, float4 c, float4 d) {
+  return make_float4(conv1(a.x, b.x, c.x, d.x, w.w0, w.cb.x), conv1(a.y, b.y, c.y, d.y, w.w1, w.cb.y),
+                     conv1(a.z, b.z, c.z, d.z, w.w2, w.cb.z), conv1(a.w, b.w, c.w, d.w, w.w3, w.cb.w));
 }
 
 // The token tensors q, k, v as 3-D tensor maps (element, head, position over all requests):
@@ -364,25 +370,39 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
     float4 x[8];
     float ss = 0.0f;
     if (CONV) {
-      // position t's conv output from staged rows t .. t+3 (positions t-3 .. t), parked in the
-      // hi tile at the place its normalised hi part goes (this thread reads it back below)
+      // the conv outputs of the warp's eight rows, first with lane = channel group over a
+      // sliding window of staged rows (row u's output from staged rows u .. u+3, positions
+      // u-3 .. u; taps and biases loaded once), parked in a per-warp scratch in the [K; Q]
+      // remainder tile (free until the split below: row u at 512 u, channel group g in 16-byte
+      // slot g ^ u, conflict-free both ways), then read back with this thread's row and groups
       const int tensor = isk ? 1 : 0;
-#pragma unroll 2
-      for (int i = 0; i < 8; ++i) {
-        const int g = g0 + 4 * i;
-        const float4 y = live ? conv4(smem, tensor, g, conv_in4(smem, tensor, t, g), conv_in4(smem, tensor, t + 1, g),
-                                      conv_in4(smem, tensor, t + 2, g), conv_in4(smem, tensor, t + 3, g))
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-        ss += y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
-        *reinterpret_cast<float4*>(smem + OFF_XH + kmaj_off(r, 4 * g, X_LBO)) = y;
+      const int r0 = 8 * wq;
+      unsigned char* scr = smem + OFF_XL + warp * 4096;
+      {
+        const ConvW4 cw = conv_w4(smem, tensor, lane);
+        float4 xa = conv_in4(smem, tensor, r0, lane), xb = conv_in4(smem, tensor, r0 + 1, lane),
+               xc = conv_in4(smem, tensor, r0 + 2, lane);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float4 xd = conv_in4(smem, tensor, r0 + u + 3, lane);
+          *reinterpret_cast<float4*>(scr + u * 512 + ((lane ^ u) << 4)) =
+              r0 + u < n ? conv4(cw, xa, xb, xc, xd) : make_float4(0.f, 0.f, 0.f, 0.f);
+          xa = xb;
+          xb = xc;
+          xc = xd;
+        }
       }
+      __syncwarp();
+      const int tl = lane & 7;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = *reinterpret_cast<const float4*>(scr + tl * 512 + (((g0 + 4 * i) ^ tl) << 4));
     } else {
 #pragma unroll
       for (int i = 0; i < 8; ++i)
         x[i] = live ? staged4(st, isk ? 1 : 0, t, g0 + 4 * i, bf16) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) ss += x[i].x * x[i].x + x[i].y * x[i].y + x[i].z * x[i].z + x[i].w * x[i].w;
     }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss += x[i].x * x[i].x + x[i].y * x[i].y + x[i].z * x[i].z + x[i].w * x[i].w;
     if (warp == 4) {  // gates of the chunk, lane = token
       const bool lv = lane < n;
       float lam = pf_lam, be = pf_beta;
@@ -411,35 +431,28 @@ __global__ void __launch_bounds__(TC_NT, 1) gdn_prefill_tc_kernel(const DecodePa
     ss += __shfl_xor_sync(0xffffffffu, ss, 16);
     const float sc = (l2 ? rsqrtf(ss + p.l2_eps) : 1.0f) * (isk ? 1.0f : p.q_scale);
     if ((lane >> 3) == 0) (isk ? skf : sqf)[t] = exact ? sc : 1.0f;
-    if (CONV) {
-#pragma unroll 2
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t off = kmaj_off(r, 4 * (g0 + 4 * i), X_LBO);
-        const float4 y = *reinterpret_cast<const float4*>(smem + OFF_XH + off);
-        store_split4(smem, OFF_XH, OFF_XL, off, y.x * sc, y.y * sc, y.z * sc, y.w * sc);
-      }
-    } else {
+    if (CONV) asm volatile("bar.sync 1, 256;" ::: "memory");  // every warp's scratch is read
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int g = g0 + 4 * i;
-        const float a0 = x[i].x * sc, a1 = x[i].y * sc, a2 = x[i].z * sc, a3 = x[i].w * sc;
-        if (exact)  // the raw values: exact TF32, no remainder
-          *reinterpret_cast<float4*>(smem + OFF_XH + kmaj_off(r, 4 * g, X_LBO)) = x[i];
-        else
-          store_split4(smem, OFF_XH, OFF_XL, kmaj_off(r, 4 * g, X_LBO), a0, a1, a2, a3);
-      }
+    for (int i = 0; i < 8; ++i) {
+      const int g = g0 + 4 * i;
+      const float a0 = x[i].x * sc, a1 = x[i].y * sc, a2 = x[i].z * sc, a3 = x[i].w * sc;
+      if (exact)  // the raw values: exact TF32, no remainder
+        *reinterpret_cast<float4*>(smem + OFF_XH + kmaj_off(r, 4 * g, X_LBO)) = x[i];
+      else
+        store_split4(smem, OFF_XH, OFF_XL, kmaj_off(r, 4 * g, X_LBO), a0, a1, a2, a3);
     }
     if (CONV) {
       // value rows v0 .. v0+3 (four per compute warp), channels 4 lane .. 4 lane + 3: a sliding
       // window of input rows
       const int v0 = 16 * (warp >> 2) + 4 * wq;
+      const ConvW4 cw = conv_w4(smem, 2, lane);
       float4 xa = conv_in4(smem, 2, v0, lane), xb = conv_in4(smem, 2, v0 + 1, lane), xc = conv_in4(smem, 2, v0 + 2, lane);
-#pragma unroll 1
+#pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int tv = v0 + u;
         const float4 xd = conv_in4(smem, 2, tv + 3, lane);
         reinterpret_cast<float4*>(V + tv * TD)[lane] =
-            tv < n ? conv4(smem, 2, lane, xa, xb, xc, xd) : make_float4(0.f, 0.f, 0.f, 0.f);
+            tv < n ? conv4(cw, xa, xb, xc, xd) : make_float4(0.f, 0.f, 0.f, 0.f);
         xa = xb;
         xb = xc;
         xc = xd;
