@@ -459,3 +459,97 @@ def test_prefill_fused_conv_tensor_core_ragged_chunks_no_bias():
     e_o, e_s, ok, _ = _run_ext(128, False, 200, np.array([200, 3, 1, 31, 32, 35, 97, 64]), conv=True,
                                bias=False, H=3, slot=[0, 5, 2, 7, 1, 3, 6, 4], seed=81)
     assert e_o <= TOL and e_s <= TOL and ok, (e_o, e_s, ok)
+
+
+def _sampled_full_shape(name, T, pairs, seed):
+    """gdn_prefill over a workload's whole batch (B requests x H heads, the grid the bench times),
+    from a zero state, checked against the oracle on sampled (request, head) pairs: every
+    position's output and the final state (and conv state) of each sampled head. Inputs as the
+    bench draws them: N(0,1) bf16 q/k/v (or mixed_qkv through the workload's conv weights),
+    alpha = sigmoid(N(0,1) + 3), beta = sigmoid(N(0,1)); the KDA workload takes its raw gate
+    f = N(0,1) and write logit, and N(0,1) output gates."""
+    w = wl.WORKLOADS[name]
+    B, H, D, dlam = w.batch, w.num_heads, w.dk, w.dlam
+    r = np.random.default_rng(seed)
+    flags, oflags = gdn.QKV_BF16, oracle.L2NORM
+    dev, smp = {}, [dict() for _ in pairs]
+    chans = [np.concatenate([np.arange(t * H * D + h * D, t * H * D + (h + 1) * D) for t in range(3)])
+             for _, h in pairs]
+    if w.conv:
+        flags |= gdn.FUSE_CONV
+        bits, a = wl.bf16_round(r.standard_normal((B, T, w.channels), dtype=np.float32))
+        dev["mixed_qkv"] = dev_bf16(bits)
+        del bits
+        cw = wl.conv_weights(w)
+        dev["conv_w"] = dev_f32(cw)
+        dev["conv_pool"] = torch.zeros((B, w.channels, 3), dtype=torch.bfloat16, device="cuda")
+        for i, (b, h) in enumerate(pairs):
+            smp[i].update(mixed=a[b:b + 1][:, :, chans[i]].astype(np.float64), conv_w=cw[chans[i]].astype(np.float64),
+                          conv_b=None, conv_pool=np.zeros((1, 3 * D, 3)))
+        del a
+    else:
+        for n in ("q", "k", "v"):
+            bits, a = wl.bf16_round(r.standard_normal((B, T, H, D), dtype=np.float32))
+            dev[n] = dev_bf16(bits)
+            for i, (b, h) in enumerate(pairs):
+                smp[i][n] = a[b:b + 1, :, h:h + 1].astype(np.float64)
+            del bits, a
+    a_raw = r.standard_normal((B, T, H, dlam), dtype=np.float32) + np.float32(3)
+    b_raw = r.standard_normal((B, T, H), dtype=np.float32)
+    if w.kda_full:
+        flags |= gdn.GATE_KDA | gdn.OUT_NORM_GATE
+        oflags |= oracle.GATE_KDA | oracle.OUT_NORM_GATE
+        kp = wl.kda_gate_params(w)
+        lam, beta = a_raw - np.float32(3), b_raw
+        g = r.standard_normal((B, T, H, D), dtype=np.float32)
+        dev.update(out_gate=dev_f32(g), **{n: dev_f32(kp[n]) for n in ("a_log", "dt_bias", "out_norm_w")})
+        for i, (b, h) in enumerate(pairs):
+            smp[i].update(out_gate=g[b:b + 1, :, h:h + 1].astype(np.float64),
+                          a_log=kp["a_log"][h:h + 1].astype(np.float64),
+                          dt_bias=kp["dt_bias"][h:h + 1].astype(np.float64),
+                          out_norm_w=kp["out_norm_w"].astype(np.float64), lower_bound=kp["lower_bound"])
+        del g
+    else:
+        lam = (-np.log1p(np.exp(-a_raw.astype(np.float64)))).astype(np.float32)
+        beta = (1 / (1 + np.exp(-b_raw.astype(np.float64)))).astype(np.float32)
+    dev.update(log_decay=dev_f32(lam), beta=dev_f32(beta))
+    for i, (b, h) in enumerate(pairs):
+        smp[i].update(lam=lam[b:b + 1, :, h:h + 1].astype(np.float64), beta=beta[b:b + 1, :, h:h + 1].astype(np.float64))
+    del lam, beta, a_raw, b_raw
+    dims = gdn.make_dims(B, H, D, num_slots=B, decay_per_key=w.decay_per_key, flags=flags, q_scale=D ** -0.5)
+    pool = torch.zeros((B, H, D, D), dtype=torch.float32, device="cuda")
+    o = torch.full((B, T, H, D), 5.0, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gdn.prefill(dims, T, gdn.make_inputs(slot=dev_i32(np.arange(B)), **dev), pool, o, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    cfg = dict(batch=1, num_heads=1, dk=D, dv=D, num_slots=1, dlam=dlam, log_capacity=0, flags=oflags,
+               q_scale=D ** -0.5, l2_eps=1e-6)
+    for i, (b, h) in enumerate(pairs):
+        pool_ref = np.zeros((1, 1, D, D))
+        o_ref = oracle.prefill_batch(cfg, pool_ref, np.zeros(1, np.int32), np.array([T]), **smp[i])
+        og = o[b, :, h].cpu().numpy().astype(np.float64)
+        e_o = float(np.max(np.abs(og - o_ref[0, :, 0]))) / float(np.max(np.abs(o_ref[0, :, 0])))
+        sg = pool[b, h].cpu().numpy().astype(np.float64)
+        e_s = float(np.max(np.abs(sg - pool_ref[0, 0]))) / float(np.max(np.abs(pool_ref[0, 0])))
+        assert e_o <= TOL and e_s <= TOL, (name, b, h, e_o, e_s)
+        if w.conv:
+            cp = dev["conv_pool"][b][torch.from_numpy(chans[i]).cuda()].cpu()
+            cg = (cp.view(torch.int16).numpy().astype(np.uint16).astype(np.uint32) << 16).view(np.float32)
+            assert np.array_equal(cg.astype(np.float64), smp[i]["conv_pool"][0]), (name, b, h)
+
+
+def test_prefill_headline_full_batch_sampled():
+    """The headline prefill (B=128, H=32, T=256: the tensor-core kernel for a per-head decay)."""
+    _sampled_full_shape("headline", 256, [(0, 0), (127, 31), (5, 17), (64, 3), (99, 26)], seed=91)
+
+
+def test_prefill_small_conv_full_batch_sampled():
+    """The fused-conv prefill at its workload's full batch (B=64, H=16, T=256)."""
+    _sampled_full_shape("small_conv", 256, [(0, 0), (63, 15), (17, 8), (40, 1)], seed=92)
+
+
+def test_prefill_kda_full_full_batch_sampled():
+    """The per-key tensor-core prefill with the KDA gate and epilogue at its workload's full
+    batch (B=256, H=32), prompts of 128 positions."""
+    _sampled_full_shape("kda_full", 128, [(0, 0), (255, 31), (128, 16), (77, 9)], seed=93)
