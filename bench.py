@@ -188,6 +188,31 @@ def head_bytes(mode: str, n: int, w, klb=2, conv=False, ulb=4) -> int:
 
 # ----------------------------------------------------------------------------- GPU arm
 
+# Prefill on the other tensor-core prefill kernels, measured beside the headline one:
+# (workload, positions per request) -- the fused conv, and the per-key decay with the KDA gate
+# and output epilogue.
+PREFILL_CONFIGS = (("small_conv", 256), ("kda_full", 128))
+
+
+def run_prefill_configs(args, dev, stream, gdn, runner=None):
+    """The prefill leg on each of PREFILL_CONFIGS; a leg that raises is reported as
+    unavailable, with the error, instead of ending the run. Returns (legs, launches)."""
+    import argparse
+    from linear_attention_decode_gdn_gb300 import workloads as wl
+    runner = runner or run_prefill
+    legs, launches = {}, 0
+    for name, T in PREFILL_CONFIGS:
+        w = wl.WORKLOADS[name]
+        leg_args = argparse.Namespace(**dict(vars(args), prefill=T))
+        try:
+            leg = runner(leg_args, w, decode_flags(gdn, w), dev, stream, gdn)
+        except Exception as e:  # noqa: BLE001 -- one leg's failure must not cost the bench line
+            leg = {"unavailable": f"{type(e).__name__}: {e}"}
+        launches += int(leg.get("launches", 0))
+        legs[f"{name}/T{T}"] = dict(leg, workload=f"{name}: {w.description}")
+    return legs, launches
+
+
 def decode_flags(gdn, w, klog_prenorm=False) -> int:
     flags = (gdn.QKV_BF16 if w.qkv_bf16 else 0) | (gdn.FUSE_CONV if w.conv else 0)
     if klog_prenorm:
@@ -588,9 +613,13 @@ def run_gpu(args, rank, local_rank, world):
         sweep_clocks = sclocks.summary()
     verify = run_verify(args, w, flags, dev, stream, gdn, peak) if args.verify else None
     prefill = run_prefill(args, w, flags, dev, stream, gdn) if args.prefill else None
+    # (one GPU only: a leg that failed on one rank would leave the others in its collective)
+    prefill_configs, pc_launches = None, 0
+    if args.prefill and not args.no_sweeps and args.workload == "headline" and world == 1:
+        prefill_configs, pc_launches = run_prefill_configs(args, dev, stream, gdn)
 
     launches = (launches_main + (e2e["launches"] if e2e else 0) + (verify["launches"] if verify else 0)
-                + (prefill.get("launches", 0) if prefill else 0) + sweep_launches)
+                + (prefill.get("launches", 0) if prefill else 0) + sweep_launches + pc_launches)
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": lt / args.steps * 1e3, "higher_is_better": True,
@@ -612,6 +641,7 @@ def run_gpu(args, rank, local_rank, world):
         **({"sweeps": dict(sweeps, clocks=sweep_clocks)} if sweeps else {}),
         **({"verify": verify} if verify else {}),
         **({"prefill": prefill} if prefill else {}),
+        **({"prefill_configs": prefill_configs} if prefill_configs else {}),
         "pages_context": PAGES_CONTEXT,
         "gpu_launches": launches,
         "clocks": {k: v for k, v in clocks.summary().items()},
